@@ -1,0 +1,254 @@
+/*
+ * tv.h -- C ABI of the tree-speculative-verification library for gated-DeltaNet hybrids.
+ *
+ * One verify round of a hybrid model (qwen35-tree-spec post, §七 完整验证流程) runs a draft
+ * tree, given by a parents[] array, through two kinds of layers:
+ *
+ *   - gated-DeltaNet (GDN) layers, where every node i gets its own recurrent state
+ *         S_i = alpha_i * S_p @ (I - beta_i k_i k_i^T) + beta_i v_i k_i^T,   o_i = S_i q_i
+ *     evolved from its parent p (the committed state S_0 for a root), either by
+ *     depth-by-depth fork/checkpoint (same post, §四) or by the TreeWY form, which keeps a
+ *     small pseudo-value matrix instead of per-node states (TreeWY: Speculative Verification
+ *     for Gated DeltaNet Hybrids, abstract);
+ *   - full-attention layers, where every node attends to the committed KV prefix plus its
+ *     ancestors plus itself at RoPE position prefix_len + depth (handbook chapter
+ *     投机解码进阶：树形草稿与 EAGLE, §实现, forward_with_mask and tree_mask);
+ *
+ * then commits the accepted path: the GDN state goes back to the last accepted node's state
+ * (qwen35-tree-spec §五 用途 2) and the accepted nodes' KV moves to the contiguous slots after
+ * the prefix (handbook chapter, note after the listing: the KV is reused, not recomputed).
+ *
+ * Conventions for every call below
+ * --------------------------------
+ *  - Pointers are DEVICE pointers owned by the caller, unless a comment says otherwise; the
+ *    library allocates no memory.  Every tensor is dense, row-major (last index fastest) with
+ *    the shape written beside it, and its base address is 16-byte aligned.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *    The return value reports only what the host can see before launch: TV_OK, or
+ *    TV_ERR_INVALID_ARG (null/misaligned pointer, non-positive or inconsistent size),
+ *    TV_ERR_UNSUPPORTED (a size or dtype outside the supported set) or TV_ERR_CUDA (a launch
+ *    failed; tv_last_cuda_error() then holds the CUDA error code).  Nothing is launched when
+ *    the return value is not TV_OK.
+ *  - Data-dependent errors (a malformed tree, a bad accepted path, a block table that is too
+ *    short or points outside the cache) are written per sequence to the device array
+ *    err[B] (0 = that sequence is fine, else a TV_ERR_* code).  A failed sequence's outputs
+ *    are left unwritten; the other sequences are unaffected.  No kernel traps or waits
+ *    without bound.  Read err after synchronising the stream.
+ *  - parents[b][i] is -1 (node i follows the committed state directly: a root) or an
+ *    earlier node index (-1 <= parents[i] < i); anything else is TV_ERR_BAD_TREE.
+ *  - Sizes: 1 <= N <= TV_MAX_NODES nodes per tree, every sequence of a call has N nodes.
+ *  - dtype codes: TV_F32 (fp32) or TV_BF16 (bf16, round-to-nearest-even on store).
+ *    Arithmetic is fp32 throughout.
+ */
+#ifndef TV_H_
+#define TV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TV_API __attribute__((visibility("default")))
+#else
+#define TV_API
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* tv_stream_t; /* same type as cudaStream_t */
+
+enum tv_status {
+  TV_OK = 0,
+  TV_ERR_INVALID_ARG = -1,
+  TV_ERR_BAD_TREE = -2,
+  TV_ERR_BAD_PATH = -3,
+  TV_ERR_UNSUPPORTED = -4,
+  TV_ERR_CUDA = -5,
+  TV_ERR_TIMEOUT = -6,
+  TV_ERR_CAPACITY = -7,     /* block table too short for prefix_len + N slots */
+  TV_ERR_BAD_BLOCK = -8     /* a block-table entry outside [0, num_blocks) */
+};
+
+enum tv_dtype { TV_F32 = 0, TV_BF16 = 1 };
+enum tv_mode { TV_MODE_FORK = 0, TV_MODE_WY = 1 };
+
+#define TV_MAX_NODES 256
+#define TV_BLOCK_SIZE 16
+
+/* Human-readable name of a tv_status code (static string, never NULL). */
+TV_API const char* tv_status_string(int status);
+
+/* CUDA error code (cudaError_t value) of the last call that returned TV_ERR_CUDA on this
+ * host thread, or 0. */
+TV_API int tv_last_cuda_error(void);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+TV_API int tv_version(void);
+
+/* ------------------------------------------------------------------------------------------
+ * tv_tree_prepare -- topology of B draft trees.
+ *
+ * Source: handbook chapter 树形草稿与 EAGLE, §实现, `depths` (depth 0 for a root, parent's
+ * depth + 1 otherwise) and `tree_mask` (node i sees itself and every ancestor).
+ *
+ *   parents   [B, N] int32          in
+ *   depth     [B, N] int32          out: depth of every node
+ *   mask_bits [B, N, W] uint32      out: W = ceil(N / 32); bit (j % 32) of word j / 32 of row
+ *                                   i is 1 iff node j is i or an ancestor of i
+ *   err       [B] int32             out: 0 or TV_ERR_BAD_TREE
+ * Outputs of a sequence whose tree is malformed are unspecified.
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_tree_prepare(const int32_t* parents, int B, int N, int32_t* depth, uint32_t* mask_bits,
+                    int32_t* err, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * tv_gdn_tree_verify_fork -- one GDN layer over B draft trees, fork/checkpoint mode.
+ *
+ * Source: qwen35-tree-spec §四 (Fork/Checkpoint, 逐深度处理): every node evolves from its
+ * parent's snapshot (S_0 for a root) and its own snapshot is kept for the commit step; the
+ * per-node semantics is exactly the root-to-node path replay of the gated delta rule above.
+ * The kernel keeps each node's state in fp32 on chip and walks the tree depth-first, so each
+ * parent state is read from HBM once (S_0) and each node's snapshot is written once.
+ *
+ *   q, k        [B, N, H, dk]  io_dtype      in
+ *   v           [B, N, H, dv]  io_dtype      in
+ *   alpha, beta [B, N, H]      fp32          in  (decay in (0,1], write strength)
+ *   S0          [B, H, dv, dk] state_dtype   in  committed state (row = value index)
+ *   parents     [B, N]         int32         in
+ *   q_scale                                      o_i = S_i (q_scale * q_i)
+ *   out         [B, N, H, dv]  io_dtype      out o_i
+ *   node_states [B, N, H, dv, dk] state_dtype out S_i of every node (the checkpoints)
+ *   err         [B] int32                    out 0 or TV_ERR_BAD_TREE
+ * Supported: dk, dv in {64, 128}; (io, state) in {(F32,F32), (BF16,BF16), (BF16,F32)}.
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_gdn_tree_verify_fork(const void* q, const void* k, const void* v, const float* alpha,
+                            const float* beta, const void* S0, const int32_t* parents, int B,
+                            int N, int H, int dk, int dv, int io_dtype, int state_dtype,
+                            float q_scale, void* out, void* node_states, int32_t* err,
+                            tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * tv_gdn_tree_verify_wy -- one GDN layer over B draft trees, TreeWY mode.
+ *
+ * Source: TreeWY abstract -- all node outputs from one triangular solve over a small
+ * pseudo-value matrix, no per-node states.  Reading of the algebra (not on the page): with
+ * gamma_i the product of alpha along the root-to-node path P(i), Gamma_ij = gamma_i/gamma_j,
+ * and the pseudo-value w_i = beta_i (v_i - alpha_i S_parent k_i),
+ *     S_i = gamma_i S_0 + sum_{j in P(i)} Gamma_ij w_j k_j^T,
+ *     (I + diag(beta)(A o Gamma o K K^T)) W = diag(beta)(V - diag(gamma) K S_0^T),
+ *     O = diag(gamma) (q_scale Q) S_0^T + (M o Gamma o (q_scale Q) K^T) W,
+ * A the strict-ancestor mask, M = A + I the tree mask.  The system is unit lower triangular
+ * because parents[i] < i; it is solved along ancestor lists (each row of A has depth(i)
+ * nonzeros).
+ *
+ *   inputs as tv_gdn_tree_verify_fork
+ *   out         [B, N, H, dv]  io_dtype   out o_i
+ *   pseudo_v    [B, N, H, dv]  fp32       out W (w_i per node and head)
+ *   log_gamma   [B, N, H]      fp32       out log(gamma_i)
+ *   err         [B] int32                 out 0, TV_ERR_BAD_TREE, or TV_ERR_UNSUPPORTED if
+ *                                         the sum over nodes of (depth+1) exceeds 4096
+ * Supported: dk, dv in {64, 128}; (io, state) as for fork.
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_gdn_tree_verify_wy(const void* q, const void* k, const void* v, const float* alpha,
+                          const float* beta, const void* S0, const int32_t* parents, int B,
+                          int N, int H, int dk, int dv, int io_dtype, int state_dtype,
+                          float q_scale, void* out, float* pseudo_v, float* log_gamma,
+                          int32_t* err, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * tv_gdn_commit -- write the accepted node's state back into S_0.
+ *
+ * Source: qwen35-tree-spec §五 用途 2 and §七 Step 4 (restore the state of the last accepted
+ * token, drop the other snapshots); TreeWY abstract (rebuild only the accepted state).
+ * The accepted path of sequence b is accepted_path[b][0 .. accepted_len[b]-1]: path[0] a
+ * root and path[r] a child of path[r-1]; 1 <= accepted_len[b] <= Lmax.
+ *
+ *   mode = TV_MODE_FORK:  S0[b] <- node_states[b, path[L-1]]
+ *   mode = TV_MODE_WY:    S0[b] <- gamma_a S0[b] + sum_r Gamma_{a,path[r]} w_{path[r]} k_{path[r]}^T
+ *                         (a = path[L-1]), from pseudo_v, log_gamma and k of the verify call
+ *
+ *   accepted_path [B, Lmax] int32   in
+ *   accepted_len  [B] int32         in
+ *   parents       [B, N] int32      in  (to check the path)
+ *   node_states   [B,N,H,dv,dk] state_dtype in  (fork mode; may be NULL in WY mode)
+ *   pseudo_v      [B,N,H,dv] fp32, log_gamma [B,N,H] fp32, k [B,N,H,dk] io_dtype
+ *                                   in  (WY mode; may be NULL in fork mode)
+ *   S0            [B,H,dv,dk] state_dtype   in/out
+ *   err           [B] int32         out 0, TV_ERR_BAD_TREE or TV_ERR_BAD_PATH (S0[b] untouched)
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,
+                  const int32_t* parents, const void* node_states, const float* pseudo_v,
+                  const float* log_gamma, const void* k, void* S0, int B, int N, int H, int dk,
+                  int dv, int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * tv_tree_attn -- tree-masked GQA attention over a paged KV prefix.
+ *
+ * Source: handbook chapter 树形草稿与 EAGLE, §实现, forward_with_mask: q and k of the new
+ * nodes are rotated (RoPE) at position prefix_len + depth; keys/values are the cached prefix
+ * followed by the nodes'; node i sees the whole prefix, its ancestors and itself; query head
+ * h reads KV head h / (Hq / Hkv); softmax scale sm_scale (pass 1/sqrt(hd) for the default).
+ * RoPE reading: rotate-half pairs (x_c, x_{c+hd/2}), angle pos * rope_theta^(-2c/hd), over the
+ * full head dim.  Cached prefix keys are stored already rotated.
+ *
+ * The call first writes each node's rotated key and its value into the cache at logical slot
+ * prefix_len[b] + i, then attends over logical slots [0, prefix_len[b] + N).
+ *
+ *   q            [B, N, Hq, hd]  bf16     in  (not rotated)
+ *   k_new, v_new [B, N, Hkv, hd] bf16     in  (k not rotated)
+ *   k_cache, v_cache [num_blocks, Hkv, block_size, hd] bf16  in/out
+ *   block_table  [B, max_blocks] int32    in  logical slot s of sequence b lives in block
+ *                                         block_table[b][s / block_size], row s % block_size
+ *   prefix_len   [B] int32                in
+ *   parents      [B, N] int32             in
+ *   out          [B, N, Hq, hd] bf16      out
+ *   workspace    device scratch of at least tv_tree_attn_workspace_size(...) bytes, 256-byte
+ *                aligned, owned by the caller; contents on entry are ignored.  Calls that
+ *                share a workspace must not overlap in time.
+ *   err          [B] int32                out 0, TV_ERR_BAD_TREE, TV_ERR_CAPACITY
+ *                                         (prefix_len + N > max_blocks * block_size or
+ *                                         prefix_len < 0) or TV_ERR_BAD_BLOCK
+ * Supported: hd in {64, 128, 256}; block_size = 16; Hq a multiple of Hkv; B <= 65535.
+ * ---------------------------------------------------------------------------------------- */
+TV_API size_t tv_tree_attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int max_blocks,
+                                   int block_size);
+
+TV_API int tv_tree_attn(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                 void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
+                 const int32_t* prefix_len, const int32_t* parents, int B, int N, int Hq,
+                 int Hkv, int hd, int block_size, float rope_theta, float sm_scale, void* out,
+                 void* workspace, size_t workspace_bytes, int32_t* err, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * tv_kv_compact -- keep the accepted path's KV, in place.
+ *
+ * Source: handbook chapter 树形草稿与 EAGLE, note after the listing (the accepted nodes' KV
+ * was computed at the right positions during verification and is moved to the sequence's
+ * contiguous slots; rejected slots become void) and qwen35-tree-spec §七 Step 4.
+ * For r < L = accepted_len[b]: logical slot prefix_len[b] + r receives what logical slot
+ * prefix_len[b] + path[r] held before the call (every source is read before any write), for
+ * K and V and all KV heads.  Slots at or past the new length are left as they are.
+ *
+ *   k_cache, v_cache [num_blocks, Hkv, block_size, hd] bf16   in/out
+ *   block_table [B, max_blocks] int32, prefix_len [B] int32, parents [B, N] int32   in
+ *   accepted_path [B, Lmax] int32, accepted_len [B] int32                            in
+ *   slot_map    [B, Lmax] int32   out physical source slot (block * block_size + row) of
+ *                                 each kept entry, -1 for r >= L
+ *   new_len     [B] int32         out prefix_len + L (prefix_len on error)
+ *   err         [B] int32         out 0, TV_ERR_BAD_TREE, TV_ERR_BAD_PATH, TV_ERR_CAPACITY
+ *                                 or TV_ERR_BAD_BLOCK
+ * Supported: hd in {64, 128, 256}; block_size = 16.
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_kv_compact(void* k_cache, void* v_cache, int num_blocks, const int32_t* block_table,
+                  int max_blocks, const int32_t* prefix_len, const int32_t* parents, int N,
+                  const int32_t* accepted_path, const int32_t* accepted_len, int Lmax, int B,
+                  int Hkv, int hd, int block_size, int32_t* slot_map, int32_t* new_len,
+                  int32_t* err, tv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TV_H_ */

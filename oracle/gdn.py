@@ -33,7 +33,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .tree import depths, is_valid_path, path_to
+from .tree import depths, is_valid_path, is_valid_tree, path_to
 
 
 def gdn_step(S: np.ndarray, k: np.ndarray, v: np.ndarray, alpha, beta) -> np.ndarray:
@@ -104,32 +104,35 @@ def verify_by_depth(inp: dict):
     return o, states
 
 
-def pseudo_values(inp: dict, b: int):
-    """TreeWY quantities of sequence b from their definitions (reading stated in the module
-    docstring): ``w [N, H, dv]`` with w_i = beta_i (v_i - alpha_i S_parent k_i), and
-    ``log_gamma [N, H]`` = sum of log(alpha) along the root-to-node path."""
+def pseudo_value_node(inp: dict, b: int, i: int):
+    """TreeWY quantities of node i of sequence b from their definitions (reading stated in the
+    module docstring): ``w_i [H, dv]`` = beta_i (v_i - alpha_i S_parent k_i) and
+    ``log_gamma_i [H]`` = sum of log(alpha) along the root-to-node path."""
     parents = inp["parents"][b]
-    N, H, dk = inp["q"].shape[1:]
-    dv = inp["v"].shape[-1]
-    w = np.zeros((N, H, dv))
-    log_gamma = np.zeros((N, H))
-    for i in range(N):
-        p = int(parents[i])
-        S_parent = inp["S0"][b] if p == -1 else node_state(inp, b, p)[0]
-        Sk = np.matmul(S_parent, inp["k"][b, i][:, :, None])[:, :, 0]
-        a = inp["alpha"][b, i][:, None]
-        w[i] = inp["beta"][b, i][:, None] * (inp["v"][b, i] - a * Sk)
-        log_gamma[i] = sum(np.log(inp["alpha"][b, j]) for j in path_to(parents, i))
+    p = int(parents[i])
+    S_parent = inp["S0"][b] if p == -1 else node_state(inp, b, p)[0]
+    Sk = np.matmul(S_parent, inp["k"][b, i][:, :, None])[:, :, 0]
+    a = inp["alpha"][b, i][:, None]
+    w = inp["beta"][b, i][:, None] * (inp["v"][b, i] - a * Sk)
+    log_gamma = sum(np.log(inp["alpha"][b, j]) for j in path_to(parents, i))
     return w, log_gamma
+
+
+def pseudo_values(inp: dict, b: int):
+    """``w [N, H, dv]`` and ``log_gamma [N, H]`` of every node of sequence b."""
+    N = inp["q"].shape[1]
+    pairs = [pseudo_value_node(inp, b, i) for i in range(N)]
+    return np.stack([w for w, _ in pairs]), np.stack([lg for _, lg in pairs])
 
 
 def commit(inp: dict, path: np.ndarray, path_len: np.ndarray) -> np.ndarray:
     """Committed state ``[B,H,dv,dk]`` after acceptance: the state of the last accepted node
-    (qwen35-tree-spec §五 用途 2).  A sequence whose path is not a root-to-node path keeps S_0."""
+    (qwen35-tree-spec §五 用途 2).  A sequence whose tree is malformed or whose path is not a
+    root-to-node path keeps S_0."""
     out = inp["S0"].copy()
     for b in range(out.shape[0]):
         L = int(path_len[b])
-        if not is_valid_path(inp["parents"][b], path[b], L):
+        if not (is_valid_tree(inp["parents"][b]) and is_valid_path(inp["parents"][b], path[b], L)):
             continue
         out[b] = node_state(inp, b, int(path[b][L - 1]))[0]
     return out

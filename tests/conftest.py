@@ -12,6 +12,10 @@ GOLDEN = os.path.join(ROOT, "tests", "golden")
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    # The CUDA library is built in-tree (incrementally) before any test module imports the
+    # binding; a failed build fails the session loudly.
+    import __graft_entry__
+    __graft_entry__.build()
 
 
 def read_golden(name: str) -> list[str]:

@@ -1,0 +1,115 @@
+"""The C-ABI library loads and exports every symbol ``include/tv.h`` declares; host-side
+argument checks reject bad calls before any device work (CPU only: no call here reaches the
+GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import tree_speculative_verification_gdn_gb300 as tv
+
+# These tests pass host addresses where device pointers belong and rely on the host-side checks
+# rejecting the call first; they never run where a GPU could receive such a pointer.
+cpu_only = pytest.mark.skipif(torch.cuda.is_available(), reason="host-address stand-ins; CPU only")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "tv.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"TV_API\s+[\w\s\*]*?\b(tv_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported_and_bound():
+    names = _declared()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(tv.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in tv.EXPORTED, name
+    assert sorted(tv.EXPORTED) == names
+
+
+def test_enum_values_match_header():
+    with open(os.path.join(ROOT, "include", "tv.h")) as f:
+        text = f.read()
+    for name in ("TV_OK", "TV_ERR_INVALID_ARG", "TV_ERR_BAD_TREE", "TV_ERR_BAD_PATH", "TV_ERR_UNSUPPORTED",
+                 "TV_ERR_CUDA", "TV_ERR_TIMEOUT", "TV_ERR_CAPACITY", "TV_ERR_BAD_BLOCK", "TV_F32", "TV_BF16",
+                 "TV_MODE_FORK", "TV_MODE_WY"):
+        m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
+        assert m and int(m.group(1)) == getattr(tv, name), name
+    for name in ("TV_MAX_NODES", "TV_BLOCK_SIZE"):
+        m = re.search(rf"#define\s+{name}\s+(\d+)", text)
+        assert m and int(m.group(1)) == getattr(tv, name)
+
+
+def test_status_strings_and_version():
+    assert tv.status_string(0) == "ok"
+    for code in range(-8, 0):
+        assert tv.status_string(code) and tv.status_string(code) != "unknown status"
+    assert tv.status_string(99) == "unknown status"
+    assert tv.lib.tv_version() >= 100
+
+
+def test_null_pointers_are_rejected_before_launch():
+    L = tv.lib
+    assert L.tv_tree_prepare(None, 1, 4, None, None, None, None) == tv.TV_ERR_INVALID_ARG
+    args = [None] * 7 + [1, 7, 2, 64, 64, tv.TV_F32, tv.TV_F32, 1.0, None, None, None, None]
+    assert L.tv_gdn_tree_verify_fork(*args) == tv.TV_ERR_INVALID_ARG
+    args = [None] * 7 + [1, 7, 2, 64, 64, tv.TV_F32, tv.TV_F32, 1.0, None, None, None, None, None]
+    assert L.tv_gdn_tree_verify_wy(*args) == tv.TV_ERR_INVALID_ARG
+    assert L.tv_gdn_commit(tv.TV_MODE_FORK, None, None, 3, None, None, None, None, None, None, 1, 7, 2, 64,
+                           64, 0, 0, None, None) == tv.TV_ERR_INVALID_ARG
+
+
+def _fake(n=1 << 20):
+    """A 256-byte-aligned host address standing in for a device pointer; the checks below fail
+    on sizes before anything dereferences it."""
+    buf = ctypes.create_string_buffer(n + 256)
+    addr = (ctypes.addressof(buf) + 255) & ~255
+    return buf, ctypes.c_void_p(addr)
+
+
+@cpu_only
+@pytest.mark.parametrize("dk,dv,io,st,want", [
+    (96, 64, 0, 0, tv.TV_ERR_UNSUPPORTED),
+    (64, 32, 0, 0, tv.TV_ERR_UNSUPPORTED),
+    (64, 64, 0, 1, tv.TV_ERR_UNSUPPORTED),   # fp32 I/O with a bf16 state has no kernel
+    (64, 64, 5, 0, tv.TV_ERR_INVALID_ARG),
+])
+def test_unsupported_sizes_and_dtypes(dk, dv, io, st, want):
+    keep, p = _fake()
+    args = [p] * 7 + [1, 7, 2, dk, dv, io, st, 1.0, p, p, p, None]
+    assert tv.lib.tv_gdn_tree_verify_fork(*args) == want
+    del keep
+
+
+@cpu_only
+def test_size_limits():
+    keep, p = _fake()
+    args = [p] * 7 + [1, 257, 2, 64, 64, 0, 0, 1.0, p, p, p, None]
+    assert tv.lib.tv_gdn_tree_verify_fork(*args) == tv.TV_ERR_UNSUPPORTED
+    args = [p] * 7 + [0, 7, 2, 64, 64, 0, 0, 1.0, p, p, p, None]
+    assert tv.lib.tv_gdn_tree_verify_fork(*args) == tv.TV_ERR_INVALID_ARG
+    # misaligned q
+    q = ctypes.c_void_p(p.value + 4)
+    args = [q] + [p] * 6 + [1, 7, 2, 64, 64, 0, 0, 1.0, p, p, p, None]
+    assert tv.lib.tv_gdn_tree_verify_fork(*args) == tv.TV_ERR_INVALID_ARG
+    # attention: unsupported head dim / block size, Hq not a multiple of Hkv
+    a = [p] * 5 + [4, p, 2, p, p, 1, 3, 4, 2, 96, 16, 1e6, 0.1, p, p, 1 << 20, p, None]
+    assert tv.lib.tv_tree_attn(*a) == tv.TV_ERR_UNSUPPORTED
+    a = [p] * 5 + [4, p, 2, p, p, 1, 3, 4, 2, 64, 32, 1e6, 0.1, p, p, 1 << 20, p, None]
+    assert tv.lib.tv_tree_attn(*a) == tv.TV_ERR_UNSUPPORTED
+    a = [p] * 5 + [4, p, 2, p, p, 1, 3, 3, 2, 64, 16, 1e6, 0.1, p, p, 1 << 20, p, None]
+    assert tv.lib.tv_tree_attn(*a) == tv.TV_ERR_INVALID_ARG
+    del keep
+
+
+def test_workspace_size_is_host_only_and_monotone():
+    s1 = tv.tv_tree_attn_workspace_size(1, 15, 16, 4, 128, 258)
+    s2 = tv.tv_tree_attn_workspace_size(32, 40, 16, 4, 256, 2053)
+    assert 0 < s1 < s2
+    assert tv.tv_tree_attn_workspace_size(1, 15, 16, 3, 128, 258) == 0   # Hq % Hkv != 0

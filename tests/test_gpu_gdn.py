@@ -1,0 +1,238 @@
+"""GPU vs fp64 oracle: GDN tree verify (fork and TreeWY modes) and commit, through the C ABI.
+
+Small cases are compared element by element over every output; the full-size config-2 and
+config-4 cases (the launch configuration the benchmark times) are compared on sampled
+(sequence, node) outputs the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import tree_speculative_verification_gdn_gb300 as tv
+import workloads as W
+from oracle import gdn as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _caterpillar(n):
+    """Spine nodes each with one leaf and one spine child: every spine node branches."""
+    parents, spine = [-1], 0
+    while len(parents) < n:
+        parents.append(spine)           # leaf
+        if len(parents) < n:
+            parents.append(spine)       # next spine node
+            spine = len(parents) - 1
+    return parents
+
+
+def _forest(n, rng):
+    """Several roots (children of the committed state) with random subtrees."""
+    parents = []
+    for i in range(n):
+        parents.append(-1 if i == 0 or rng.random() < 0.2 else int(rng.integers(0, i)))
+    return parents
+
+
+def _check_all(case, modes=("fork", "wy")):
+    io = case.io
+    inp = case.oracle_inputs()
+    o_ref, S_ref = G.verify(inp)
+    res = {}
+    if "fork" in modes:
+        f = _gpu.run_fork(case)
+        assert (f["err"] == 0).all()
+        _gpu.assert_close(f["out"], o_ref, io, "fork o")
+        _gpu.assert_close(f["states"], S_ref, io if case.state == io else "bf16", "fork states")
+        res["fork"] = f
+    if "wy" in modes:
+        w = _gpu.run_wy(case)
+        assert (w["err"] == 0).all()
+        _gpu.assert_close(w["out"], o_ref, io, "wy o")
+        for b in range(case.q.shape[0]):
+            w_ref, lg_ref = G.pseudo_values(inp, b)
+            _gpu.assert_close(w["pseudo_v"][b], w_ref, io, f"wy pseudo-values b={b}")
+            _gpu.assert_close(w["log_gamma"][b], lg_ref, io, f"wy log-gamma b={b}")
+        res["wy"] = w
+    commit_ref = G.commit(inp, case.path.numpy(), case.path_len.numpy())
+    for mode, r in res.items():
+        S0 = _gpu.run_commit(case, mode, r)
+        assert (r["commit_err"] == 0).all()
+        _gpu.assert_close(S0, commit_ref, io if case.state == io else "bf16", f"{mode} commit")
+    return res
+
+
+def test_config0_fp32():
+    _check_all(W.cfg0())
+
+
+@pytest.mark.parametrize("tree", ["chain", "tree"])
+def test_config1_bf16(tree):
+    _check_all(W.cfg1_gdn(tree))
+
+
+@pytest.mark.parametrize("io,state", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32")])
+@pytest.mark.parametrize("d", [64, 128])
+def test_small_random_trees(io, state, d):
+    rng = np.random.default_rng(d + len(io))
+    trees = [W.random_tree(33, rng) for _ in range(3)]
+    _check_all(W.gdn_case(trees, H=2, dk=d, dv=d, io=io, state=state, seed=d))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_tiny_trees(n):
+    trees = [W.chain(n), [-1] * n]
+    _check_all(W.gdn_case(trees, H=3, dk=64, dv=64, io="f32", state="f32", seed=n))
+
+
+def test_mixed_dims():
+    rng = np.random.default_rng(7)
+    trees = [W.random_tree(20, rng) for _ in range(2)]
+    _check_all(W.gdn_case(trees, H=2, dk=128, dv=64, io="f32", state="f32", seed=3))
+    _check_all(W.gdn_case(trees, H=2, dk=64, dv=128, io="bf16", state="bf16", seed=4))
+
+
+def test_stack_stress_shapes():
+    """Caterpillar (every spine node branches), complete binary tree of depth 7 (deepest light
+    nesting for 255 nodes), forest, deep chain."""
+    rng = np.random.default_rng(11)
+    trees = [_caterpillar(64), W.full_tree(2, 5)[:63] + [0], _forest(64, rng), W.chain(64)]
+    _check_all(W.gdn_case(trees, H=1, dk=64, dv=64, io="f32", state="f32", seed=5))
+
+
+def test_max_nodes_complete_binary():
+    trees = [W.full_tree(2, 7) + [0]]  # 255 + 1 = 256 nodes, depth 7
+    case = W.gdn_case(trees, H=1, dk=64, dv=64, io="f32", state="f32", seed=6)
+    inp = case.oracle_inputs()
+    f = _gpu.run_fork(case)
+    w = _gpu.run_wy(case)
+    assert int(f["err"][0]) == 0 and int(w["err"][0]) == 0
+    rng = np.random.default_rng(0)
+    for i in list(rng.choice(256, 24, replace=False)) + [255, 254, 127]:
+        S, o = G.node_state(inp, 0, int(i))
+        _gpu.assert_close(f["states"][0, i], S, "f32", f"fork state {i}")
+        _gpu.assert_close(f["out"][0, i], o, "f32", f"fork o {i}")
+        _gpu.assert_close(w["out"][0, i], o, "f32", f"wy o {i}")
+
+
+def test_fork_and_wy_agree_and_commits_agree():
+    rng = np.random.default_rng(21)
+    trees = [W.random_tree(40, rng) for _ in range(4)]
+    case = W.gdn_case(trees, H=4, dk=128, dv=128, io="bf16", state="f32", seed=8)
+    f = _gpu.run_fork(case)
+    w = _gpu.run_wy(case)
+    o_f, o_w = W.f64(f["out"]), W.f64(w["out"])
+    _gpu.assert_close(o_w, o_f, "bf16", "wy vs fork")
+    S_f = _gpu.run_commit(case, "fork", f)
+    S_w = _gpu.run_commit(case, "wy", w)
+    _gpu.assert_close(S_w, W.f64(S_f), "bf16", "wy commit vs fork commit")
+
+
+def _sampled_check(case, n_seq, n_nodes, seed):
+    inp = case.oracle_inputs()
+    B, N = case.q.shape[:2]
+    io = case.io
+    f = _gpu.run_fork(case)
+    w = _gpu.run_wy(case)
+    assert (f["err"] == 0).all() and (w["err"] == 0).all()
+    rng = np.random.default_rng(seed)
+    seqs = sorted(set([0, B - 1] + list(rng.choice(B, n_seq, replace=False))))
+    S_got, S_ref, o_got_f, o_got_w, o_ref = [], [], [], [], []
+    for b in seqs:
+        for i in sorted(set([0, N - 1] + list(rng.choice(N, n_nodes, replace=False)))):
+            S, o = G.node_state(inp, b, int(i))
+            S_ref.append(S); o_ref.append(o)
+            S_got.append(W.f64(f["states"][b, i])); o_got_f.append(W.f64(f["out"][b, i]))
+            o_got_w.append(W.f64(w["out"][b, i]))
+    _gpu.assert_close(np.stack(S_got), np.stack(S_ref), io, "fork states (sampled)")
+    _gpu.assert_close(np.stack(o_got_f), np.stack(o_ref), io, "fork o (sampled)")
+    _gpu.assert_close(np.stack(o_got_w), np.stack(o_ref), io, "wy o (sampled)")
+    pv_got, pv_ref, lg_got, lg_ref = [], [], [], []
+    for b in seqs[:2]:
+        for i in sorted(set([0, N - 1] + list(rng.choice(N, n_nodes, replace=False)))):
+            wr, lr = G.pseudo_value_node(inp, b, int(i))
+            pv_ref.append(wr); lg_ref.append(lr)
+            pv_got.append(W.f64(w["pseudo_v"][b, i])); lg_got.append(W.f64(w["log_gamma"][b, i]))
+    _gpu.assert_close(np.stack(pv_got), np.stack(pv_ref), io, "wy pseudo-values (sampled)")
+    _gpu.assert_close(np.stack(lg_got), np.stack(lg_ref), io, "wy log-gamma (sampled)")
+    commit_ref = {bb: G.node_state(inp, bb, int(case.path[bb, int(case.path_len[bb]) - 1]))[0]
+                  for bb in seqs[:3]}
+    for mode, r in (("fork", f), ("wy", w)):
+        S0 = _gpu.run_commit(case, mode, r)
+        assert (r["commit_err"] == 0).all()
+        for bb, ref in commit_ref.items():
+            _gpu.assert_close(S0[bb], ref, io, f"{mode} commit b={bb}")
+    # fork and WY agree on every output, not only the sampled ones
+    _gpu.assert_close(w["out"], W.f64(f["out"]), io, "wy vs fork, all outputs")
+
+
+def test_config2_full_size_sampled():
+    """One config-2 layer at its full size: B=64, N=40 (k=3 d=3), H=16, d=128, bf16."""
+    _sampled_check(W.cfg2_layer(layer=0), n_seq=3, n_nodes=5, seed=2)
+
+
+@pytest.mark.parametrize("N,B", [(15, 8), (64, 8), (256, 4)])
+def test_config4_trees_sampled(N, B):
+    _sampled_check(W.cfg4_gdn_layer(N, B), n_seq=2, n_nodes=4, seed=N)
+
+
+def test_malformed_tree_only_fails_its_sequence():
+    rng = np.random.default_rng(3)
+    trees = [W.random_tree(12, rng) for _ in range(3)]
+    case = W.gdn_case(trees, H=2, dk=64, dv=64, io="f32", state="f32", seed=9)
+    case.parents[1, 5] = 7          # a later node: not allowed
+    inp = case.oracle_inputs()
+    for run in (_gpu.run_fork, _gpu.run_wy):
+        r = run(case)
+        assert r["err"].tolist() == [0, tv.TV_ERR_BAD_TREE, 0]
+        for b in (0, 2):
+            for i in range(12):
+                _, o = G.node_state(inp, b, i)
+                _gpu.assert_close(r["out"][b, i], o, "f32", f"healthy sequence {b}")
+        assert torch.isnan(r["out"][1]).all()     # the failed sequence is left unwritten
+
+
+def test_wy_path_capacity_is_reported():
+    case = W.gdn_case([W.chain(256)], H=1, dk=64, dv=64, io="f32", state="f32", seed=1)
+    r = _gpu.run_wy(case)
+    assert int(r["err"][0]) == tv.TV_ERR_UNSUPPORTED
+    f = _gpu.run_fork(case)   # fork mode has no such limit
+    assert int(f["err"][0]) == 0
+    inp = case.oracle_inputs()
+    S, o = G.node_state(inp, 0, 255)
+    _gpu.assert_close(f["states"][0, 255], S, "f32", "deep chain fork state")
+
+
+def test_commit_rejects_bad_paths_and_leaves_state():
+    tree = [-1, 0, 0, 1, 1, 2, 2]
+    case = W.gdn_case([tree] * 4, H=2, dk=64, dv=64, io="f32", state="f32", seed=2,
+                      paths=[[0, 2, 6], [0, 3], [1, 3], [0]])
+    path = case.path.clone()
+    L = case.path_len.clone()
+    L[3] = 0                                   # empty path
+    inp = case.oracle_inputs()
+    for mode, run in (("fork", _gpu.run_fork), ("wy", _gpu.run_wy)):
+        r = run(case)
+        S0 = _gpu.run_commit(case, mode, r, path=path, path_len=L)
+        assert r["commit_err"].tolist() == [0, tv.TV_ERR_BAD_PATH, tv.TV_ERR_BAD_PATH, tv.TV_ERR_BAD_PATH]
+        _gpu.assert_close(S0[0], G.node_state(inp, 0, 6)[0], "f32", f"{mode} good commit")
+        for b in (1, 2, 3):
+            assert torch.equal(S0[b], case.S0[b])
+
+
+def test_host_side_argument_errors():
+    case = W.cfg0()
+    x = _gpu.gdn_inputs(case)
+    out = torch.empty_like(x["v"])
+    st = torch.empty((1, 7, 2, 64, 64), device="cuda")
+    err = torch.empty(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(tv.TVError) as e:
+        tv.tv_gdn_tree_verify_fork(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], x["parents"],
+                                   out, st, err, q_scale=float("nan"))
+    assert e.value.status == tv.TV_ERR_INVALID_ARG
+    q96 = torch.zeros((1, 7, 2, 96), device="cuda")
+    with pytest.raises(tv.TVError) as e:
+        tv.tv_gdn_tree_verify_fork(q96, q96, x["v"], x["alpha"], x["beta"], x["S0"], x["parents"], out, st,
+                                   err)
+    assert e.value.status == tv.TV_ERR_UNSUPPORTED

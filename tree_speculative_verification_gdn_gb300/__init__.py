@@ -1,0 +1,181 @@
+"""Python binding of the CUDA library ``_lib/libtv.so`` (argument marshalling only).
+
+Every function has the name of the C entry point it calls (``include/tv.h``), takes torch
+tensors that live on the GPU, and passes their data pointers, sizes and dtype codes.  All of
+the work runs in the library's kernels; there is no CPU fallback.  Importing this package
+raises ``ImportError`` when the library has not been built
+(``python tree_speculative_verification_gdn_gb300/_build.py``).
+
+Non-OK return codes raise :class:`TVError`.  Per-sequence, data-dependent errors land in the
+caller's ``err`` tensor (read it after synchronising).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libtv.so")
+
+# Status codes and enums of include/tv.h.
+TV_OK = 0
+TV_ERR_INVALID_ARG = -1
+TV_ERR_BAD_TREE = -2
+TV_ERR_BAD_PATH = -3
+TV_ERR_UNSUPPORTED = -4
+TV_ERR_CUDA = -5
+TV_ERR_TIMEOUT = -6
+TV_ERR_CAPACITY = -7
+TV_ERR_BAD_BLOCK = -8
+TV_F32 = 0
+TV_BF16 = 1
+TV_MODE_FORK = 0
+TV_MODE_WY = 1
+TV_MAX_NODES = 256
+TV_BLOCK_SIZE = 16
+
+EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_prepare",
+            "tv_gdn_tree_verify_fork", "tv_gdn_tree_verify_wy", "tv_gdn_commit",
+            "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_kv_compact")
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_Z = ctypes.c_size_t
+
+_SIGNATURES = {
+    "tv_status_string": (ctypes.c_char_p, [_I]),
+    "tv_last_cuda_error": (_I, []),
+    "tv_version": (_I, []),
+    "tv_tree_prepare": (_I, [_P, _I, _I, _P, _P, _P, _P]),
+    "tv_gdn_tree_verify_fork": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "tv_gdn_tree_verify_wy": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "tv_gdn_commit": (_I, [_I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "tv_tree_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "tv_tree_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _P, _P, _Z,
+                          _P, _P]),
+    "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+}
+
+
+class TVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib.tv_status_string(status).decode()
+        if status == TV_ERR_CUDA:
+            msg += f" (cudaError {lib.tv_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{status}]")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first with "
+                          "python tree_speculative_verification_gdn_gb300/_build.py or "
+                          "__graft_entry__.build()")
+    handle = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
+lib = _load()
+
+_DTYPES = {torch.float32: TV_F32, torch.bfloat16: TV_BF16}
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not (t.is_cuda and t.is_contiguous()):
+        raise ValueError("tensors passed to the library must be contiguous CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != TV_OK:
+        raise TVError(status, where)
+
+
+def status_string(status: int) -> str:
+    return lib.tv_status_string(status).decode()
+
+
+def tv_tree_prepare(parents, depth, mask_bits, err, stream=None) -> None:
+    """parents [B,N] int32 -> depth [B,N] int32, mask_bits [B,N,ceil(N/32)] int32 (bit pattern
+    of uint32 words), err [B] int32."""
+    B, N = parents.shape
+    _check(lib.tv_tree_prepare(_ptr(parents), B, N, _ptr(depth), _ptr(mask_bits), _ptr(err),
+                               _stream(stream)), "tv_tree_prepare")
+
+
+def tv_gdn_tree_verify_fork(q, k, v, alpha, beta, S0, parents, out, node_states, err,
+                            q_scale: float = 1.0, stream=None) -> None:
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(lib.tv_gdn_tree_verify_fork(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(parents), B, N, H, dk, dv,
+        _DTYPES[q.dtype], _DTYPES[S0.dtype], float(q_scale), _ptr(out), _ptr(node_states), _ptr(err),
+        _stream(stream)), "tv_gdn_tree_verify_fork")
+
+
+def tv_gdn_tree_verify_wy(q, k, v, alpha, beta, S0, parents, out, pseudo_v, log_gamma, err,
+                          q_scale: float = 1.0, stream=None) -> None:
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(lib.tv_gdn_tree_verify_wy(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(parents), B, N, H, dk, dv,
+        _DTYPES[q.dtype], _DTYPES[S0.dtype], float(q_scale), _ptr(out), _ptr(pseudo_v), _ptr(log_gamma),
+        _ptr(err), _stream(stream)), "tv_gdn_tree_verify_wy")
+
+
+def tv_gdn_commit(mode: int, accepted_path, accepted_len, parents, S0, err, *, node_states=None,
+                  pseudo_v=None, log_gamma=None, k=None, io_dtype=None, N=None, stream=None) -> None:
+    """Fork mode reads ``node_states``; WY mode reads ``pseudo_v``, ``log_gamma`` and ``k``."""
+    B, H, dv, dk = S0.shape
+    Lmax = accepted_path.shape[1]
+    N = parents.shape[1] if N is None else N
+    io = _DTYPES[k.dtype] if k is not None else (_DTYPES[io_dtype] if io_dtype is not None else
+                                                  _DTYPES[S0.dtype])
+    _check(lib.tv_gdn_commit(
+        int(mode), _ptr(accepted_path), _ptr(accepted_len), Lmax, _ptr(parents), _ptr(node_states),
+        _ptr(pseudo_v), _ptr(log_gamma), _ptr(k), _ptr(S0), B, N, H, dk, dv, io, _DTYPES[S0.dtype],
+        _ptr(err), _stream(stream)), "tv_gdn_commit")
+
+
+def tv_tree_attn_workspace_size(B, N, Hq, Hkv, hd, max_blocks, block_size=TV_BLOCK_SIZE) -> int:
+    return int(lib.tv_tree_attn_workspace_size(B, N, Hq, Hkv, hd, max_blocks, block_size))
+
+
+def tv_tree_attn(q, k_new, v_new, k_cache, v_cache, block_table, prefix_len, parents, out,
+                 workspace, err, rope_theta: float, sm_scale: float | None = None, stream=None) -> None:
+    B, N, Hq, hd = q.shape
+    Hkv = k_new.shape[2]
+    num_blocks, _, bs, _ = k_cache.shape
+    max_blocks = block_table.shape[1]
+    scale = hd ** -0.5 if sm_scale is None else sm_scale
+    _check(lib.tv_tree_attn(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table),
+        max_blocks, _ptr(prefix_len), _ptr(parents), B, N, Hq, Hkv, hd, bs, float(rope_theta), float(scale),
+        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
+        _stream(stream)), "tv_tree_attn")
+
+
+def tv_kv_compact(k_cache, v_cache, block_table, prefix_len, parents, accepted_path, accepted_len,
+                  slot_map, new_len, err, stream=None) -> None:
+    num_blocks, Hkv, bs, hd = k_cache.shape
+    B, max_blocks = block_table.shape
+    N = parents.shape[1]
+    Lmax = accepted_path.shape[1]
+    _check(lib.tv_kv_compact(
+        _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table), max_blocks, _ptr(prefix_len),
+        _ptr(parents), N, _ptr(accepted_path), _ptr(accepted_len), Lmax, B, Hkv, hd, bs, _ptr(slot_map),
+        _ptr(new_len), _ptr(err), _stream(stream)), "tv_kv_compact")

@@ -1,0 +1,292 @@
+// Tree-masked GQA attention over a paged KV prefix (handbook chapter 树形草稿与 EAGLE, §实现,
+// forward_with_mask / tree_mask; positions prefix_len + depth from the chapter's summary).
+//
+// Four launches on the caller's stream:
+//   1. check   -- per sequence: tree, capacity (prefix_len + N slots in the block table) and
+//                 every block-table entry the call touches; err[b] is final after it.
+//   2. rope    -- per node: rotate q (into the workspace, bf16) and k at prefix_len + depth,
+//                 write rotated k and v into the node's cache slot prefix_len + i.
+//   3. partial -- split-KV: each CTA takes one (sequence, KV head, key chunk, 32 query rows)
+//                 and runs an online softmax over its chunk of logical slots, masking the node
+//                 slots with the tree mask; writes (max, sum, unnormalised output) per row.
+//   4. combine -- merges the chunks of every (sequence, node, query head).
+// Query rows of one KV head are (node, group member) pairs, so K/V of a chunk is shared by
+// every query head of the group.
+#include "tv_common.cuh"
+#include "tv_internal.h"
+
+namespace tv {
+namespace {
+
+constexpr int kRowsPerCta = 32;
+constexpr int kPartialThreads = 256;  // 8 warps x 4 rows
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnPlan {
+  int chunk, nsplit, R, RG;
+  size_t off_qrot, off_ml, off_acc, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+AttnPlan plan_attn(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int bs) {
+  AttnPlan p;
+  const long long slots = (long long)max_blocks * bs;
+  const long long work = (long long)B * Hkv * slots;
+  long long chunk = (work + 2047) / 2048;        // ~2048 (sequence, KV head, chunk) items
+  chunk = (chunk + 127) / 128 * 128;
+  if (chunk < 128) chunk = 128;
+  if (chunk > 8192) chunk = 8192;
+  p.chunk = (int)chunk;
+  p.nsplit = (int)((slots + chunk - 1) / chunk);
+  p.R = (Hq / Hkv) * N;
+  p.RG = (p.R + kRowsPerCta - 1) / kRowsPerCta;
+  p.off_qrot = 0;
+  p.off_ml = align256((size_t)B * N * Hq * hd * sizeof(bf16));
+  p.off_acc = p.off_ml + align256((size_t)B * Hkv * p.nsplit * p.R * 2 * sizeof(float));
+  p.total = p.off_acc + align256((size_t)B * Hkv * p.nsplit * p.R * hd * sizeof(float));
+  return p;
+}
+
+__global__ void attn_check_kernel(AttnArgs a) {
+  __shared__ int par[TV_MAX_NODES];
+  __shared__ int flag, bad_block;
+  const int b = blockIdx.x;
+  int st = load_and_check_tree(a.parents + (size_t)b * a.N, a.N, par, &flag);
+  if (!st) {
+    const int P = a.prefix_len[b];
+    if (P < 0 || (long long)P + a.N > (long long)a.max_blocks * a.block_size) st = TV_ERR_CAPACITY;
+  }
+  if (!st) {
+    if (threadIdx.x == 0) bad_block = 0;
+    __syncthreads();
+    const int nblk = (a.prefix_len[b] + a.N + a.block_size - 1) / a.block_size;
+    for (int lb = threadIdx.x; lb < nblk; lb += blockDim.x) {
+      const int blk = a.block_table[(size_t)b * a.max_blocks + lb];
+      if (blk < 0 || blk >= a.num_blocks) bad_block = 1;
+    }
+    __syncthreads();
+    if (bad_block) st = TV_ERR_BAD_BLOCK;
+  }
+  if (threadIdx.x == 0) a.err[b] = st;
+}
+
+// One CTA per (sequence, node).
+__global__ void attn_rope_kernel(AttnArgs a, bf16* __restrict__ qrot) {
+  const int b = blockIdx.x / a.N, i = blockIdx.x % a.N;
+  if (a.err[b]) return;
+  const int32_t* par = a.parents + (size_t)b * a.N;
+  int depth = 0;
+  for (int j = par[i]; j >= 0; j = par[j]) ++depth;
+  const int P = a.prefix_len[b];
+  const long long pos = (long long)P + depth;
+  const int hd = a.hd, half = hd / 2, bs = a.block_size;
+  const int slot = P + i;
+  const int blk = a.block_table[(size_t)b * a.max_blocks + slot / bs];
+  const bf16* q = static_cast<const bf16*>(a.q) + ((size_t)b * a.N + i) * a.Hq * hd;
+  const bf16* kn = static_cast<const bf16*>(a.k_new) + ((size_t)b * a.N + i) * a.Hkv * hd;
+  const bf16* vn = static_cast<const bf16*>(a.v_new) + ((size_t)b * a.N + i) * a.Hkv * hd;
+  bf16* qo = qrot + ((size_t)b * a.N + i) * a.Hq * hd;
+  bf16* kc = static_cast<bf16*>(a.k_cache);
+  bf16* vc = static_cast<bf16*>(a.v_cache);
+  const double two_pi = 6.283185307179586;
+  for (int c = threadIdx.x; c < half; c += blockDim.x) {
+    // Angle in fp64, reduced to [-pi, pi] before the fp32 sin/cos: positions reach ~33K.
+    const double inv = pow((double)a.rope_theta, -2.0 * c / hd);
+    const double ang = (double)pos * inv;
+    const float red = (float)(ang - two_pi * rint(ang / two_pi));
+    float sn, cs;
+    sincosf(red, &sn, &cs);
+    for (int h = 0; h < a.Hq; ++h) {
+      const float x1 = to_f32(q[h * hd + c]), x2 = to_f32(q[h * hd + c + half]);
+      qo[h * hd + c] = from_f32<bf16>(x1 * cs - x2 * sn);
+      qo[h * hd + c + half] = from_f32<bf16>(x2 * cs + x1 * sn);
+    }
+    for (int g = 0; g < a.Hkv; ++g) {
+      const float x1 = to_f32(kn[g * hd + c]), x2 = to_f32(kn[g * hd + c + half]);
+      const size_t row = (((size_t)blk * a.Hkv + g) * bs + slot % bs) * hd;
+      kc[row + c] = from_f32<bf16>(x1 * cs - x2 * sn);
+      kc[row + c + half] = from_f32<bf16>(x2 * cs + x1 * sn);
+      vc[row + c] = vn[g * hd + c];
+      vc[row + c + half] = vn[g * hd + c + half];
+    }
+  }
+}
+
+// Split-KV partial attention on CUDA cores.  grid.x = nsplit * Hkv * RG, grid.y = B.
+template <int HD>
+__global__ void __launch_bounds__(kPartialThreads) attn_partial_simt_kernel(AttnArgs a, const bf16* __restrict__ qrot,
+                                                                            float* __restrict__ ml,
+                                                                            float* __restrict__ acc, int chunk,
+                                                                            int nsplit, int RG) {
+  constexpr int DPL = HD / 32;  // head dims per lane
+  __shared__ __align__(16) bf16 Ks[16][HD];
+  __shared__ __align__(16) bf16 Vs[16][HD];
+  __shared__ uint32_t maskw[kRowsPerCta][TV_MAX_NODES / 32];
+  __shared__ int par[TV_MAX_NODES];
+
+  const int b = blockIdx.y;
+  const int split = blockIdx.x % nsplit;
+  const int rest = blockIdx.x / nsplit;
+  const int kvh = rest % a.Hkv, rg = rest / a.Hkv;
+  if (a.err[b]) return;
+  const int N = a.N, P = a.prefix_len[b], total = P + N;
+  const int lo = split * chunk;
+  if (lo >= total) return;
+  const int hi = min(total, lo + chunk);
+  const int G = a.Hq / a.Hkv, R = G * N, W = (N + 31) / 32;
+
+  for (int x = threadIdx.x; x < N; x += blockDim.x) par[x] = a.parents[(size_t)b * N + x];
+  __syncthreads();
+  for (int x = threadIdx.x; x < kRowsPerCta * W; x += blockDim.x) {
+    const int rr = rg * kRowsPerCta + x / W, w = x % W;
+    uint32_t bits = 0;
+    if (rr < R)
+      for (int j = rr / G; j >= 0; j = par[j])
+        if ((j >> 5) == w) bits |= 1u << (j & 31);
+    maskw[x / W][w] = bits;
+  }
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const float scale = a.sm_scale * kLog2e;
+  float qv[4][DPL], o[4][DPL], m[4], l[4];
+  bool active[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int rr = rg * kRowsPerCta + warp * 4 + j;
+    active[j] = rr < R;
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+    const int node = active[j] ? rr / G : 0, h = kvh * G + (active[j] ? rr % G : 0);
+    const bf16* qp = qrot + (((size_t)b * N + node) * a.Hq + h) * HD + lane * DPL;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) {
+      qv[j][d] = active[j] ? to_f32(qp[d]) : 0.f;
+      o[j][d] = 0.f;
+    }
+  }
+  const bf16* kc = static_cast<const bf16*>(a.k_cache);
+  const bf16* vc = static_cast<const bf16*>(a.v_cache);
+  const int* table = a.block_table + (size_t)b * a.max_blocks;
+  constexpr int VPB = 16 * HD / 8;  // 16-byte vectors per block tile
+  for (int s0 = lo; s0 < hi; s0 += 16) {
+    __syncthreads();
+    const int blk = table[s0 / 16];
+    const uint4* ksrc = reinterpret_cast<const uint4*>(kc + ((size_t)blk * a.Hkv + kvh) * 16 * HD);
+    const uint4* vsrc = reinterpret_cast<const uint4*>(vc + ((size_t)blk * a.Hkv + kvh) * 16 * HD);
+    for (int x = threadIdx.x; x < VPB; x += blockDim.x) {
+      reinterpret_cast<uint4*>(&Ks[0][0])[x] = ksrc[x];
+      reinterpret_cast<uint4*>(&Vs[0][0])[x] = vsrc[x];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (!active[j]) continue;
+      const int xr = warp * 4 + j;
+      float sc[16];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        float part = 0.f;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) part = fmaf(qv[j][d], to_f32(Ks[kk][lane * DPL + d]), part);
+        part = group_sum<32>(part) * scale;
+        const int slot = s0 + kk;
+        bool vis = slot < hi;
+        if (vis && slot >= P) {
+          const int n = slot - P;
+          vis = (maskw[xr][n >> 5] >> (n & 31)) & 1u;
+        }
+        sc[kk] = vis ? part : -INFINITY;
+        mx = fmaxf(mx, sc[kk]);
+      }
+      const float m_new = fmaxf(m[j], mx);
+      if (m_new == -INFINITY) continue;
+      const float corr = (m[j] == -INFINITY) ? 0.f : exp2f(m[j] - m_new);
+      l[j] *= corr;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) o[j][d] *= corr;
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const float p = (sc[kk] == -INFINITY) ? 0.f : exp2f(sc[kk] - m_new);
+        l[j] += p;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) o[j][d] = fmaf(p, to_f32(Vs[kk][lane * DPL + d]), o[j][d]);
+      }
+      m[j] = m_new;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (!active[j]) continue;
+    const int rr = rg * kRowsPerCta + warp * 4 + j;
+    const size_t row = (((size_t)b * a.Hkv + kvh) * nsplit + split) * R + rr;
+    if (lane == 0) {
+      ml[row * 2] = m[j];
+      ml[row * 2 + 1] = l[j];
+    }
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[row * HD + lane * DPL + d] = o[j][d];
+  }
+}
+
+// One CTA per (sequence, node, query head); one thread per head dim.
+__global__ void attn_combine_kernel(AttnArgs a, const float* __restrict__ ml, const float* __restrict__ acc,
+                                    int chunk, int nsplit) {
+  const int h = blockIdx.x % a.Hq;
+  const int i = (blockIdx.x / a.Hq) % a.N;
+  const int b = blockIdx.x / (a.Hq * a.N);
+  if (a.err[b]) return;
+  const int G = a.Hq / a.Hkv, R = G * a.N, kvh = h / G, rr = i * G + h % G;
+  const int total = a.prefix_len[b] + a.N;
+  const int nsp = (total + chunk - 1) / chunk;
+  const size_t base = ((size_t)b * a.Hkv + kvh) * nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < nsp; ++s) M = fmaxf(M, ml[((base + s) * R + rr) * 2]);
+  const int d = threadIdx.x;
+  float lsum = 0.f, o = 0.f;
+  for (int s = 0; s < nsp; ++s) {
+    const size_t row = (base + s) * R + rr;
+    const float ms = ml[row * 2];
+    if (ms == -INFINITY) continue;
+    const float wgt = exp2f(ms - M);
+    lsum = fmaf(ml[row * 2 + 1], wgt, lsum);
+    o = fmaf(acc[row * a.hd + d], wgt, o);
+  }
+  static_cast<bf16*>(a.out)[(((size_t)b * a.N + i) * a.Hq + h) * a.hd + d] = from_f32<bf16>(o / lsum);
+}
+
+template <int HD>
+cudaError_t launch_partial(const AttnArgs& a, const AttnPlan& p, char* ws, cudaStream_t s) {
+  dim3 grid(p.nsplit * a.Hkv * p.RG, a.B);
+  attn_partial_simt_kernel<HD><<<grid, kPartialThreads, 0, s>>>(
+      a, reinterpret_cast<const bf16*>(ws + p.off_qrot), reinterpret_cast<float*>(ws + p.off_ml),
+      reinterpret_cast<float*>(ws + p.off_acc), p.chunk, p.nsplit, p.RG);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int block_size) {
+  return plan_attn(B, N, Hq, Hkv, hd, max_blocks, block_size).total;
+}
+
+cudaError_t launch_tree_attn(const AttnArgs& a, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+  const AttnPlan p = plan_attn(a.B, a.N, a.Hq, a.Hkv, a.hd, a.max_blocks, a.block_size);
+  if (workspace_bytes < p.total) return cudaErrorInvalidValue;
+  char* ws = static_cast<char*>(workspace);
+  attn_check_kernel<<<a.B, 128, 0, s>>>(a);
+  attn_rope_kernel<<<a.B * a.N, 128, 0, s>>>(a, reinterpret_cast<bf16*>(ws + p.off_qrot));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.hd == 64) e = launch_partial<64>(a, p, ws, s);
+  else if (a.hd == 128) e = launch_partial<128>(a, p, ws, s);
+  else e = launch_partial<256>(a, p, ws, s);
+  if (e != cudaSuccess) return e;
+  attn_combine_kernel<<<a.B * a.N * a.Hq, a.hd, 0, s>>>(a, reinterpret_cast<const float*>(ws + p.off_ml),
+                                                        reinterpret_cast<const float*>(ws + p.off_acc),
+                                                        p.chunk, p.nsplit);
+  return cudaGetLastError();
+}
+
+}  // namespace tv

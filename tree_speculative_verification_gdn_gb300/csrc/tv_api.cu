@@ -1,0 +1,174 @@
+// C ABI entry points (declared in include/tv.h): host-side argument checks, then the
+// launchers of the individual kernels.  Nothing here allocates device memory.
+#include <math.h>
+#include <stdint.h>
+
+#include "tv.h"
+#include "tv_internal.h"
+
+namespace tv {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+}  // namespace tv
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return TV_OK;
+  g_last_cuda = static_cast<int>(e);
+  return TV_ERR_CUDA;
+}
+
+bool a16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool a4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool dim_ok(int d) { return d == 64 || d == 128; }
+
+// (io, state) pairs with a kernel: (F32,F32), (BF16,BF16), (BF16,F32).
+int gdn_dtypes(int io, int state) {
+  if ((io == TV_F32 && state == TV_F32) || (io == TV_BF16 && state == TV_BF16) ||
+      (io == TV_BF16 && state == TV_F32))
+    return TV_OK;
+  if ((io != TV_F32 && io != TV_BF16) || (state != TV_F32 && state != TV_BF16)) return TV_ERR_INVALID_ARG;
+  return TV_ERR_UNSUPPORTED;
+}
+
+int gdn_common(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+               const void* S0, const int32_t* parents, int B, int N, int H, int dk, int dv, int io,
+               int state, float q_scale, const void* out, const int32_t* err) {
+  if (!a16(q) || !a16(k) || !a4(v) || !a4(alpha) || !a4(beta) || !a16(S0) || !a4(parents) || !a4(out) ||
+      !a4(err))
+    return TV_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || H < 1 || !isfinite(q_scale)) return TV_ERR_INVALID_ARG;
+  if (N > TV_MAX_NODES || !dim_ok(dk) || !dim_ok(dv)) return TV_ERR_UNSUPPORTED;
+  return gdn_dtypes(io, state);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tv_status_string(int status) {
+  switch (status) {
+    case TV_OK: return "ok";
+    case TV_ERR_INVALID_ARG: return "invalid argument";
+    case TV_ERR_BAD_TREE: return "malformed tree (parents[i] must be -1 or an earlier node)";
+    case TV_ERR_BAD_PATH: return "accepted path is not a root-to-node path";
+    case TV_ERR_UNSUPPORTED: return "unsupported size or dtype";
+    case TV_ERR_CUDA: return "CUDA launch error";
+    case TV_ERR_TIMEOUT: return "device wait timed out";
+    case TV_ERR_CAPACITY: return "block table too short for prefix_len + N slots";
+    case TV_ERR_BAD_BLOCK: return "block-table entry outside the cache";
+    default: return "unknown status";
+  }
+}
+
+int tv_last_cuda_error(void) { return g_last_cuda; }
+
+int tv_version(void) { return 100; }
+
+int tv_tree_prepare(const int32_t* parents, int B, int N, int32_t* depth, uint32_t* mask_bits,
+                    int32_t* err, tv_stream_t stream) {
+  if (!a4(parents) || !a4(depth) || !a4(mask_bits) || !a4(err) || B < 1 || N < 1) return TV_ERR_INVALID_ARG;
+  if (N > TV_MAX_NODES) return TV_ERR_UNSUPPORTED;
+  return cuda_status(tv::launch_tree_prepare(parents, B, N, depth, mask_bits, err, stream));
+}
+
+int tv_gdn_tree_verify_fork(const void* q, const void* k, const void* v, const float* alpha,
+                            const float* beta, const void* S0, const int32_t* parents, int B, int N,
+                            int H, int dk, int dv, int io_dtype, int state_dtype, float q_scale,
+                            void* out, void* node_states, int32_t* err, tv_stream_t stream) {
+  int st = gdn_common(q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale,
+                      out, err);
+  if (st != TV_OK) return st;
+  if (!a16(node_states)) return TV_ERR_INVALID_ARG;
+  tv::GdnArgs a{q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale, out, err};
+  return cuda_status(tv::launch_gdn_fork(a, node_states, stream));
+}
+
+int tv_gdn_tree_verify_wy(const void* q, const void* k, const void* v, const float* alpha,
+                          const float* beta, const void* S0, const int32_t* parents, int B, int N,
+                          int H, int dk, int dv, int io_dtype, int state_dtype, float q_scale, void* out,
+                          float* pseudo_v, float* log_gamma, int32_t* err, tv_stream_t stream) {
+  int st = gdn_common(q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale,
+                      out, err);
+  if (st != TV_OK) return st;
+  if (!a4(pseudo_v) || !a4(log_gamma)) return TV_ERR_INVALID_ARG;
+  tv::GdnArgs a{q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale, out, err};
+  return cuda_status(tv::launch_gdn_wy(a, pseudo_v, log_gamma, stream));
+}
+
+int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,
+                  const int32_t* parents, const void* node_states, const float* pseudo_v,
+                  const float* log_gamma, const void* k, void* S0, int B, int N, int H, int dk, int dv,
+                  int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream) {
+  if (!a4(accepted_path) || !a4(accepted_len) || !a4(parents) || !a16(S0) || !a4(err)) return TV_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || H < 1 || Lmax < 1) return TV_ERR_INVALID_ARG;
+  if (mode == TV_MODE_FORK) {
+    if (!a16(node_states)) return TV_ERR_INVALID_ARG;
+  } else if (mode == TV_MODE_WY) {
+    if (!a4(pseudo_v) || !a4(log_gamma) || !a16(k)) return TV_ERR_INVALID_ARG;
+  } else {
+    return TV_ERR_INVALID_ARG;
+  }
+  if (N > TV_MAX_NODES || !dim_ok(dk) || !dim_ok(dv)) return TV_ERR_UNSUPPORTED;
+  int st = gdn_dtypes(io_dtype, state_dtype);
+  if (st != TV_OK) return st;
+  tv::CommitArgs a{mode, accepted_path, accepted_len, Lmax, parents, node_states, pseudo_v, log_gamma, k,
+                   S0, B, N, H, dk, dv, io_dtype, state_dtype, err};
+  return cuda_status(tv::launch_gdn_commit(a, stream));
+}
+
+size_t tv_tree_attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int block_size) {
+  if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || hd < 1 || max_blocks < 1 || block_size < 1) return 0;
+  return tv::attn_workspace_size(B, N, Hq, Hkv, hd, max_blocks, block_size);
+}
+
+int tv_tree_attn(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                 int num_blocks, const int32_t* block_table, int max_blocks, const int32_t* prefix_len,
+                 const int32_t* parents, int B, int N, int Hq, int Hkv, int hd, int block_size,
+                 float rope_theta, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
+                 int32_t* err, tv_stream_t stream) {
+  if (!a16(q) || !a16(k_new) || !a16(v_new) || !a16(k_cache) || !a16(v_cache) || !a4(block_table) ||
+      !a4(prefix_len) || !a4(parents) || !a16(out) || !a16(workspace) || !a4(err))
+    return TV_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || num_blocks < 1 || max_blocks < 1 ||
+      !(rope_theta > 0.f) || !isfinite(rope_theta) || !isfinite(sm_scale))
+    return TV_ERR_INVALID_ARG;
+  if (N > TV_MAX_NODES || (hd != 64 && hd != 128 && hd != 256) || block_size != TV_BLOCK_SIZE)
+    return TV_ERR_UNSUPPORTED;
+  if (B > 65535) return TV_ERR_UNSUPPORTED;
+  if (workspace_bytes < tv::attn_workspace_size(B, N, Hq, Hkv, hd, max_blocks, block_size))
+    return TV_ERR_INVALID_ARG;
+  tv::AttnArgs a{q, k_new, v_new, k_cache, v_cache, num_blocks, block_table, max_blocks, prefix_len, parents,
+                 B, N, Hq, Hkv, hd, block_size, rope_theta, sm_scale, out, err};
+  return cuda_status(tv::launch_tree_attn(a, workspace, workspace_bytes, stream));
+}
+
+int tv_kv_compact(void* k_cache, void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
+                  const int32_t* prefix_len, const int32_t* parents, int N, const int32_t* accepted_path,
+                  const int32_t* accepted_len, int Lmax, int B, int Hkv, int hd, int block_size,
+                  int32_t* slot_map, int32_t* new_len, int32_t* err, tv_stream_t stream) {
+  if (!a16(k_cache) || !a16(v_cache) || !a4(block_table) || !a4(prefix_len) || !a4(parents) ||
+      !a4(accepted_path) || !a4(accepted_len) || !a4(slot_map) || !a4(new_len) || !a4(err))
+    return TV_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || Hkv < 1 || Lmax < 1 || num_blocks < 1 || max_blocks < 1) return TV_ERR_INVALID_ARG;
+  if (N > TV_MAX_NODES || (hd != 64 && hd != 128 && hd != 256) || block_size != TV_BLOCK_SIZE)
+    return TV_ERR_UNSUPPORTED;
+  tv::CompactArgs a{k_cache, v_cache, num_blocks, block_table, max_blocks, prefix_len, parents, N,
+                    accepted_path, accepted_len, Lmax, B, Hkv, hd, block_size, slot_map, new_len, err};
+  return cuda_status(tv::launch_kv_compact(a, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// Host-side launchers of the CUDA kernels; called by the C ABI in tv_api.cu after the
+// arguments have been checked.  Each returns the CUDA error of its launch(es).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "tv.h"
+
+namespace tv {
+
+int device_sm_count();
+
+struct GdnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* alpha;
+  const float* beta;
+  const void* S0;
+  const int32_t* parents;
+  int B, N, H, dk, dv;
+  int io, state;
+  float q_scale;
+  void* out;
+  int32_t* err;
+};
+
+cudaError_t launch_tree_prepare(const int32_t* parents, int B, int N, int32_t* depth,
+                                uint32_t* mask_bits, int32_t* err, cudaStream_t s);
+
+cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, cudaStream_t s);
+
+cudaError_t launch_gdn_wy(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s);
+
+struct CommitArgs {
+  int mode;
+  const int32_t* path;
+  const int32_t* path_len;
+  int Lmax;
+  const int32_t* parents;
+  const void* node_states;
+  const float* pseudo_v;
+  const float* log_gamma;
+  const void* k;
+  void* S0;
+  int B, N, H, dk, dv, io, state;
+  int32_t* err;
+};
+cudaError_t launch_gdn_commit(const CommitArgs& a, cudaStream_t s);
+
+struct AttnArgs {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  int num_blocks;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* prefix_len;
+  const int32_t* parents;
+  int B, N, Hq, Hkv, hd, block_size;
+  float rope_theta, sm_scale;
+  void* out;
+  int32_t* err;
+};
+size_t attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int block_size);
+cudaError_t launch_tree_attn(const AttnArgs& a, void* workspace, size_t workspace_bytes,
+                             cudaStream_t s);
+
+struct CompactArgs {
+  void* k_cache;
+  void* v_cache;
+  int num_blocks;
+  const int32_t* block_table;
+  int max_blocks;
+  const int32_t* prefix_len;
+  const int32_t* parents;
+  int N;
+  const int32_t* path;
+  const int32_t* path_len;
+  int Lmax, B, Hkv, hd, block_size;
+  int32_t* slot_map;
+  int32_t* new_len;
+  int32_t* err;
+};
+cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t s);
+
+}  // namespace tv

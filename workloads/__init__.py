@@ -64,9 +64,9 @@ def random_tree(n: int, rng: np.random.Generator, max_children: int = 4,
 
     Nodes are expanded in breadth-first order; each expanded node draws c ~ U{1..max_children}
     children until ``n`` nodes exist; nodes at ``max_depth`` are not expanded.  If the
-    frontier empties first the caller's generator simply draws again.
+    frontier empties first the caller's generator simply draws again (at most 1000 times).
     """
-    while True:
+    for _ in range(1000):
         parents, depth = [-1], [0]
         head = 0
         while len(parents) < n and head < len(parents):
@@ -82,6 +82,7 @@ def random_tree(n: int, rng: np.random.Generator, max_children: int = 4,
                 depth.append(depth[node] + 1)
         if len(parents) == n:
             return parents
+    raise ValueError(f"no tree of {n} nodes with <= {max_children} children and depth <= {max_depth}")
 
 
 def random_accepted_path(parents: list[int], rng: np.random.Generator,
