@@ -1,0 +1,557 @@
+"""Benchmark of one verify round of tree-speculative verification on a GDN hybrid.
+
+One step is one pass of every step of the hot path over one batch of synthetic inputs:
+
+  * tree prepare for the batch's draft trees;
+  * the 24-layer gated-DeltaNet stack of config 2 (B=64 sequences, 40-node k=3 d=3 trees,
+    H=16, d=128, bf16) in fork/checkpoint mode -- verify all 24 layers, then commit all 24 --
+    and in TreeWY mode -- verify all 24, then commit all 24 (separate S_0 buffers per mode);
+  * one tree-masked attention layer of config 3 (B=32, 16q/4kv, hd 256, bf16, paged prefixes
+    P ~ U[2048, 32768], 40-node trees) followed by the KV compaction of its accepted paths.
+
+``value`` = GDN node-layer verifications per second over the whole step (64 x 40 nodes x 24
+layers x 2 modes per step, divided by the step time, attention rows included).  Every row is
+also timed on its own with CUDA events on the launching stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica (weak scaling, no collective on the data path).
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS = 24
+METRIC = "tree-verified draft nodes/s per GDN layer; HBM GB/s & tensor util vs roofline"
+WORKLOAD = ("config 2: 24 GDN layers, B=64, N=40 (k=3 d=3), H=16, dk=dv=128, bf16, fork+commit and "
+            "TreeWY+commit; config 3: tree attention B=32, 16q/4kv, hd=256, paged P~U[2048,32768], N=40, "
+            "+ KV compaction")
+
+
+# ----------------------------------------------------------------------------- accounting
+def checkpoint_bytes(layers: int, heads: int, dk: int, dv: int, elem_bytes: int) -> int:
+    """Bytes of one GDN checkpoint of a whole stack (qwen35-tree-spec §六: 24 x 16 x 128 x 128 x 2
+    bytes ~ 12 MB)."""
+    return layers * heads * dk * dv * elem_bytes
+
+
+def gdn_bytes(B, N, H, dk, dv, e_io, e_state, mode, L_sum=0):
+    """Algorithmic HBM bytes of one GDN layer call (inputs read once, outputs written once)."""
+    inputs = B * (H * dv * dk * e_state + N * H * (2 * dk + dv) * e_io + N * H * 8 + N * 4)
+    if mode == "fork":
+        return inputs + B * N * H * dv * e_io + B * N * H * dv * dk * e_state
+    if mode == "wy":
+        return inputs + B * N * H * dv * e_io + B * N * H * dv * 4 + B * N * H * 4
+    if mode == "commit_fork":
+        return 2 * B * H * dv * dk * e_state + B * N * 4
+    if mode == "commit_wy":
+        return 2 * B * H * dv * dk * e_state + L_sum * H * (dv * 4 + dk * e_io + 4) + B * N * 4
+    raise ValueError(mode)
+
+
+def attn_bytes(prefix_lens, N, Hq, Hkv, hd, e=2):
+    kv = sum(prefix_lens) * Hkv * hd * 2 * e
+    nodes = len(prefix_lens) * N * (Hq + 2 * Hkv) * hd * e      # q, k_new, v_new
+    writes = len(prefix_lens) * N * (2 * Hkv + Hq) * hd * e     # cache node slots + out
+    return kv + nodes + writes
+
+
+def attn_flops(prefix_lens, depths_per_seq, Hq, hd):
+    """QK^T and PV over the visible keys of every node: 4 * hd flops per (query head, key)."""
+    total = 0
+    for P, dep in zip(prefix_lens, depths_per_seq):
+        total += sum(4 * Hq * hd * (P + d + 1) for d in dep)
+    return total
+
+
+def _depths(parents):
+    d = []
+    for p in parents:
+        d.append(0 if p < 0 else d[p] + 1)
+    return d
+
+
+def compact_bytes(path_lens, Hkv, hd, e=2):
+    return sum(path_lens) * Hkv * hd * e * 2 * 2   # K and V, read + write
+
+
+# ----------------------------------------------------------------------------- helpers
+def kernel_traffic(row: str):
+    """dram read+write bytes per launch of a row's main kernel from ``profiles/traffic.txt``, a
+    summary of an ncu capture; null when the kernel's source changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for ln in f:
+            parts = ln.split()
+            if len(parts) >= 4 and parts[0] == row:
+                src = os.path.join(ROOT, "tree_speculative_verification_gdn_gb300", "csrc", parts[2])
+                if not os.path.exists(src):
+                    return None
+                with open(src, "rb") as g:
+                    digest = hashlib.sha256(g.read()).hexdigest()[:16]
+                return float(parts[1]) if digest == parts[3] else None
+    return None
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- our arm
+class Round:
+    """Device buffers of one verify round and the sequence of ABI calls that run it."""
+
+    def __init__(self, rank: int, layers: int, torch, tv, W):
+        self.torch, self.tv = torch, tv
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self.dev = dev
+        seed = 1000 * rank
+        self.layers = layers
+        self.gdn_host = [W.cfg2_layer(layer=l, seed=seed) for l in range(layers)]
+        c0 = self.gdn_host[0]
+        self.B, self.N, self.H, self.dk, self.dv = c0.shape
+        B, N, H, dk, dv = self.B, self.N, self.H, self.dk, self.dv
+        self.attn_host = W.cfg3(seed=seed)
+        a = self.attn_host
+        self.aB, self.aN, self.Hq, self.Hkv, self.hd = a.shape
+
+        def d(t):
+            return t.contiguous().to(dev)
+
+        # per-round inputs (copied from host in the end-to-end measurement)
+        self.in_gdn = [dict(q=d(c.q), k=d(c.k), v=d(c.v), alpha=d(c.alpha), beta=d(c.beta)) for c in self.gdn_host]
+        self.parents = d(c0.parents)
+        self.path, self.path_len = d(c0.path), d(c0.path_len)
+        self.in_attn = dict(q=d(a.q), k_new=d(a.k_new), v_new=d(a.v_new), block_table=d(a.block_table),
+                            prefix_len=d(a.prefix_len), parents=d(a.parents), path=d(a.path),
+                            path_len=d(a.path_len))
+        # resident state
+        self.S0_fork = [d(c.S0) for c in self.gdn_host]
+        self.S0_wy = [d(c.S0) for c in self.gdn_host]
+        self.k_cache, self.v_cache = d(a.k_cache), d(a.v_cache)
+        # outputs
+        bf = torch.bfloat16
+        self.o_fork = [torch.empty((B, N, H, dv), dtype=bf, device=dev) for _ in range(layers)]
+        self.o_wy = [torch.empty((B, N, H, dv), dtype=bf, device=dev) for _ in range(layers)]
+        mem0 = torch.cuda.memory_allocated()
+        self.states = [torch.empty((B, N, H, dv, dk), dtype=bf, device=dev) for _ in range(layers)]
+        self.fork_state_bytes = torch.cuda.memory_allocated() - mem0
+        mem0 = torch.cuda.memory_allocated()
+        self.pv = [torch.empty((B, N, H, dv), dtype=torch.float32, device=dev) for _ in range(layers)]
+        self.lg = [torch.empty((B, N, H), dtype=torch.float32, device=dev) for _ in range(layers)]
+        self.wy_state_bytes = torch.cuda.memory_allocated() - mem0
+        i32 = torch.int32
+        self.depth = torch.empty((B, N), dtype=i32, device=dev)
+        self.mask = torch.empty((B, N, (N + 31) // 32), dtype=i32, device=dev)
+        self.err = torch.zeros((16, max(B, self.aB)), dtype=i32, device=dev)
+        self.a_out = torch.empty((self.aB, self.aN, self.Hq, self.hd), dtype=bf, device=dev)
+        ws = tv.tv_tree_attn_workspace_size(self.aB, self.aN, self.Hq, self.Hkv, self.hd, a.block_table.shape[1])
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.slot_map = torch.empty(a.path.shape, dtype=i32, device=dev)
+        self.new_len = torch.empty((self.aB,), dtype=i32, device=dev)
+        self.rows = ["tree_prepare", "fork_verify", "fork_commit", "wy_verify", "wy_commit", "tree_attn",
+                     "kv_compact"]
+        self.launches_per_step = 1 + layers * 4 + 4 + 1
+
+    def step(self, ev=None):
+        """One verify round.  ``ev``: optional dict row -> list of (start, end) event pairs."""
+        torch, tv = self.torch, self.tv
+        B = self.B
+        err = self.err
+
+        def mark(row, fn):
+            if ev is None:
+                fn()
+                return
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            ev[row].append((s, e))
+
+        mark("tree_prepare", lambda: tv.tv_tree_prepare(self.parents, self.depth, self.mask, err[0, :B]))
+        for l in range(self.layers):
+            x = self.in_gdn[l]
+            mark("fork_verify", lambda: tv.tv_gdn_tree_verify_fork(
+                x["q"], x["k"], x["v"], x["alpha"], x["beta"], self.S0_fork[l], self.parents, self.o_fork[l],
+                self.states[l], err[1, :B]))
+        for l in range(self.layers):
+            mark("fork_commit", lambda: tv.tv_gdn_commit(
+                tv.TV_MODE_FORK, self.path, self.path_len, self.parents, self.S0_fork[l], err[2, :B],
+                node_states=self.states[l]))
+        for l in range(self.layers):
+            x = self.in_gdn[l]
+            mark("wy_verify", lambda: tv.tv_gdn_tree_verify_wy(
+                x["q"], x["k"], x["v"], x["alpha"], x["beta"], self.S0_wy[l], self.parents, self.o_wy[l],
+                self.pv[l], self.lg[l], err[3, :B]))
+        for l in range(self.layers):
+            x = self.in_gdn[l]
+            mark("wy_commit", lambda: tv.tv_gdn_commit(
+                tv.TV_MODE_WY, self.path, self.path_len, self.parents, self.S0_wy[l], err[4, :B],
+                pseudo_v=self.pv[l], log_gamma=self.lg[l], k=x["k"]))
+        a = self.in_attn
+        aB = self.aB
+        mark("tree_attn", lambda: tv.tv_tree_attn(
+            a["q"], a["k_new"], a["v_new"], self.k_cache, self.v_cache, a["block_table"], a["prefix_len"],
+            a["parents"], self.a_out, self.ws, err[5, :aB], rope_theta=1e6))
+        mark("kv_compact", lambda: tv.tv_kv_compact(
+            self.k_cache, self.v_cache, a["block_table"], a["prefix_len"], a["parents"], a["path"], a["path_len"],
+            self.slot_map, self.new_len, err[6, :aB]))
+
+    # end-to-end: per-round inputs from pinned host memory, outputs back to pinned host memory
+    def host_buffers(self):
+        torch = self.torch
+        pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
+        self.h_in = [{k: pin(v) for k, v in x.items()} for x in self.in_gdn]
+        self.h_attn = {k: pin(v) for k, v in self.in_attn.items()}
+        self.h_parents, self.h_path, self.h_path_len = pin(self.parents), pin(self.path), pin(self.path_len)
+        self.h_o_fork = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.o_fork]
+        self.h_o_wy = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.o_wy]
+        self.h_a_out = torch.empty(self.a_out.shape, dtype=self.a_out.dtype).pin_memory()
+        self.h_err = torch.empty(self.err.shape, dtype=self.err.dtype).pin_memory()
+        self.h_small = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (self.slot_map, self.new_len)]
+        h2d = sum(t.numel() * t.element_size() for x in self.h_in for t in x.values())
+        h2d += sum(t.numel() * t.element_size() for t in self.h_attn.values())
+        h2d += sum(t.numel() * t.element_size() for t in (self.h_parents, self.h_path, self.h_path_len))
+        d2h = sum(t.numel() * t.element_size() for t in self.h_o_fork + self.h_o_wy)
+        d2h += self.h_a_out.numel() * 2 + self.h_err.numel() * 4 + sum(t.numel() * 4 for t in self.h_small)
+        return h2d, d2h
+
+    def step_e2e(self):
+        for dst, src in zip(self.in_gdn, self.h_in):
+            for k in dst:
+                dst[k].copy_(src[k], non_blocking=True)
+        for k in self.in_attn:
+            self.in_attn[k].copy_(self.h_attn[k], non_blocking=True)
+        self.parents.copy_(self.h_parents, non_blocking=True)
+        self.path.copy_(self.h_path, non_blocking=True)
+        self.path_len.copy_(self.h_path_len, non_blocking=True)
+        self.step()
+        for h, d in zip(self.h_o_fork, self.o_fork):
+            h.copy_(d, non_blocking=True)
+        for h, d in zip(self.h_o_wy, self.o_wy):
+            h.copy_(d, non_blocking=True)
+        self.h_a_out.copy_(self.a_out, non_blocking=True)
+        self.h_err.copy_(self.err, non_blocking=True)
+        self.h_small[0].copy_(self.slot_map, non_blocking=True)
+        self.h_small[1].copy_(self.new_len, non_blocking=True)
+
+
+class OraclePool:
+    """The fp64 oracle, as it stands, on every host core: one config-2 sequence (40 nodes,
+    16 heads, one GDN layer) per task through ``oracle.gdn.verify_by_depth``, in spawned worker
+    processes with single-threaded BLAS.  Started before any GPU work."""
+
+    def __init__(self, cores: int | None = None):
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        self.cores = cores or os.cpu_count() or 1
+        env_keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+        old = {k: os.environ.get(k) for k in env_keys}
+        for k in env_keys:
+            os.environ[k] = "1"
+        try:
+            self.ex = cf.ProcessPoolExecutor(max_workers=self.cores, mp_context=mp.get_context("spawn"),
+                                             initializer=_oracle_init)
+            list(self.ex.map(_oracle_sequence, [0] * self.cores))   # imports + input generation
+        finally:
+            for k, v in old.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        self.next_b = 0
+
+    def sample(self, seconds: float) -> dict:
+        t0 = time.perf_counter()
+        done = 0
+        while True:
+            list(self.ex.map(_oracle_sequence, [(self.next_b + j) % 64 for j in range(self.cores)]))
+            self.next_b += self.cores
+            done += self.cores
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
+        return {"value": done * 40 / dt, "unit": "nodes/s", "cores": self.cores, "kind": "oracle",
+                "sample": f"{done} config-2 sequences (40 nodes x 16 heads, one GDN layer, bf16 inputs in fp64) "
+                          f"through the oracle's depth-by-depth schedule in {dt:.1f} s"}
+
+    def close(self):
+        self.ex.shutdown()
+
+
+_ORACLE_CACHE = {}
+
+
+def _oracle_init():
+    import workloads as W
+    _ORACLE_CACHE["inp"] = W.cfg2_layer(layer=0).oracle_inputs()
+
+
+def _oracle_sequence(b):
+    import numpy as np
+    from oracle import gdn as G
+    inp = _ORACLE_CACHE["inp"]
+    sub = {k: (v[b:b + 1] if isinstance(v, np.ndarray) else v) for k, v in inp.items()}
+    G.verify_by_depth(sub)
+    return b
+
+
+def run_ours(args) -> None:
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pool = OraclePool()                         # spawned before any GPU work
+        cpu_base = pool.sample(args.cpu_seconds)
+        pool.close()
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import tree_speculative_verification_gdn_gb300 as tv
+    import workloads as W
+
+    rnd = Round(rank, args.layers, torch, tv, W)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        rnd.step()
+    barrier()
+    assert int(rnd.err.abs().sum()) == 0, f"verify errors: {rnd.err.cpu().tolist()}"
+
+    ev = {r: [] for r in rnd.rows}
+    steps_ev = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        s = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        rnd.step(ev)
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        steps_ev.append((s, e))
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    step_ms = sorted(s.elapsed_time(e) for s, e in steps_ev)
+    row_ms = {r: sum(s.elapsed_time(e) for s, e in ev[r]) / args.steps for r in rnd.rows}
+    row_calls = {r: len(ev[r]) // args.steps for r in rnd.rows}
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        h2d, d2h = rnd.host_buffers()
+        for _ in range(2):
+            rnd.step_e2e()
+        barrier()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(args.steps):
+            rnd.step_e2e()
+        e.record(stream)
+        barrier()
+        e2e_ms = s.elapsed_time(e) / args.steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        nodes = rnd.B * rnd.N * rnd.layers * 2 * world
+        e2e = {"value": nodes / (e2e_ms * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    peaks = load_peaks()
+    B, N, H, dk, dv = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv
+    L_sum = int(rnd.gdn_host[0].path_len.sum())
+    a = rnd.attn_host
+    plens = [int(x) for x in a.prefix_len]
+    row_bytes = {
+        "tree_prepare": B * N * 4 * 3,
+        "fork_verify": gdn_bytes(B, N, H, dk, dv, 2, 2, "fork"),
+        "fork_commit": gdn_bytes(B, N, H, dk, dv, 2, 2, "commit_fork"),
+        "wy_verify": gdn_bytes(B, N, H, dk, dv, 2, 2, "wy"),
+        "wy_commit": gdn_bytes(B, N, H, dk, dv, 2, 2, "commit_wy", L_sum),
+        "tree_attn": attn_bytes(plens, rnd.aN, rnd.Hq, rnd.Hkv, rnd.hd),
+        "kv_compact": compact_bytes([int(x) for x in a.path_len], rnd.Hkv, rnd.hd),
+    }
+    a_flops = attn_flops(plens, [_depths(t) for t in a.trees], rnd.Hq, rnd.hd)
+    rows = {}
+    for r in rnd.rows:
+        per_call_ms = row_ms[r] / max(1, row_calls[r])
+        gbs = row_bytes[r] / (per_call_ms * 1e-3) / 1e9 if per_call_ms > 0 else 0.0
+        rows[r] = {"ms_per_call": round(per_call_ms, 5), "calls_per_step": row_calls[r],
+                   "algorithmic_bytes_per_call": row_bytes[r], "achieved_gbs": round(gbs, 1),
+                   "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    rows["tree_attn"]["achieved_tflops"] = round(a_flops / (row_ms["tree_attn"] * 1e-3) / 1e12, 2)
+    rows["fork_verify"]["nodes_per_s_per_layer"] = round(B * N / (rows["fork_verify"]["ms_per_call"] * 1e-3))
+    rows["wy_verify"]["nodes_per_s_per_layer"] = round(B * N / (rows["wy_verify"]["ms_per_call"] * 1e-3))
+    dom = max(rnd.rows, key=lambda r: row_ms[r])
+    roof = {"kernel": dom, "bound": "hbm", "achieved": rows[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": rows[dom]["frac_hbm"], "traffic": kernel_traffic(dom),
+            "peak_source": peaks["source"] + " (copy, burst)"}
+    nodes_per_step = B * N * rnd.layers * 2 * world
+    value = nodes_per_step / (ms_per_step * 1e-3)
+    mem = {"fork_checkpoint_bytes": rnd.fork_state_bytes, "wy_pseudo_value_bytes": rnd.wy_state_bytes,
+           "pages_bytes_per_checkpoint": checkpoint_bytes(24, 16, 128, 128, 2),
+           "pages_accounting_fork_bytes": checkpoint_bytes(24, 16, 128, 128, 2) * B * N,
+           "peak_allocated_bytes": torch.cuda.max_memory_allocated()}
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "nodes/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "ms_per_step_min": round(step_ms[0], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": rnd.layers, "global_batch": B * world,
+                       "nodes_per_tree": N, "attn_batch": rnd.aB * world,
+                       "l2": "working set >> 129 MB L2 (fork checkpoints 1.3 GB per layer)",
+                       "parallelism": f"replicas x{world}"},
+            "gpu_launches": rnd.launches_per_step * args.steps, "clocks": clk, "roofline": roof,
+            "rows": rows, "state_memory": mem, "e2e": e2e, "cpu_baseline": cpu_base}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args) -> None:
+    """The fp64 oracle on the host cores, each step a bounded sample of the same workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    pool = OraclePool()
+    seconds = max(2.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        pool.sample(seconds=0.0)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(pool.sample(seconds=seconds))
+    dt = time.perf_counter() - t0
+    pool.close()
+    value = statistics.mean(v["value"] for v in vals)
+    base = dict(vals[-1])
+    base["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "nodes/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": base["sample"]},
+            "cpu_baseline": base,
+            "e2e": {"value": round(value, 2), "unit": "nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=LAYERS, help="GDN layers per step (24 = the config)")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
