@@ -9,24 +9,28 @@
 // alpha_i, beta_i.  A CTA therefore owns a slab of 16 rows of one (sequence, head), keeps
 // their fp32 state on chip and walks the whole tree once, depth-first, instead of one launch
 // per depth reading every parent snapshot back from HBM.  HBM traffic is the floor: S_0 read
-// once, each checkpoint written once.  Each row is held by 8 lanes (dk/8 columns each), so a
-// dot product costs 3 shuffles.
+// once per root, each checkpoint written once.  Each row is held by 16 lanes (dk/16 columns
+// each), so a dot product costs 4 shuffles.  The inputs of the next 8 nodes (k, q and the
+// slab's v) stream into a shared-memory ring through bulk asynchronous copies.
 //
 // Depth-first order visits a node's light children first and its heaviest child (largest
 // subtree) last.  A branching node pushes its state to a shared-memory slot that its later
 // children read back; the first child takes the state straight from registers.  With
 // heavy-last order a slot is at most 1 + (number of light edges above the node) and each
-// light edge halves the subtree, so 8 slots (S_0 + 7) cover every tree of <= 256 nodes.
+// light edge halves the subtree, so slots 1..7 cover every tree of <= 256 nodes (a branching
+// node has >= 3 nodes in its subtree, so it sits below at most 6 light edges).
+#include "tv_async.cuh"
 #include "tv_common.cuh"
 #include "tv_internal.h"
 
 namespace tv {
 namespace {
 
-constexpr int kLPR = 8;                 // lanes per state row
+constexpr int kLPR = 16;                // lanes per state row
 constexpr int kRows = 16;               // state rows per CTA
-constexpr int kThreads = kLPR * kRows;  // 128
-constexpr int kSlots = 8;               // on-chip state slots: S_0 + 7 branch points
+constexpr int kThreads = kLPR * kRows;  // 256
+constexpr int kSlots = 7;               // on-chip state slots 1..7 (S_0 is re-read for a root)
+constexpr int kStages = 8;              // depth of the node-input ring
 
 struct Sched {
   int par[TV_MAX_NODES];
@@ -103,111 +107,149 @@ __device__ int build_schedule(const int32_t* __restrict__ parents, int N, Sched&
   for (int i = tid; i < N; i += nt) {
     const int p = s.par[i];
     s.src[i] = (p < 0) ? 0 : (s.pre[i] == s.pre[p] + 1 ? -1 : s.push[p]);
-    if (s.order[i] < 0 || s.src[i] >= kSlots) s.flag = 1;  // never expected: guards every index
+    if (s.order[i] < 0 || s.src[i] > kSlots) s.flag = 1;  // never expected: guards every index
   }
   __syncthreads();
-  return (s.maxslot < kSlots && !s.flag) ? 0 : TV_ERR_UNSUPPORTED;
+  return (s.maxslot <= kSlots && !s.flag) ? 0 : TV_ERR_UNSUPPORTED;
 }
 
-template <typename TIO, int CPL>
-struct NodeIn {
-  float k[CPL], q[CPL];
-  float v, alpha, beta;
-  __device__ __forceinline__ void load(const TIO* __restrict__ kp, const TIO* __restrict__ qp,
-                                       const TIO* __restrict__ vp, const float* __restrict__ ap,
-                                       const float* __restrict__ bp) {
-    load_vec<CPL>(kp, k);
-    load_vec<CPL>(qp, q);
-    v = to_f32(__ldg(vp));
-    alpha = __ldg(ap);
-    beta = __ldg(bp);
-  }
+// Inputs of one node for the CTA's (sequence, head, row slab), filled by bulk async copies.
+template <typename TIO, int DK>
+struct Stage {
+  TIO k[DK];
+  TIO q[DK];
+  TIO v[kRows];
 };
+
+// CPL consecutive elements of a stage (shared memory) -> floats.
+template <int CPL>
+__device__ __forceinline__ void load_stage_vec(const float* p, float* out) {
+#pragma unroll
+  for (int j = 0; j < CPL / 4; ++j) {
+    const float4 t = reinterpret_cast<const float4*>(p)[j];
+    out[4 * j] = t.x; out[4 * j + 1] = t.y; out[4 * j + 2] = t.z; out[4 * j + 3] = t.w;
+  }
+}
+template <int CPL>
+__device__ __forceinline__ void load_stage_vec(const bf16* p, float* out) {
+#pragma unroll
+  for (int j = 0; j < CPL / 8; ++j) unpack8(reinterpret_cast<const uint4*>(p)[j], out + 8 * j);
+  if constexpr (CPL % 8 == 4) unpack4(*reinterpret_cast<const uint2*>(p + CPL - 4), out + CPL - 4);
+}
 
 template <typename TIO, typename TS, int DK>
 __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __restrict__ states,
                                                             int ctas_per_seq) {
   constexpr int CPL = DK / kLPR;  // columns per lane
   constexpr int Q4 = CPL / 4;     // float4 per lane per slot
-  extern __shared__ __align__(16) unsigned char smem[];
+  using StageT = Stage<TIO, DK>;
+  extern __shared__ __align__(128) unsigned char smem[];
   Sched& sc = *reinterpret_cast<Sched*>(smem);
-  float4* stack = reinterpret_cast<float4*>(smem + sizeof(Sched));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sizeof(Sched));
+  float* s_alpha = reinterpret_cast<float*>(bars + kStages);
+  float* s_beta = s_alpha + TV_MAX_NODES;
+  StageT* ring = reinterpret_cast<StageT*>(s_beta + TV_MAX_NODES);
+  float4* stack = reinterpret_cast<float4*>(ring + kStages);
 
   const int b = blockIdx.x / ctas_per_seq, g = blockIdx.x % ctas_per_seq;
   const int N = a.N, H = a.H, dv = a.dv;
+  const int tid = threadIdx.x;
   const int status = build_schedule(a.parents + (size_t)b * N, N, sc);
-  if (g == 0 && threadIdx.x == 0) a.err[b] = status;
+  if (g == 0 && tid == 0) a.err[b] = status;
   if (status) return;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
 
   const TIO* __restrict__ q = static_cast<const TIO*>(a.q);
   const TIO* __restrict__ k = static_cast<const TIO*>(a.k);
   const TIO* __restrict__ v = static_cast<const TIO*>(a.v);
   const TS* __restrict__ S0 = static_cast<const TS*>(a.S0);
   TIO* __restrict__ out = static_cast<TIO*>(a.out);
-
-  const int tid = threadIdx.x, lane8 = tid & (kLPR - 1), rl = tid / kLPR;
+  const int lane = tid % kLPR, rl = tid / kLPR;
   const int slabs = dv / kRows, items = H * slabs;
   const float q_scale = a.q_scale;
+  uint32_t seq = 0;      // node loads issued and consumed by this CTA before the current item
+  bool timed_out = false;
 
   for (int item = g; item < items; item += ctas_per_seq) {
-    const int h = item / slabs;
-    const int r = (item % slabs) * kRows + rl;
-    float cur[CPL];
-    load_vec<CPL>(S0 + (((size_t)b * H + h) * dv + r) * DK + lane8 * CPL, cur);
-#pragma unroll
-    for (int j = 0; j < Q4; ++j)
-      stack[j * kThreads + tid] = make_float4(cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
-
-    auto in_ptrs = [&](int node, NodeIn<TIO, CPL>& x) {
+    const int h = item / slabs, r0 = (item % slabs) * kRows, r = r0 + rl;
+    auto issue = [&](uint32_t s, int node) {  // one thread: start the loads of node into stage s
       const size_t nh = ((size_t)b * N + node) * H + h;
-      x.load(k + nh * DK + lane8 * CPL, q + nh * DK + lane8 * CPL, v + nh * dv + r,
-             a.alpha + nh, a.beta + nh);
+      StageT& st = ring[s % kStages];
+      uint64_t* bar = &bars[s % kStages];
+      mbar_arrive_expect_tx(bar, sizeof(StageT));
+      bulk_g2s(st.k, k + nh * DK, DK * sizeof(TIO), bar);
+      bulk_g2s(st.q, q + nh * DK, DK * sizeof(TIO), bar);
+      bulk_g2s(st.v, v + nh * dv + r0, kRows * sizeof(TIO), bar);
     };
-    NodeIn<TIO, CPL> cin, nin;
-    int i = sc.order[0];
-    in_ptrs(i, cin);
+    for (int i = tid; i < N; i += kThreads) {
+      s_alpha[i] = __ldg(a.alpha + ((size_t)b * N + i) * H + h);
+      s_beta[i] = __ldg(a.beta + ((size_t)b * N + i) * H + h);
+    }
+    if (tid == 0)
+      for (int t = 0; t < N && t < kStages; ++t) issue(seq + t, sc.order[t]);
+    __syncthreads();
+
+    const TS* s0row = S0 + (((size_t)b * H + h) * dv + r) * DK + lane * CPL;
+    float cur[CPL];
     for (int t = 0; t < N; ++t) {
-      const int inext = (t + 1 < N) ? sc.order[t + 1] : i;
-      in_ptrs(inext, nin);  // prefetch the next node's inputs
+      const int i = sc.order[t];
+      const uint32_t s = seq + t;
       const int src = sc.src[i], push = sc.push[i];
-      if (src >= 0) {
+      if (src == 0) {
+        load_vec<CPL>(s0row, cur);  // a root starts from the committed state
+      } else if (src > 0) {
 #pragma unroll
         for (int j = 0; j < Q4; ++j) {
-          const float4 f = stack[(src * Q4 + j) * kThreads + tid];
+          const float4 f = stack[((src - 1) * Q4 + j) * kThreads + tid];
           cur[4 * j] = f.x; cur[4 * j + 1] = f.y; cur[4 * j + 2] = f.z; cur[4 * j + 3] = f.w;
         }
       }
+      if (!mbar_wait(&bars[s % kStages], (s / kStages) & 1u)) timed_out = true;
+      const StageT& st = ring[s % kStages];
+      float kf[CPL], qf[CPL];
+      load_stage_vec<CPL>(st.k + lane * CPL, kf);
+      load_stage_vec<CPL>(st.q + lane * CPL, qf);
+      const float vr = to_f32(st.v[rl]);
+      const float al = s_alpha[i], be = s_beta[i];
       float tk = 0.f;
 #pragma unroll
-      for (int e = 0; e < CPL; ++e) tk = fmaf(cur[e], cin.k[e], tk);
-      tk = group_sum<kLPR>(tk);                       // (S_p k_i)_r
-      const float w = cin.beta * (cin.v - cin.alpha * tk);  // pseudo-value w_i[r]
+      for (int e = 0; e < CPL; ++e) tk = fmaf(cur[e], kf[e], tk);
+      tk = group_sum<kLPR>(tk);                 // (S_p k_i)_r
+      const float w = be * (vr - al * tk);      // pseudo-value w_i[r]
       float ov = 0.f;
 #pragma unroll
       for (int e = 0; e < CPL; ++e) {
-        cur[e] = fmaf(w, cin.k[e], cin.alpha * cur[e]);
-        ov = fmaf(cur[e], cin.q[e], ov);
+        cur[e] = fmaf(w, kf[e], al * cur[e]);
+        ov = fmaf(cur[e], qf[e], ov);
       }
-      ov = group_sum<kLPR>(ov);                       // (S_i q_i)_r
+      ov = group_sum<kLPR>(ov);                 // (S_i q_i)_r
       const size_t nh = ((size_t)b * N + i) * H + h;
-      if (lane8 == 0) out[nh * dv + r] = from_f32<TIO>(ov * q_scale);
-      store_vec_cs<CPL>(states + (nh * dv + r) * DK + lane8 * CPL, cur);
-      if (push >= 0) {
+      if (lane == 0) out[nh * dv + r] = from_f32<TIO>(ov * q_scale);
+      store_vec_cs<CPL>(states + (nh * dv + r) * DK + lane * CPL, cur);
+      if (push > 0) {
 #pragma unroll
         for (int j = 0; j < Q4; ++j)
-          stack[(push * Q4 + j) * kThreads + tid] =
+          stack[((push - 1) * Q4 + j) * kThreads + tid] =
               make_float4(cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
       }
-      i = inext;
-      cin = nin;
+      __syncthreads();  // stage s is free again
+      if (tid == 0 && t + kStages < N) issue(s + kStages, sc.order[t + kStages]);
     }
+    seq += N;
   }
+  if (timed_out) a.err[b] = TV_ERR_TIMEOUT;
 }
 
 template <typename TIO, typename TS, int DK>
 cudaError_t launch_fork_t(const GdnArgs& a, void* states, cudaStream_t s) {
   auto kern = gdn_fork_kernel<TIO, TS, DK>;
-  const size_t smem = sizeof(Sched) + (size_t)kSlots * (DK / kLPR / 4) * kThreads * sizeof(float4);
+  const size_t smem = sizeof(Sched) + kStages * sizeof(uint64_t) + 2 * TV_MAX_NODES * sizeof(float) +
+                      kStages * sizeof(Stage<TIO, DK>) +
+                      (size_t)kSlots * (DK / kLPR / 4) * kThreads * sizeof(float4);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int occ = 0;

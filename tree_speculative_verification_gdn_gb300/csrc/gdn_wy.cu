@@ -184,6 +184,11 @@ cudaError_t launch_wy_t(const GdnArgs& a, float* pseudo_v, float* log_gamma, cud
 }  // namespace
 
 cudaError_t launch_gdn_wy(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s) {
+  if (gdn_wy_tc_supported(a)) return launch_gdn_wy_tc(a, pseudo_v, log_gamma, s);
+  return launch_gdn_wy_simt(a, pseudo_v, log_gamma, s);
+}
+
+cudaError_t launch_gdn_wy_simt(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s) {
   if (a.io == TV_F32 && a.state == TV_F32)
     return a.dk == 64 ? launch_wy_t<float, float, 64>(a, pseudo_v, log_gamma, s)
                       : launch_wy_t<float, float, 128>(a, pseudo_v, log_gamma, s);

@@ -1,0 +1,264 @@
+// TreeWY GDN tree verify on the 5th-generation tensor cores (bf16 I/O and state, dk = dv = 128).
+//
+// Same algebra as the CUDA-core kernel in gdn_wy.cu (TreeWY: Speculative Verification for
+// Gated DeltaNet Hybrids, abstract; reading stated there).  The one dense contraction of the
+// method -- S_0 times every node's key and query, [S_0 K^T | S_0 Q^T], a 128 x 2N x 128 product
+// per (sequence, head) -- runs as tcgen05 MMAs: TMA stages S_0 (A operand, 128 x 128) and the
+// node keys and queries (B operands, N x 128 each, zero rows past N) into shared memory in the
+// 128-byte swizzle layout, one thread issues 16 MMAs (M = 128, N = Npad, K = 16) that
+// accumulate in fp32 in TMEM, and the epilogue reads row r of both products back with
+// tcgen05.ld -- row r belongs to TMEM lane r, i.e. to thread r.  Each thread then runs the
+// ancestor-list forward substitution for its row in fp32; the (node, ancestor) coefficients
+// are computed meanwhile by the four warps from the same shared-memory tiles.
+#include "tv_async.cuh"
+#include "tv_common.cuh"
+#include "tv_internal.h"
+#include "tv_tc.cuh"
+#include "tv_tma_host.h"
+
+namespace tv {
+namespace {
+
+constexpr int kThreads = 128;   // one thread per state row (TMEM lane)
+constexpr int kD = 128;         // dk = dv
+constexpr int kPathCap = 4096;  // max sum over nodes of (depth + 1)
+constexpr uint32_t kTileA = kD * kD * 2;  // S_0 tile bytes
+
+struct TcHead {
+  uint64_t tma_bar;
+  uint64_t mma_bar;
+  uint32_t tmem_base;
+  int flag, total, fail;
+  int par[TV_MAX_NODES];
+  int depth[TV_MAX_NODES];
+  int off[TV_MAX_NODES + 1];
+  float lg[TV_MAX_NODES];
+  float beta[TV_MAX_NODES];
+};
+
+__global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* __restrict__ pseudo_v,
+                                                             float* __restrict__ log_gamma, int cap, int Npad,
+                                                             uint32_t tmem_cols,
+                                                             const __grid_constant__ CUtensorMap mS0,
+                                                             const __grid_constant__ CUtensorMap mK,
+                                                             const __grid_constant__ CUtensorMap mQ) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 1024-byte aligned tiles
+  unsigned char* sA = smem;                                  // S_0: 2 k-blocks x 128 rows x 128 B
+  unsigned char* sKQ = smem + kTileA;                        // K: 2 x Npad x 128 B, then Q: same
+  const uint32_t kq_bytes = (uint32_t)Npad * 128u;           // one k-block of K or Q
+  TcHead& hd = *reinterpret_cast<TcHead*>(sKQ + 4 * kq_bytes);
+  int* pidx = reinterpret_cast<int*>(&hd + 1);
+  float* cK = reinterpret_cast<float*>(pidx + cap);
+  float* cQ = cK + cap;
+  float* wsm = reinterpret_cast<float*>(sKQ);                // [N][128], after the MMAs are done
+
+  const int N = a.N, H = a.H;
+  const int b = blockIdx.x / H, h = blockIdx.x % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  if (tid == 0) {
+    mbar_init(&hd.tma_bar, 1);
+    mbar_init(&hd.mma_bar, 1);
+    hd.fail = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(&hd.tmem_base, tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = hd.tmem_base;
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&hd.tma_bar, kTileA + 4 * kq_bytes);
+    for (int kb = 0; kb < 2; ++kb) {
+      tma_load_2d(sA + kb * (kTileA / 2), &mS0, kb * 64, (b * H + h) * kD, &hd.tma_bar);
+      tma_load_4d(sKQ + kb * kq_bytes, &mK, kb * 64, h, 0, b, &hd.tma_bar);
+      tma_load_4d(sKQ + (2 + kb) * kq_bytes, &mQ, kb * 64, h, 0, b, &hd.tma_bar);
+    }
+  }
+
+  // Topology, log(gamma), beta and the path lists while the tiles are in flight.
+  int status = load_and_check_tree(a.parents + (size_t)b * N, N, hd.par, &hd.flag);
+  if (!status) {
+    for (int i = tid; i < N; i += kThreads) {
+      hd.depth[i] = node_depth(hd.par, i);
+      float lg = 0.f;
+      for (int j = i; j >= 0; j = hd.par[j]) lg += logf(__ldg(a.alpha + ((size_t)b * N + j) * H + h));
+      hd.lg[i] = lg;
+      hd.beta[i] = __ldg(a.beta + ((size_t)b * N + i) * H + h);
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive scan of (depth + 1)
+      int carry = 0;
+      for (int base = 0; base < N; base += 32) {
+        const int i = base + lane;
+        int x = (i < N) ? hd.depth[i] + 1 : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (i < N) hd.off[i + 1] = carry + x;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) { hd.off[0] = 0; hd.total = carry; }
+    }
+    __syncthreads();
+    if (hd.total > cap) status = TV_ERR_UNSUPPORTED;
+  }
+  if (!status) {
+    for (int i = tid; i < N; i += kThreads) {
+      int j = i;
+      for (int u = hd.depth[i]; u >= 0; --u) { pidx[hd.off[i] + u] = j; j = hd.par[j]; }
+    }
+  }
+  // The tiles must have landed before anything reads them -- or before the CTA may exit.
+  if (!mbar_wait(&hd.tma_bar, 0)) hd.fail = 1;
+  __syncthreads();
+  const bool run = !status && !hd.fail;
+
+  if (run && tid == 0) {
+    tc_fence_after();
+    const uint32_t idesc = idesc_bf16_f32(128, Npad);
+    const uint32_t a0 = smem_addr(sA), kq0 = smem_addr(sKQ);
+    for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t ad = sw128_desc(a0 + kb * (kTileA / 2) + ks * 32);
+        const uint64_t bk = sw128_desc(kq0 + kb * kq_bytes + ks * 32);
+        const uint64_t bq = sw128_desc(kq0 + (2 + kb) * kq_bytes + ks * 32);
+        const uint32_t acc = (kb | ks) ? 1u : 0u;
+        mma_bf16(tmem, ad, bk, idesc, acc);
+        mma_bf16(tmem + (uint32_t)Npad, ad, bq, idesc, acc);
+      }
+    }
+    mma_commit(&hd.mma_bar);
+  }
+
+  if (run) {
+    // Coefficients c_ij = beta_i Gamma_ij (k_i.k_j) (strict ancestors) and
+    // e_ij = q_scale Gamma_ij (q_i.k_j) (path incl. i), one warp per node, from the swizzled
+    // tiles: lane l holds elements 4l..4l+3.
+    const int kb = lane / 16, chunk = (lane % 16) / 2, half = lane & 1;
+    auto elem4 = [&](int region, int n, float* x) {
+      const unsigned char* p = sKQ + (region * 2 + kb) * kq_bytes + n * 128 + ((chunk ^ (n & 7)) << 4) + 8 * half;
+      unpack4(*reinterpret_cast<const uint2*>(p), x);
+    };
+    for (int i = warp; i < N; i += kThreads / 32) {
+      float ki[4], qi[4];
+      elem4(0, i, ki);
+      elem4(1, i, qi);
+      const int d = hd.depth[i], o = hd.off[i];
+      for (int t = 0; t <= d; ++t) {
+        const int j = pidx[o + t];
+        float kj[4];
+        elem4(0, j, kj);
+        float kk = 0.f, qk = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kk = fmaf(ki[e], kj[e], kk);
+          qk = fmaf(qi[e], kj[e], qk);
+        }
+        kk = group_sum<32>(kk);
+        qk = group_sum<32>(qk);
+        if (lane == 0) {
+          const float G = expf(hd.lg[i] - hd.lg[j]);
+          cK[o + t] = (t < d) ? hd.beta[i] * G * kk : 0.f;
+          cQ[o + t] = a.q_scale * G * qk;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (run && !mbar_wait(&hd.mma_bar, 0)) hd.fail = 1;
+  tc_fence_after();
+  __syncthreads();
+
+  if (run && !hd.fail) {
+    const bf16* __restrict__ v = static_cast<const bf16*>(a.v);
+    bf16* __restrict__ out = static_cast<bf16*>(a.out);
+    const int r = tid;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const float q_scale = a.q_scale;
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      float dK[16], dQ[16], vv[16];
+      tmem_ld16(tmem + lane_base + (uint32_t)c0, dK);
+      tmem_ld16(tmem + lane_base + (uint32_t)(Npad + c0), dQ);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        vv[j] = (c0 + j < N) ? to_f32(v[(((size_t)b * N + c0 + j) * H + h) * kD + r]) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int i = c0 + j;
+        if (i < N) {
+          const float gam = expf(hd.lg[i]);
+          const int d = hd.depth[i], o = hd.off[i];
+          float w = hd.beta[i] * (vv[j] - gam * dK[j]);
+          for (int t = 0; t < d; ++t) w -= cK[o + t] * wsm[pidx[o + t] * kD + r];
+          wsm[i * kD + r] = w;
+          float ov = q_scale * gam * dQ[j];
+          for (int t = 0; t <= d; ++t) ov = fmaf(cQ[o + t], wsm[pidx[o + t] * kD + r], ov);
+          const size_t ni = ((size_t)b * N + i) * H + h;
+          out[ni * kD + r] = from_f32<bf16>(ov);
+          pseudo_v[ni * kD + r] = w;
+        }
+      }
+    }
+    for (int i = tid; i < N; i += kThreads) log_gamma[((size_t)b * N + i) * H + h] = hd.lg[i];
+  }
+  if (h == 0 && tid == 0) a.err[b] = status ? status : (hd.fail ? TV_ERR_TIMEOUT : 0);
+  if (hd.fail && tid == 0) {  // a wait gave up: let in-flight copies and MMAs drain (bounded)
+    mbar_wait(&hd.tma_bar, 0);
+    if (!status) mbar_wait(&hd.mma_bar, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, tmem_cols);
+}
+
+}  // namespace
+
+bool gdn_wy_tc_supported(const GdnArgs& a) {
+  return a.io == TV_BF16 && a.state == TV_BF16 && a.dk == kD && a.dv == kD;
+}
+
+cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s) {
+  const int Npad = (a.N + 15) / 16 * 16;
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * Npad)) cols <<= 1;
+  int cap = a.N * (a.N + 1) / 2;
+  if (cap > kPathCap) cap = kPathCap;
+  size_t smem = 1024 + kTileA + (size_t)4 * Npad * 128 + sizeof(TcHead) + (size_t)cap * 12;
+  auto kern = gdn_wy_tc_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  // TMEM: the CTAs resident on one SM must fit in its 512 columns; pad shared memory if needed.
+  for (;;) {
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    if ((uint32_t)occ * cols <= 512u || smem >= 227 * 1024) break;
+    smem += 8 * 1024;
+    if (smem > 227 * 1024) smem = 227 * 1024;
+  }
+  CUtensorMap mS0, mK, mQ;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.B * a.H * kD};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!make_map_bf16_sw128(&mS0, a.S0, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)a.H, (cuuint64_t)a.N, (cuuint64_t)a.B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)a.H * kD * 2, (cuuint64_t)a.N * a.H * kD * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)Npad, 1};
+    if (!make_map_bf16_sw128(&mK, a.k, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16_sw128(&mQ, a.q, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  kern<<<a.B * a.H, kThreads, smem, s>>>(a, pseudo_v, log_gamma, cap, Npad, cols, mS0, mK, mQ);
+  return cudaGetLastError();
+}
+
+}  // namespace tv

@@ -30,10 +30,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ vector memory ops
-// NE contiguous elements <-> NE floats.  NE * sizeof(T) must be a multiple of 16 and the
-// address 16-byte aligned.
+// NE contiguous elements <-> NE floats.  NE is a multiple of 4; the address is aligned to
+// 4 * sizeof(T) bytes (16 for fp32, 8 for bf16) and, for bf16 with NE >= 8, to 16 bytes.
+__device__ __forceinline__ void unpack8(uint4 t, float* o) {
+  o[0] = bf16lo(t.x); o[1] = bf16hi(t.x); o[2] = bf16lo(t.y); o[3] = bf16hi(t.y);
+  o[4] = bf16lo(t.z); o[5] = bf16hi(t.z); o[6] = bf16lo(t.w); o[7] = bf16hi(t.w);
+}
+__device__ __forceinline__ void unpack4(uint2 t, float* o) {
+  o[0] = bf16lo(t.x); o[1] = bf16hi(t.x); o[2] = bf16lo(t.y); o[3] = bf16hi(t.y);
+}
+__device__ __forceinline__ uint4 pack8(const float* i) {
+  return make_uint4(pack_bf16x2(i[0], i[1]), pack_bf16x2(i[2], i[3]), pack_bf16x2(i[4], i[5]),
+                    pack_bf16x2(i[6], i[7]));
+}
+__device__ __forceinline__ uint2 pack4(const float* i) {
+  return make_uint2(pack_bf16x2(i[0], i[1]), pack_bf16x2(i[2], i[3]));
+}
+
 template <int NE>
 __device__ __forceinline__ void load_vec(const float* __restrict__ p, float* out) {
+  static_assert(NE % 4 == 0, "vector of 4");
 #pragma unroll
   for (int j = 0; j < NE / 4; ++j) {
     float4 t = __ldg(reinterpret_cast<const float4*>(p) + j);
@@ -42,18 +58,15 @@ __device__ __forceinline__ void load_vec(const float* __restrict__ p, float* out
 }
 template <int NE>
 __device__ __forceinline__ void load_vec(const bf16* __restrict__ p, float* out) {
+  static_assert(NE % 4 == 0, "vector of 4");
 #pragma unroll
-  for (int j = 0; j < NE / 8; ++j) {
-    uint4 t = __ldg(reinterpret_cast<const uint4*>(p) + j);
-    out[8 * j + 0] = bf16lo(t.x); out[8 * j + 1] = bf16hi(t.x);
-    out[8 * j + 2] = bf16lo(t.y); out[8 * j + 3] = bf16hi(t.y);
-    out[8 * j + 4] = bf16lo(t.z); out[8 * j + 5] = bf16hi(t.z);
-    out[8 * j + 6] = bf16lo(t.w); out[8 * j + 7] = bf16hi(t.w);
-  }
+  for (int j = 0; j < NE / 8; ++j) unpack8(__ldg(reinterpret_cast<const uint4*>(p) + j), out + 8 * j);
+  if constexpr (NE % 8 == 4) unpack4(__ldg(reinterpret_cast<const uint2*>(p + NE - 4)), out + NE - 4);
 }
-// Plain (coherent) loads, for data written earlier by the same kernel.
+// Plain (coherent) loads, for data written earlier by the same kernel or call sequence.
 template <int NE>
 __device__ __forceinline__ void load_vec_rw(const float* p, float* out) {
+  static_assert(NE % 4 == 0, "vector of 4");
 #pragma unroll
   for (int j = 0; j < NE / 4; ++j) {
     float4 t = reinterpret_cast<const float4*>(p)[j];
@@ -62,52 +75,40 @@ __device__ __forceinline__ void load_vec_rw(const float* p, float* out) {
 }
 template <int NE>
 __device__ __forceinline__ void load_vec_rw(const bf16* p, float* out) {
+  static_assert(NE % 4 == 0, "vector of 4");
 #pragma unroll
-  for (int j = 0; j < NE / 8; ++j) {
-    uint4 t = reinterpret_cast<const uint4*>(p)[j];
-    out[8 * j + 0] = bf16lo(t.x); out[8 * j + 1] = bf16hi(t.x);
-    out[8 * j + 2] = bf16lo(t.y); out[8 * j + 3] = bf16hi(t.y);
-    out[8 * j + 4] = bf16lo(t.z); out[8 * j + 5] = bf16hi(t.z);
-    out[8 * j + 6] = bf16lo(t.w); out[8 * j + 7] = bf16hi(t.w);
-  }
+  for (int j = 0; j < NE / 8; ++j) unpack8(reinterpret_cast<const uint4*>(p)[j], out + 8 * j);
+  if constexpr (NE % 8 == 4) unpack4(*reinterpret_cast<const uint2*>(p + NE - 4), out + NE - 4);
 }
 
 // Streaming stores (evict-first): outputs that are not re-read by this kernel.
 template <int NE>
 __device__ __forceinline__ void store_vec_cs(float* p, const float* in) {
+  static_assert(NE % 4 == 0, "vector of 4");
 #pragma unroll
   for (int j = 0; j < NE / 4; ++j)
     __stcs(reinterpret_cast<float4*>(p) + j, make_float4(in[4 * j], in[4 * j + 1], in[4 * j + 2], in[4 * j + 3]));
 }
 template <int NE>
 __device__ __forceinline__ void store_vec_cs(bf16* p, const float* in) {
+  static_assert(NE % 4 == 0, "vector of 4");
 #pragma unroll
-  for (int j = 0; j < NE / 8; ++j) {
-    uint4 t;
-    t.x = pack_bf16x2(in[8 * j + 0], in[8 * j + 1]);
-    t.y = pack_bf16x2(in[8 * j + 2], in[8 * j + 3]);
-    t.z = pack_bf16x2(in[8 * j + 4], in[8 * j + 5]);
-    t.w = pack_bf16x2(in[8 * j + 6], in[8 * j + 7]);
-    __stcs(reinterpret_cast<uint4*>(p) + j, t);
-  }
+  for (int j = 0; j < NE / 8; ++j) __stcs(reinterpret_cast<uint4*>(p) + j, pack8(in + 8 * j));
+  if constexpr (NE % 8 == 4) __stcs(reinterpret_cast<uint2*>(p + NE - 4), pack4(in + NE - 4));
 }
 template <int NE>
 __device__ __forceinline__ void store_vec(float* p, const float* in) {
+  static_assert(NE % 4 == 0, "vector of 4");
 #pragma unroll
   for (int j = 0; j < NE / 4; ++j)
     reinterpret_cast<float4*>(p)[j] = make_float4(in[4 * j], in[4 * j + 1], in[4 * j + 2], in[4 * j + 3]);
 }
 template <int NE>
 __device__ __forceinline__ void store_vec(bf16* p, const float* in) {
+  static_assert(NE % 4 == 0, "vector of 4");
 #pragma unroll
-  for (int j = 0; j < NE / 8; ++j) {
-    uint4 t;
-    t.x = pack_bf16x2(in[8 * j + 0], in[8 * j + 1]);
-    t.y = pack_bf16x2(in[8 * j + 2], in[8 * j + 3]);
-    t.z = pack_bf16x2(in[8 * j + 4], in[8 * j + 5]);
-    t.w = pack_bf16x2(in[8 * j + 6], in[8 * j + 7]);
-    reinterpret_cast<uint4*>(p)[j] = t;
-  }
+  for (int j = 0; j < NE / 8; ++j) reinterpret_cast<uint4*>(p)[j] = pack8(in + 8 * j);
+  if constexpr (NE % 8 == 4) *reinterpret_cast<uint2*>(p + NE - 4) = pack4(in + NE - 4);
 }
 
 // ------------------------------------------------------------------ reductions

@@ -32,7 +32,12 @@ cudaError_t launch_tree_prepare(const int32_t* parents, int B, int N, int32_t* d
 
 cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, cudaStream_t s);
 
+// TreeWY verify: tcgen05 kernel for bf16 I/O and state with dk = dv = 128, CUDA-core kernel
+// for every other supported shape.
 cudaError_t launch_gdn_wy(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s);
+bool gdn_wy_tc_supported(const GdnArgs& a);
+cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s);
+cudaError_t launch_gdn_wy_simt(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s);
 
 struct CommitArgs {
   int mode;
