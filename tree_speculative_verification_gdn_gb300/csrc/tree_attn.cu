@@ -6,9 +6,11 @@
 //                 every block-table entry the call touches; err[b] is final after it.
 //   2. rope    -- per node: rotate q (into the workspace, bf16) and k at prefix_len + depth,
 //                 write rotated k and v into the node's cache slot prefix_len + i.
-//   3. partial -- split-KV: each CTA takes one (sequence, KV head, key chunk, 32 query rows)
+//   3. partial -- split-KV: each CTA takes one (sequence, KV head, key chunk, query-row tile)
 //                 and runs an online softmax over its chunk of logical slots, masking the node
 //                 slots with the tree mask; writes (max, sum, unnormalised output) per row.
+//                 Head dims 128 and 256 run on the tensor cores (tree_attn_tc.cu); the CUDA-core
+//                 kernel below covers the rest.
 //   4. combine -- merges the chunks of every (sequence, node, query head).
 // Query rows of one KV head are (node, group member) pairs, so K/V of a chunk is shared by
 // every query head of the group.
@@ -279,7 +281,10 @@ cudaError_t launch_tree_attn(const AttnArgs& a, void* workspace, size_t workspac
   attn_rope_kernel<<<a.B * a.N, 128, 0, s>>>(a, reinterpret_cast<bf16*>(ws + p.off_qrot));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (a.hd == 64) e = launch_partial<64>(a, p, ws, s);
+  if (attn_tc_supported(a))
+    e = launch_attn_partial_tc(a, ws + p.off_qrot, reinterpret_cast<float*>(ws + p.off_ml),
+                               reinterpret_cast<float*>(ws + p.off_acc), p.chunk, p.nsplit, s);
+  else if (a.hd == 64) e = launch_partial<64>(a, p, ws, s);
   else if (a.hd == 128) e = launch_partial<128>(a, p, ws, s);
   else e = launch_partial<256>(a, p, ws, s);
   if (e != cudaSuccess) return e;

@@ -1,0 +1,366 @@
+// Split-KV tree attention partials on the 5th-generation tensor cores (bf16, head dim 128/256).
+//
+// Same contract as the CUDA-core partial kernel in tree_attn.cu (handbook chapter
+// 树形草稿与 EAGLE, §实现, forward_with_mask): one CTA takes one (sequence, KV head, key chunk,
+// tile of 128 query rows) -- query rows are (node, group member) pairs that share the KV head --
+// and leaves the chunk's running max, sum and unnormalised output per row for the combine
+// kernel.  Roles inside the CTA:
+//   warp 4      TMA producer: the rotated queries once, then K and V tiles of 64 keys (four
+//               16-token pages per tile, reached through the block table) into a 2-stage ring;
+//   warp 5      MMA issuer: S = Q K^T (M=128, N=64, K=head dim) into one of two TMEM S buffers,
+//               then O += P V (M=128, N=head dim, K=64, V read as an MN-major operand) into
+//               the TMEM accumulator;
+//   warps 0-3   softmax, one query row per thread (TMEM lane = row): tree mask on the node
+//               slots, running max in log2 units, P = 2^(s - m) in bf16 into shared memory.
+// The running max is raised lazily: only when a row's tile max exceeds it by more than 2^8,
+// in which case the warp rescales its rows of O in TMEM after the previous PV has completed.
+// Keys past the chunk end are masked; V rows past the sequence end are zeroed in shared memory
+// before PV, so unused cache contents never reach the accumulator.
+#include "tv_async.cuh"
+#include "tv_common.cuh"
+#include "tv_internal.h"
+#include "tv_tc.cuh"
+#include "tv_tma_host.h"
+
+namespace tv {
+namespace {
+
+constexpr int KT = 64;            // keys per tile
+constexpr int kRows = 128;        // query rows per CTA
+constexpr int kThreads = 192;     // warps 0-3 softmax, warp 4 TMA, warp 5 MMA
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescale = 8.0f;  // log2 headroom of the lazily raised running max
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[2];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int HD>
+struct Layout {
+  static constexpr uint32_t QCHUNK = kRows * 128;    // one 64-column chunk of Q
+  static constexpr uint32_t KVCHUNK = KT * 128;      // one 64-column chunk of a K or V tile
+  static constexpr uint32_t KVB = HD / 64 * KVCHUNK; // one K (or V) tile
+  static constexpr uint32_t PB = kRows * KT * 2;     // one P tile
+  static constexpr uint32_t Q = 0;
+  static constexpr uint32_t K0 = Q + HD / 64 * QCHUNK;
+  static constexpr uint32_t V0 = K0 + 2 * KVB;
+  static constexpr uint32_t P0 = V0 + 2 * KVB;
+  static constexpr uint32_t BARS = P0 + 2 * PB;
+  static constexpr uint32_t TOTAL = BARS + 128;
+  static constexpr uint32_t TMEM_COLS = (HD + 2 * KT <= 256) ? 256 : 512;
+};
+
+// Bounded mbarrier wait that also gives up once another role has flagged an abort.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if (it > 64) {
+      __nanosleep(64);
+      if ((it & 255) == 0 && *abort) return false;
+    }
+  }
+  *abort = 1;
+  return false;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_partial_tc_kernel(AttnArgs a, float* __restrict__ ml, float* __restrict__ acc, int chunk, int nsplit,
+                           int mtiles, int npt, const __grid_constant__ CUtensorMap mQ,
+                           const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV) {
+  using L = Layout<HD>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  Bars& bar = *reinterpret_cast<Bars*>(sm + L::BARS);
+  volatile int* abort = &bar.abort;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  const int b = blockIdx.y;
+  int x = blockIdx.x;
+  const int split = x % nsplit;
+  x /= nsplit;
+  const int mt = x % mtiles;
+  const int kvh = x / mtiles;
+  if (a.err[b]) return;
+  const int N = a.N, P = a.prefix_len[b], total = P + N;
+  const int lo = split * chunk;
+  if (lo >= total) return;
+  const int hi = min(total, lo + chunk);
+  const int T = (hi - lo + KT - 1) / KT;
+  const int G = a.Hq / a.Hkv, R = G * N;
+
+  if (tid == 0) {
+    mbar_init(&bar.q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar.kv_full[s], 1);
+      mbar_init(&bar.s_full[s], 1);
+      mbar_init(&bar.p_full[s], kRows);
+      mbar_init(&bar.pv_done[s], 1);
+    }
+    mbar_init(&bar.drain, 1);
+    bar.abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 5) tmem_alloc(&bar.tmem_base, L::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tO = bar.tmem_base;          // columns [0, HD): output accumulator
+  const uint32_t tS = bar.tmem_base + HD;     // columns [HD, HD + 2 KT): two S buffers
+  unsigned char* sQ = sm + L::Q;
+  int issued = 0;  // K/V tiles whose loads the producer started
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(HD * G * npt * 2));
+      for (int c = 0; c < HD / 64; ++c) tma_load_5d(sQ + c * L::QCHUNK, &mQ, c * 64, 0, kvh, mt * npt, b, &bar.q_full);
+      const int last_lb = (total - 1) / 16;
+      const int* table = a.block_table + (size_t)b * a.max_blocks;
+      for (int j = 0; j < T; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !wait_or_abort(&bar.pv_done[st], ((j - 2) >> 1) & 1, abort)) break;
+        mbar_arrive_expect_tx(&bar.kv_full[st], 2 * L::KVB);
+        issued = j + 1;
+        const int lb0 = (lo + j * KT) / 16;
+        for (int p = 0; p < KT / 16; ++p) {
+          const int blk = table[min(lb0 + p, last_lb)];
+          for (int c = 0; c < HD / 64; ++c) {
+            tma_load_4d(sm + L::K0 + st * L::KVB + c * L::KVCHUNK + p * 2048, &mK, c * 64, 0, kvh, blk,
+                        &bar.kv_full[st]);
+            tma_load_4d(sm + L::V0 + st * L::KVB + c * L::KVCHUNK + p * 2048, &mV, c * 64, 0, kvh, blk,
+                        &bar.kv_full[st]);
+          }
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16_f32(128, KT), idO = idesc_bf16_f32(128, HD, true);
+      const uint32_t q0 = smem_addr(sQ);
+      auto issue_pv = [&](int pj) {
+        const int ps = pj & 1;
+        if (!wait_or_abort(&bar.p_full[ps], (pj >> 1) & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t p0 = smem_addr(sm + L::P0 + ps * L::PB), v0 = smem_addr(sm + L::V0 + ps * L::KVB);
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk)
+          mma_bf16(tO, sw128_desc(p0 + kk * 32), sw128_mn_desc(v0 + kk * 2048, L::KVCHUNK), idO,
+                   (pj > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar.pv_done[ps]);
+        return true;
+      };
+      bool ok = wait_or_abort(&bar.q_full, 0, abort);
+      for (int j = 0; ok && j < T; ++j) {
+        const int st = j & 1;
+        if (!wait_or_abort(&bar.kv_full[st], (j >> 1) & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k0 = smem_addr(sm + L::K0 + st * L::KVB);
+        for (int c = 0; c < HD / 64; ++c) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tS + st * KT, sw128_desc(q0 + c * L::QCHUNK + ks * 32), sw128_desc(k0 + c * L::KVCHUNK + ks * 32),
+                     idS, (c | ks) ? 1u : 0u);
+        }
+        mma_commit(&bar.s_full[st]);
+        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok) issue_pv(T - 1);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax, one row per thread
+    const int r = tid;
+    const int node = mt * npt + r / G, g = r % G;
+    const bool active = (r < G * npt) && node < N;
+    uint32_t mb[TV_MAX_NODES / 32];
+#pragma unroll
+    for (int w = 0; w < TV_MAX_NODES / 32; ++w) mb[w] = 0;
+    if (active) {
+      const int32_t* par = a.parents + (size_t)b * N;
+      for (int j = node; j >= 0; j = par[j]) {
+#pragma unroll
+        for (int w = 0; w < TV_MAX_NODES / 32; ++w)
+          if ((j >> 5) == w) mb[w] |= 1u << (j & 31);
+      }
+    }
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const float scale = a.sm_scale * kLog2e;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      const int st = j & 1;
+      if (!wait_or_abort(&bar.s_full[st], (j >> 1) & 1, abort)) { ok = false; break; }
+      tc_fence_after();
+      float s[KT];
+#pragma unroll
+      for (int q4 = 0; q4 < KT / 16; ++q4) tmem_ld16(tS + lane_base + st * KT + q4 * 16, s + q4 * 16);
+      const int base = lo + j * KT;
+      float mx = -INFINITY;
+      if (active && base + KT <= hi && base + KT <= P) {  // whole tile is visible prefix
+#pragma unroll
+        for (int c = 0; c < KT; ++c) {
+          s[c] *= scale;
+          mx = fmaxf(mx, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < KT; ++c) {
+          const int slot = base + c;
+          bool vis = active && slot < hi;
+          if (vis && slot >= P) {
+            const int n = slot - P;
+            uint32_t word = 0;
+#pragma unroll
+            for (int w = 0; w < TV_MAX_NODES / 32; ++w) word = ((n >> 5) == w) ? mb[w] : word;
+            vis = (word >> (n & 31)) & 1u;
+          }
+          s[c] = vis ? s[c] * scale : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+      }
+      const bool raise = mx > m_used + kRescale;
+      const bool rescale_o = raise && m_used != -INFINITY;
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        // O holds earlier tiles: wait for the last PV, then scale this warp's rows in TMEM.
+        if (!wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) { ok = false; break; }
+        tc_fence_after();
+        const float f = rescale_o ? exp2f(m_used - mx) : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < HD; c0 += 16) {
+          float o16[16];
+          tmem_ld16(tO + lane_base + c0, o16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o16[e] *= f;
+          tmem_st16(tO + lane_base + c0, o16);
+        }
+      }
+      if (raise) {
+        l = rescale_o ? l * exp2f(m_used - mx) : 0.f;
+        m_used = mx;
+      }
+      if (j >= 2 && !wait_or_abort(&bar.pv_done[st], ((j - 2) >> 1) & 1, abort)) { ok = false; break; }
+      unsigned char* prow = sm + L::P0 + st * L::PB + r * 128;
+      float psum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float sv = s[ch * 8 + e];
+          pv[e] = (sv == -INFINITY) ? 0.f : exp2f(sv - m_used);
+        }
+        const uint4 packed = pack8(pv);
+        float back[8];
+        unpack8(packed, back);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) psum += back[e];
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = packed;
+      }
+      l += psum;
+      if (base + KT > hi) {  // zero V rows past the chunk end: their P is 0 but contents are unknown
+        if (!wait_or_abort(&bar.kv_full[st], (j >> 1) & 1, abort)) { ok = false; break; }
+        const int first = hi - base;
+        unsigned char* v0 = sm + L::V0 + st * L::KVB;
+        for (int idx = r; idx < (KT - first) * (HD / 8); idx += kRows) {
+          const int kr = first + idx / (HD / 8), rem = idx % (HD / 8);
+          *reinterpret_cast<uint4*>(v0 + (rem / 8) * L::KVCHUNK + kr * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(&bar.p_full[st]);
+    }
+    if (ok && wait_or_abort(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort)) {
+      tc_fence_after();
+      const size_t row = (((size_t)b * a.Hkv + kvh) * nsplit + split) * R + (size_t)node * G + g;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 16) {
+        float o16[16];
+        tmem_ld16(tO + lane_base + c0, o16);
+        if (active) {
+          float4* dst = reinterpret_cast<float4*>(acc + row * HD + c0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_float4(o16[4 * e], o16[4 * e + 1], o16[4 * e + 2], o16[4 * e + 3]);
+        }
+      }
+      if (active) {
+        ml[row * 2] = m_used;
+        ml[row * 2 + 1] = l;
+      }
+    }
+  }
+  __syncthreads();
+  if (bar.abort) {  // drain everything this CTA started before its TMEM and shared memory go away
+    if (warp == 5 && lane == 0) {
+      mma_commit(&bar.drain);
+      mbar_wait(&bar.drain, 0);
+    }
+    if (warp == 4 && lane == 0) {
+      mbar_wait(&bar.q_full, 0);
+      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) mbar_wait(&bar.kv_full[j & 1], (j >> 1) & 1);
+    }
+    if (tid == 0) a.err[b] = TV_ERR_TIMEOUT;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(bar.tmem_base, L::TMEM_COLS);
+}
+
+template <int HD>
+cudaError_t launch_t(const AttnArgs& a, const void* qrot, float* ml, float* acc, int chunk, int nsplit,
+                     cudaStream_t s) {
+  using L = Layout<HD>;
+  const int G = a.Hq / a.Hkv;
+  const int npt = kRows / G;                     // nodes per tile of 128 query rows
+  const int mtiles = (a.N + npt - 1) / npt;
+  CUtensorMap mQ, mK, mV;
+  {
+    // rotated queries [B][N][Hkv][G][hd]
+    const cuuint64_t dims[5] = {(cuuint64_t)HD, (cuuint64_t)G, (cuuint64_t)a.Hkv, (cuuint64_t)a.N, (cuuint64_t)a.B};
+    const cuuint64_t strides[4] = {(cuuint64_t)HD * 2, (cuuint64_t)G * HD * 2, (cuuint64_t)a.Hq * HD * 2,
+                                   (cuuint64_t)a.N * a.Hq * HD * 2};
+    const cuuint32_t box[5] = {64, (cuuint32_t)G, 1, (cuuint32_t)npt, 1};
+    if (!make_map_bf16_sw128(&mQ, qrot, 5, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    // caches [num_blocks][Hkv][16][hd]
+    const cuuint64_t dims[4] = {(cuuint64_t)HD, 16, (cuuint64_t)a.Hkv, (cuuint64_t)a.num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)HD * 2, (cuuint64_t)16 * HD * 2, (cuuint64_t)a.Hkv * 16 * HD * 2};
+    const cuuint32_t box[4] = {64, 16, 1, 1};
+    if (!make_map_bf16_sw128(&mK, a.k_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16_sw128(&mV, a.v_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  const size_t smem = L::TOTAL + 1024;
+  auto kern = attn_partial_tc_kernel<HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(nsplit * mtiles * a.Hkv, a.B);
+  kern<<<grid, kThreads, smem, s>>>(a, ml, acc, chunk, nsplit, mtiles, npt, mQ, mK, mV);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_tc_supported(const AttnArgs& a) {
+  const int G = a.Hq / a.Hkv;
+  return (a.hd == 128 || a.hd == 256) && G >= 1 && G <= 128 && (128 % G) == 0 && a.block_size == 16;
+}
+
+cudaError_t launch_attn_partial_tc(const AttnArgs& a, const void* qrot, float* ml, float* acc, int chunk,
+                                   int nsplit, cudaStream_t s) {
+  if (chunk % KT) return cudaErrorInvalidValue;
+  return a.hd == 128 ? launch_t<128>(a, qrot, ml, acc, chunk, nsplit, s)
+                     : launch_t<256>(a, qrot, ml, acc, chunk, nsplit, s);
+}
+
+}  // namespace tv

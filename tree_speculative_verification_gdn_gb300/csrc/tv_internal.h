@@ -72,6 +72,11 @@ struct AttnArgs {
   int32_t* err;
 };
 size_t attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int block_size);
+// Split-KV partials on the tensor cores (head dim 128 or 256, Hq/Hkv dividing 128); the
+// CUDA-core partial kernel covers every other supported shape.
+bool attn_tc_supported(const AttnArgs& a);
+cudaError_t launch_attn_partial_tc(const AttnArgs& a, const void* qrot, float* ml, float* acc, int chunk,
+                                   int nsplit, cudaStream_t s);
 cudaError_t launch_tree_attn(const AttnArgs& a, void* workspace, size_t workspace_bytes,
                              cudaStream_t s);
 
