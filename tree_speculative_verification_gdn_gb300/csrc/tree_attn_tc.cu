@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       const int st = j & 1;
-      if (!wait_or_abort(&bar.s_full[st], (j >> 1) & 1, abort)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, wait_or_abort(&bar.s_full[st], (j >> 1) & 1, abort))) { ok = false; break; }
       tc_fence_after();
       float s[KT];
 #pragma unroll
@@ -231,7 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool rescale_o = raise && m_used != -INFINITY;
       if (__any_sync(0xffffffffu, rescale_o)) {
         // O holds earlier tiles: wait for the last PV, then scale this warp's rows in TMEM.
-        if (!wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const float f = rescale_o ? exp2f(m_used - mx) : 1.f;
 #pragma unroll 1
@@ -247,7 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = rescale_o ? l * exp2f(m_used - mx) : 0.f;
         m_used = mx;
       }
-      if (j >= 2 && !wait_or_abort(&bar.pv_done[st], ((j - 2) >> 1) & 1, abort)) { ok = false; break; }
+      if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[st], ((j - 2) >> 1) & 1, abort))) {
+        ok = false;
+        break;
+      }
       unsigned char* prow = sm + L::P0 + st * L::PB + r * 128;
       float psum = 0.f;
 #pragma unroll
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l += psum;
       if (base + KT > hi) {  // zero V rows past the chunk end: their P is 0 but contents are unknown
-        if (!wait_or_abort(&bar.kv_full[st], (j >> 1) & 1, abort)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.kv_full[st], (j >> 1) & 1, abort))) { ok = false; break; }
         const int first = hi - base;
         unsigned char* v0 = sm + L::V0 + st * L::KVB;
         for (int idx = r; idx < (KT - first) * (HD / 8); idx += kRows) {
@@ -279,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar.p_full[st]);
     }
-    if (ok && wait_or_abort(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort)) {
+    if (ok && __all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort))) {
       tc_fence_after();
       const size_t row = (((size_t)b * a.Hkv + kvh) * nsplit + split) * R + (size_t)node * G + g;
 #pragma unroll 1
