@@ -7,9 +7,10 @@
 // node keys and queries (B operands, N x 128 each, zero rows past N) into shared memory in the
 // 128-byte swizzle layout, one thread issues 16 MMAs (M = 128, N = Npad, K = 16) that
 // accumulate in fp32 in TMEM, and the epilogue reads row r of both products back with
-// tcgen05.ld -- row r belongs to TMEM lane r, i.e. to thread r.  Each thread then runs the
-// ancestor-list forward substitution for its row in fp32; the (node, ancestor) coefficients
-// are computed meanwhile by the four warps from the same shared-memory tiles.
+// tcgen05.ld -- row r belongs to TMEM lane r.  The (node, path entry) coefficients come from
+// the same shared-memory tiles, 8 lanes per entry.  The forward substitution then runs depth
+// level by depth level: within a level every node is independent, so two warp groups split it
+// and each warp keeps 8 nodes' loads in flight.
 #include "tv_async.cuh"
 #include "tv_common.cuh"
 #include "tv_internal.h"
@@ -19,21 +20,26 @@
 namespace tv {
 namespace {
 
-constexpr int kThreads = 128;   // one thread per state row (TMEM lane)
+constexpr int kThreads = 256;   // two warp groups; warp w reads TMEM lanes 32 (w % 4) .. + 31
 constexpr int kD = 128;         // dk = dv
 constexpr int kPathCap = 4096;  // max sum over nodes of (depth + 1)
+constexpr int kBatch = 8;       // nodes per warp in flight during the solve
 constexpr uint32_t kTileA = kD * kD * 2;  // S_0 tile bytes
 
 struct TcHead {
   uint64_t tma_bar;
   uint64_t mma_bar;
   uint32_t tmem_base;
-  int flag, total, fail;
+  int flag, total, fail, maxdepth;
   int par[TV_MAX_NODES];
   int depth[TV_MAX_NODES];
   int off[TV_MAX_NODES + 1];
   float lg[TV_MAX_NODES];
+  float gam[TV_MAX_NODES];
   float beta[TV_MAX_NODES];
+  int lvl_cnt[TV_MAX_NODES + 1];   // nodes per depth, then start of each depth level
+  int lvl_fill[TV_MAX_NODES];
+  int lvl_nodes[TV_MAX_NODES];     // nodes grouped by depth
 };
 
 __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* __restrict__ pseudo_v,
@@ -49,8 +55,8 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   unsigned char* sKQ = smem + kTileA;                        // K: 2 x Npad x 128 B, then Q: same
   const uint32_t kq_bytes = (uint32_t)Npad * 128u;           // one k-block of K or Q
   TcHead& hd = *reinterpret_cast<TcHead*>(sKQ + 4 * kq_bytes);
-  int* pidx = reinterpret_cast<int*>(&hd + 1);
-  float* cK = reinterpret_cast<float*>(pidx + cap);
+  int* pent = reinterpret_cast<int*>(&hd + 1);               // (node << 8) | path node, per entry
+  float* cK = reinterpret_cast<float*>(pent + cap);
   float* cQ = cK + cap;
   float* wsm = reinterpret_cast<float*>(sKQ);                // [N][128], after the MMAs are done
 
@@ -62,6 +68,7 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
     mbar_init(&hd.tma_bar, 1);
     mbar_init(&hd.mma_bar, 1);
     hd.fail = 0;
+    hd.maxdepth = 0;
     mbar_fence_init();
   }
   if (warp == 0) tmem_alloc(&hd.tmem_base, tmem_cols);
@@ -79,18 +86,24 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
     }
   }
 
-  // Topology, log(gamma), beta and the path lists while the tiles are in flight.
+  // Topology, log(gamma), gamma, beta, depth levels and path lists while the tiles are in flight.
   int status = load_and_check_tree(a.parents + (size_t)b * N, N, hd.par, &hd.flag);
   if (!status) {
+    for (int i = tid; i <= N; i += kThreads) hd.lvl_cnt[i] = 0;
+    __syncthreads();
     for (int i = tid; i < N; i += kThreads) {
-      hd.depth[i] = node_depth(hd.par, i);
+      const int d = node_depth(hd.par, i);
+      hd.depth[i] = d;
+      atomicMax(&hd.maxdepth, d);
+      atomicAdd(&hd.lvl_cnt[d], 1);
       float lg = 0.f;
       for (int j = i; j >= 0; j = hd.par[j]) lg += logf(__ldg(a.alpha + ((size_t)b * N + j) * H + h));
       hd.lg[i] = lg;
+      hd.gam[i] = expf(lg);
       hd.beta[i] = __ldg(a.beta + ((size_t)b * N + i) * H + h);
     }
     __syncthreads();
-    if (warp == 0) {  // exclusive scan of (depth + 1)
+    if (warp == 0) {  // exclusive scans of (depth + 1) over nodes and of node counts over depths
       int carry = 0;
       for (int base = 0; base < N; base += 32) {
         const int i = base + lane;
@@ -104,14 +117,33 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
         carry += __shfl_sync(0xffffffffu, x, 31);
       }
       if (lane == 0) { hd.off[0] = 0; hd.total = carry; }
+      carry = 0;
+      const int nl = hd.maxdepth + 1;
+      for (int base = 0; base < nl; base += 32) {
+        const int d = base + lane;
+        int x = (d < nl) ? hd.lvl_cnt[d] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (d < nl) hd.lvl_cnt[d] = carry + x;  // inclusive prefix count
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
     }
     __syncthreads();
     if (hd.total > cap) status = TV_ERR_UNSUPPORTED;
   }
   if (!status) {
+    // lvl_cnt now holds inclusive prefix counts: level d spans [lvl_cnt[d-1], lvl_cnt[d]).
+    for (int d = tid; d <= hd.maxdepth; d += kThreads) hd.lvl_fill[d] = 0;
+    __syncthreads();
     for (int i = tid; i < N; i += kThreads) {
+      const int d = hd.depth[i];
+      const int start = d ? hd.lvl_cnt[d - 1] : 0;
+      hd.lvl_nodes[start + atomicAdd(&hd.lvl_fill[d], 1)] = i;
       int j = i;
-      for (int u = hd.depth[i]; u >= 0; --u) { pidx[hd.off[i] + u] = j; j = hd.par[j]; }
+      for (int u = d; u >= 0; --u) { pent[hd.off[i] + u] = (i << 8) | j; j = hd.par[j]; }
     }
   }
   // The tiles must have landed before anything reads them -- or before the CTA may exit.
@@ -139,35 +171,42 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
 
   if (run) {
     // Coefficients c_ij = beta_i Gamma_ij (k_i.k_j) (strict ancestors) and
-    // e_ij = q_scale Gamma_ij (q_i.k_j) (path incl. i), one warp per node, from the swizzled
-    // tiles: lane l holds elements 4l..4l+3.
-    const int kb = lane / 16, chunk = (lane % 16) / 2, half = lane & 1;
-    auto elem4 = [&](int region, int n, float* x) {
-      const unsigned char* p = sKQ + (region * 2 + kb) * kq_bytes + n * 128 + ((chunk ^ (n & 7)) << 4) + 8 * half;
-      unpack4(*reinterpret_cast<const uint2*>(p), x);
+    // e_ij = q_scale Gamma_ij (q_i.k_j) (path incl. i): 8 lanes per (node, path entry) pair, each
+    // lane 16 of the 128 elements, read from the swizzled tiles.
+    const int grp = tid / 8, gl = tid % 8;
+    auto chunk8 = [&](int region, int n, int g16, float* x) {  // elements 8*g16 .. 8*g16+7 of row n
+      const int kb = g16 / 8, ch = g16 % 8;
+      const unsigned char* p = sKQ + (region * 2 + kb) * kq_bytes + n * 128 + ((ch ^ (n & 7)) << 4);
+      unpack8(*reinterpret_cast<const uint4*>(p), x);
     };
-    for (int i = warp; i < N; i += kThreads / 32) {
-      float ki[4], qi[4];
-      elem4(0, i, ki);
-      elem4(1, i, qi);
-      const int d = hd.depth[i], o = hd.off[i];
-      for (int t = 0; t <= d; ++t) {
-        const int j = pidx[o + t];
-        float kj[4];
-        elem4(0, j, kj);
-        float kk = 0.f, qk = 0.f;
+    for (int e0 = 0; e0 < hd.total; e0 += kThreads / 8) {
+      const int e = e0 + grp;
+      const bool valid = e < hd.total;
+      const int pk = valid ? pent[e] : 0;
+      const int i = pk >> 8, j = pk & 255;
+      float kk = 0.f, qk = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          kk = fmaf(ki[e], kj[e], kk);
-          qk = fmaf(qi[e], kj[e], qk);
+      for (int u = 0; u < 2; ++u) {
+        float ki[8], qi[8], kj[8];
+        chunk8(0, i, 2 * gl + u, ki);
+        chunk8(1, i, 2 * gl + u, qi);
+        chunk8(0, j, 2 * gl + u, kj);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          kk = fmaf(ki[x], kj[x], kk);
+          qk = fmaf(qi[x], kj[x], qk);
         }
-        kk = group_sum<32>(kk);
-        qk = group_sum<32>(qk);
-        if (lane == 0) {
-          const float G = expf(hd.lg[i] - hd.lg[j]);
-          cK[o + t] = (t < d) ? hd.beta[i] * G * kk : 0.f;
-          cQ[o + t] = a.q_scale * G * qk;
-        }
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) {
+        kk += __shfl_xor_sync(0xffffffffu, kk, o);
+        qk += __shfl_xor_sync(0xffffffffu, qk, o);
+      }
+      if (valid && gl == 0) {
+        const int t = e - hd.off[i];
+        const float G = expf(hd.lg[i] - hd.lg[j]);
+        cK[e] = (t < hd.depth[i]) ? hd.beta[i] * G * kk : 0.f;
+        cQ[e] = a.q_scale * G * qk;
       }
     }
   }
@@ -177,34 +216,48 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   __syncthreads();
 
   if (run && !hd.fail) {
+    // Forward substitution depth level by depth level: the nodes of one level depend only on
+    // shallower levels, so each warp takes kBatch of them at a time; the two warp groups split
+    // a level and meet at a barrier before the next.
     const bf16* __restrict__ v = static_cast<const bf16*>(a.v);
     bf16* __restrict__ out = static_cast<bf16*>(a.out);
-    const int r = tid;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const int q = warp % 4, wg = warp / 4;
+    const int r = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float q_scale = a.q_scale;
-    for (int c0 = 0; c0 < N; c0 += 16) {
-      float dK[16], dQ[16], vv[16];
-      tmem_ld16(tmem + lane_base + (uint32_t)c0, dK);
-      tmem_ld16(tmem + lane_base + (uint32_t)(Npad + c0), dQ);
+    for (int d = 0; d <= hd.maxdepth; ++d) {
+      const int s0 = d ? hd.lvl_cnt[d - 1] : 0, s1 = hd.lvl_cnt[d];
+      for (int base = s0 + wg * kBatch; base < s1; base += 2 * kBatch) {
+        uint32_t dk[kBatch], dq[kBatch];
+        float vv[kBatch];
+        int nodes[kBatch];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        vv[j] = (c0 + j < N) ? to_f32(v[(((size_t)b * N + c0 + j) * H + h) * kD + r]) : 0.f;
+        for (int x = 0; x < kBatch; ++x) {
+          const int pos = base + x;
+          nodes[x] = pos < s1 ? hd.lvl_nodes[pos] : -1;
+          const int col = nodes[x] < 0 ? 0 : nodes[x];
+          dk[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)col);
+          dq[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)(Npad + col));
+          vv[x] = nodes[x] < 0 ? 0.f : to_f32(v[(((size_t)b * N + nodes[x]) * H + h) * kD + r]);
+        }
+        tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int i = c0 + j;
-        if (i < N) {
-          const float gam = expf(hd.lg[i]);
-          const int d = hd.depth[i], o = hd.off[i];
-          float w = hd.beta[i] * (vv[j] - gam * dK[j]);
-          for (int t = 0; t < d; ++t) w -= cK[o + t] * wsm[pidx[o + t] * kD + r];
+        for (int x = 0; x < kBatch; ++x) {
+          const int i = nodes[x];
+          if (i < 0) continue;
+          const float gam = hd.gam[i];
+          const int dd = hd.depth[i], o = hd.off[i];
+          float w = hd.beta[i] * (vv[x] - gam * __uint_as_float(dk[x]));
+          for (int t = 0; t < dd; ++t) w -= cK[o + t] * wsm[(pent[o + t] & 255) * kD + r];
           wsm[i * kD + r] = w;
-          float ov = q_scale * gam * dQ[j];
-          for (int t = 0; t <= d; ++t) ov = fmaf(cQ[o + t], wsm[pidx[o + t] * kD + r], ov);
+          float ov = q_scale * gam * __uint_as_float(dq[x]);
+          for (int t = 0; t <= dd; ++t) ov = fmaf(cQ[o + t], wsm[(pent[o + t] & 255) * kD + r], ov);
           const size_t ni = ((size_t)b * N + i) * H + h;
           out[ni * kD + r] = from_f32<bf16>(ov);
           pseudo_v[ni * kD + r] = w;
         }
       }
+      __syncthreads();
     }
     for (int i = tid; i < N; i += kThreads) log_gamma[((size_t)b * N + i) * H + h] = hd.lg[i];
   }

@@ -83,12 +83,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &bar.abort;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
+  // Query-row tiles of one (KV head, chunk) are adjacent so their K/V reads meet in L2.
   const int b = blockIdx.y;
   int x = blockIdx.x;
-  const int split = x % nsplit;
-  x /= nsplit;
   const int mt = x % mtiles;
-  const int kvh = x / mtiles;
+  x /= mtiles;
+  const int split = x % nsplit;
+  const int kvh = x / nsplit;
   if (a.err[b]) return;
   const int N = a.N, P = a.prefix_len[b], total = P + N;
   const int lo = split * chunk;
@@ -201,31 +202,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, wait_or_abort(&bar.s_full[st], (j >> 1) & 1, abort))) { ok = false; break; }
       tc_fence_after();
       float s[KT];
+      {
+        uint32_t raw[KT];
 #pragma unroll
-      for (int q4 = 0; q4 < KT / 16; ++q4) tmem_ld16(tS + lane_base + st * KT + q4 * 16, s + q4 * 16);
+        for (int q4 = 0; q4 < KT / 16; ++q4) tmem_ld16_nowait(tS + lane_base + st * KT + q4 * 16, raw + q4 * 16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < KT; ++c) s[c] = __uint_as_float(raw[c]);
+      }
       const int base = lo + j * KT;
+      // Visible columns of this tile for this row: the prefix part and, on node slots, the row
+      // node's ancestors and itself.
+      uint64_t vis = 0;
+      if (active) {
+        const int nprefix = min(max(min(hi, P) - base, 0), KT);     // prefix slots in the tile
+        vis = nprefix >= 64 ? ~0ull : ((1ull << nprefix) - 1ull);
+        const int node_end = min(hi - base, KT);
+        for (int c = max(nprefix, 0); c < node_end; ++c) {
+          const int n = base + c - P;
+          uint32_t word = 0;
+#pragma unroll
+          for (int w = 0; w < TV_MAX_NODES / 32; ++w) word = ((n >> 5) == w) ? mb[w] : word;
+          vis |= (uint64_t)((word >> (n & 31)) & 1u) << c;
+        }
+      }
       float mx = -INFINITY;
-      if (active && base + KT <= hi && base + KT <= P) {  // whole tile is visible prefix
 #pragma unroll
-        for (int c = 0; c < KT; ++c) {
-          s[c] *= scale;
-          mx = fmaxf(mx, s[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < KT; ++c) {
-          const int slot = base + c;
-          bool vis = active && slot < hi;
-          if (vis && slot >= P) {
-            const int n = slot - P;
-            uint32_t word = 0;
-#pragma unroll
-            for (int w = 0; w < TV_MAX_NODES / 32; ++w) word = ((n >> 5) == w) ? mb[w] : word;
-            vis = (word >> (n & 31)) & 1u;
-          }
-          s[c] = vis ? s[c] * scale : -INFINITY;
-          mx = fmaxf(mx, s[c]);
-        }
+      for (int c = 0; c < KT; ++c) {
+        s[c] = ((vis >> c) & 1ull) ? s[c] * scale : -INFINITY;
+        mx = fmaxf(mx, s[c]);
       }
       const bool raise = mx > m_used + kRescale;
       const bool rescale_o = raise && m_used != -INFINITY;
@@ -236,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const float f = rescale_o ? exp2f(m_used - mx) : 1.f;
+        const float f = rescale_o ? ex2_approx(m_used - mx) : 1.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < HD; c0 += 16) {
           float o16[16];
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (raise) {
-        l = rescale_o ? l * exp2f(m_used - mx) : 0.f;
+        l = rescale_o ? l * ex2_approx(m_used - mx) : 0.f;
         m_used = mx;
       }
       if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[st], ((j - 2) >> 1) & 1, abort))) {
@@ -262,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float sv = s[ch * 8 + e];
-          pv[e] = (sv == -INFINITY) ? 0.f : exp2f(sv - m_used);
+          // masked keys: 2^(-inf) = 0; a row with nothing visible yet keeps m_used = -inf
+          pv[e] = (m_used == -INFINITY) ? 0.f : ex2_approx(sv - m_used);
         }
         const uint4 packed = pack8(pv);
         float back[8];
