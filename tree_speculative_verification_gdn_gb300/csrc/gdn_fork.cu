@@ -10,9 +10,10 @@
 // their fp32 state on chip and walks the whole tree once, depth-first, instead of one launch
 // per depth reading every parent snapshot back from HBM.  HBM traffic is the floor: S_0 read
 // once per root, each checkpoint written once.  Each row is held by 8 lanes (dk/8 columns
-// each).  A producer warp streams every node's k, q (converted to fp32 once for the CTA's 16
-// rows), v, decay and write strength into an 8-deep shared-memory ring guarded by full/empty
-// mbarriers; the four row warps walk the tree independently, without a CTA barrier.
+// each), so a dot product costs 3 shuffles.  Every warp walks the tree on its own -- no
+// barrier inside the node loop -- with the next two nodes' k, q and v prefetched into
+// registers; the CTA's warps share one (sequence, head), so k and q come from L1 after the
+// first warp's read.
 //
 // Depth-first order visits a node's light children first and its heaviest child (largest
 // subtree) last.  A branching node pushes its state to a shared-memory slot that its later
@@ -21,27 +22,24 @@
 // light edge halves the subtree, so slots 1..7 cover every tree of <= 256 nodes (a branching
 // node has >= 3 nodes in its subtree, so it sits below at most 6 light edges); the launch
 // sizes the stack for the bound of its N (slots_for).
-#include "tv_async.cuh"
 #include "tv_common.cuh"
 #include "tv_internal.h"
-#include "tv_tc.cuh"
 
 namespace tv {
 namespace {
 
 constexpr int kLPR = 8;                 // lanes per state row
 constexpr int kRows = 16;               // state rows per CTA
-constexpr int kCompute = kLPR * kRows;  // 128 threads own the rows
-constexpr int kThreads = kCompute + 32; // plus one producer warp
+constexpr int kThreads = kLPR * kRows;  // 128
 constexpr int kSlots = 7;               // on-chip state slots 1..7 (S_0 is re-read for a root)
-constexpr int kStages = 8;              // depth of the node-input ring
 
-// The schedule the producer walks: per depth-first position t, {node, (src + 1) | (push + 1) << 8}.
+// What the node loop needs from the schedule, plus the current item's decay / write strength.
 struct Sched {
   int order[TV_MAX_NODES];   // node at each depth-first position
   int src[TV_MAX_NODES];     // where the parent state comes from: -1 registers, 0 S_0, else a slot
   int push[TV_MAX_NODES];    // slot the node's own state goes to (-1: not needed later)
-  int2 ent[TV_MAX_NODES];
+  // per depth-first position t: {node, (src + 1) | (push + 1) << 8, alpha bits, beta bits}
+  int4 ent[TV_MAX_NODES];
   int flag, maxslot, pad0, pad1;
 };
 // Scratch of the schedule builder; it lives in the (not yet used) state-stack region.
@@ -131,209 +129,172 @@ __host__ __device__ constexpr int slots_for(int n) {
   return L + 1;
 }
 
-// One node's inputs for the CTA's (sequence, head, row slab), written by the producer warp in
-// fp32: k and q (all DK columns), the slab's 16 entries of v, decay, write strength and the
-// node's schedule entry.
-template <int DK>
-struct Stage {
-  float k[DK];
-  float q[DK];
-  float v[kRows];
-  float alpha, beta;
-  int node, code;
+// A node's inputs for one lane, as stored (bf16 pairs or fp32), prefetched into registers.
+template <typename TIO, int CPL>
+struct Raw;
+template <int CPL>
+struct Raw<bf16, CPL> {
+  uint32_t k[CPL / 2], q[CPL / 2];
+  float v;
+  int4 e;  // schedule entry of the node
+  __device__ __forceinline__ void load(const bf16* kp, const bf16* qp, const bf16* vp) {
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(kp) + j);
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp) + j);
+      k[4 * j] = a.x; k[4 * j + 1] = a.y; k[4 * j + 2] = a.z; k[4 * j + 3] = a.w;
+      q[4 * j] = c.x; q[4 * j + 1] = c.y; q[4 * j + 2] = c.z; q[4 * j + 3] = c.w;
+    }
+    v = to_f32(__ldg(vp));
+  }
+  __device__ __forceinline__ float kf(int e) const { return (e & 1) ? bf16hi(k[e >> 1]) : bf16lo(k[e >> 1]); }
+  __device__ __forceinline__ float qf(int e) const { return (e & 1) ? bf16hi(q[e >> 1]) : bf16lo(q[e >> 1]); }
 };
-
-template <typename TIO, int DK>
-__device__ __forceinline__ void load_row_part(const TIO* p, float* out);  // DK/32 elements
-template <>
-__device__ __forceinline__ void load_row_part<bf16, 128>(const bf16* p, float* out) {
-  unpack4(__ldg(reinterpret_cast<const uint2*>(p)), out);
-}
-template <>
-__device__ __forceinline__ void load_row_part<bf16, 64>(const bf16* p, float* out) {
-  const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(p));
-  out[0] = bf16lo(w); out[1] = bf16hi(w);
-}
-template <>
-__device__ __forceinline__ void load_row_part<float, 128>(const float* p, float* out) {
-  const float4 t = __ldg(reinterpret_cast<const float4*>(p));
-  out[0] = t.x; out[1] = t.y; out[2] = t.z; out[3] = t.w;
-}
-template <>
-__device__ __forceinline__ void load_row_part<float, 64>(const float* p, float* out) {
-  const float2 t = __ldg(reinterpret_cast<const float2*>(p));
-  out[0] = t.x; out[1] = t.y;
-}
+template <int CPL>
+struct Raw<float, CPL> {
+  float k[CPL], q[CPL];
+  float v;
+  int4 e;  // schedule entry of the node
+  __device__ __forceinline__ void load(const float* kp, const float* qp, const float* vp) {
+    load_vec<CPL>(kp, k);
+    load_vec<CPL>(qp, q);
+    v = __ldg(vp);
+  }
+  __device__ __forceinline__ float kf(int e) const { return k[e]; }
+  __device__ __forceinline__ float qf(int e) const { return q[e]; }
+};
 
 template <typename TIO, typename TS, int DK>
 __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __restrict__ states,
                                                             int ctas_per_seq, int nslots) {
-  constexpr int CPL = DK / kLPR;  // columns per consumer lane
+  constexpr int CPL = DK / kLPR;  // columns per lane
   constexpr int Q4 = CPL / 4;     // float4 per lane per slot
-  constexpr int PPL = DK / 32;    // columns per producer lane
-  constexpr int kAhead = 4;       // nodes whose loads the producer keeps in flight
-  using StageT = Stage<DK>;
   extern __shared__ __align__(128) unsigned char smem[];
   Sched& sc = *reinterpret_cast<Sched*>(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + sizeof(Sched));
-  uint64_t* empty = full + kStages;
-  StageT* ring = reinterpret_cast<StageT*>(empty + kStages);
-  float4* stack = reinterpret_cast<float4*>(ring + kStages);
+  float4* stack = reinterpret_cast<float4*>(smem + sizeof(Sched));
   BuildScratch& scratch = *reinterpret_cast<BuildScratch*>(stack);
 
   const int b = blockIdx.x / ctas_per_seq, g = blockIdx.x % ctas_per_seq;
   const int N = a.N, H = a.H, dv = a.dv;
-  const int tid = threadIdx.x, warp = tid / 32;
+  const int tid = threadIdx.x;
   int status = build_schedule(a.parents + (size_t)b * N, N, sc, scratch);
   if (!status && sc.maxslot > nslots) status = TV_ERR_UNSUPPORTED;
   if (g == 0 && tid == 0) a.err[b] = status;
   if (status) return;
-  for (int t = tid; t < N; t += kThreads) {
-    const int i = sc.order[t];
-    sc.ent[t] = make_int2(i, (sc.src[i] + 1) | ((sc.push[i] + 1) << 8));
-  }
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kCompute / 32);
-    }
-    mbar_fence_init();
-  }
-  __syncthreads();  // schedule and barriers ready; the stack region is free from here on
 
   const TIO* __restrict__ q = static_cast<const TIO*>(a.q);
   const TIO* __restrict__ k = static_cast<const TIO*>(a.k);
   const TIO* __restrict__ v = static_cast<const TIO*>(a.v);
   const TS* __restrict__ S0 = static_cast<const TS*>(a.S0);
   TIO* __restrict__ out = static_cast<TIO*>(a.out);
+  const int lane = tid % kLPR, rl = tid / kLPR;
   const int slabs = dv / kRows, items = H * slabs;
-  bool timed_out = false;
+  const float q_scale = a.q_scale;
+  const size_t node_stride = (size_t)H * dv;     // elements between consecutive nodes (out, v)
+  const size_t state_stride = node_stride * DK;  // elements between consecutive nodes (states)
+  const size_t kq_stride = (size_t)H * DK;       // elements between consecutive nodes (q, k)
 
-  if (warp == kCompute / 32) {
-    // ---------------------------------------------------------------- producer warp
-    const int lane = tid % 32;
-    uint32_t seq = 0;
-    for (int item = g; item < items; item += ctas_per_seq) {
-      const int h = item / slabs, r0 = (item % slabs) * kRows;
-      const size_t nh0 = (size_t)b * N * H + h;
-      for (int t0 = 0; t0 < N; t0 += kAhead) {
-        float kr[kAhead][PPL], qr[kAhead][PPL], vr[kAhead], ar[kAhead];
-        int2 en[kAhead];
-#pragma unroll
-        for (int u = 0; u < kAhead; ++u) {  // loads of up to kAhead nodes in flight
-          const int t = t0 + u < N ? t0 + u : N - 1;
-          en[u] = sc.ent[t];
-          const size_t nh = nh0 + (size_t)en[u].x * H;
-          load_row_part<TIO, DK>(k + nh * DK + lane * PPL, kr[u]);
-          load_row_part<TIO, DK>(q + nh * DK + lane * PPL, qr[u]);
-          vr[u] = lane < kRows ? to_f32(__ldg(v + nh * dv + r0 + lane)) : 0.f;
-          ar[u] = lane == kRows ? __ldg(a.alpha + nh) : (lane == kRows + 1 ? __ldg(a.beta + nh) : 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < kAhead; ++u) {
-          if (t0 + u >= N) break;
-          const uint32_t sq = seq + u, st = sq % kStages;
-          if (sq >= kStages && !mbar_wait(&empty[st], ((sq / kStages) - 1) & 1u)) timed_out = true;
-          StageT& S = ring[st];
-#pragma unroll
-          for (int e = 0; e < PPL; ++e) {
-            S.k[lane * PPL + e] = kr[u][e];
-            S.q[lane * PPL + e] = qr[u][e];
-          }
-          if (lane < kRows) S.v[lane] = vr[u];
-          if (lane == kRows) S.alpha = ar[u];
-          if (lane == kRows + 1) S.beta = ar[u];
-          if (lane == kRows + 2) { S.node = en[u].x; S.code = en[u].y; }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[st]);
-        }
-        seq += (N - t0 < kAhead) ? (N - t0) : kAhead;
-      }
+  for (int t = tid; t < N; t += kThreads) {
+    const int i = sc.order[t];
+    sc.ent[t] = make_int4(i, (sc.src[i] + 1) | ((sc.push[i] + 1) << 8), 0, 0);
+  }
+  for (int item = g; item < items; item += ctas_per_seq) {
+    const int h = item / slabs, r = (item % slabs) * kRows + rl;
+    const size_t nh0 = (size_t)b * N * H + h;    // (b, node 0, h)
+    __syncthreads();                             // the previous item is done with alpha / beta
+    for (int t = tid; t < N; t += kThreads) {
+      const size_t nh = nh0 + (size_t)sc.ent[t].x * H;
+      sc.ent[t].z = __float_as_int(__ldg(a.alpha + nh));
+      sc.ent[t].w = __float_as_int(__ldg(a.beta + nh));
     }
-  } else {
-    // ---------------------------------------------------------------- consumer warps
-    const int lane = tid % kLPR, rl = tid / kLPR;
-    const float q_scale = a.q_scale;
-    const size_t node_stride = (size_t)H * dv;     // elements between consecutive nodes (out, v)
-    const size_t state_stride = node_stride * DK;  // elements between consecutive nodes (states)
-    uint32_t seq = 0;
-    for (int item = g; item < items; item += ctas_per_seq) {
-      const int h = item / slabs, r = (item % slabs) * kRows + rl;
-      const size_t nh0 = (size_t)b * N * H + h;
-      const TS* s0row = S0 + (((size_t)b * H + h) * dv + r) * DK + lane * CPL;
-      TIO* out_r = out + nh0 * dv + r;
-      TS* st_r = states + (nh0 * dv + r) * DK + lane * CPL;
-      float cur[CPL];
-      for (int t = 0; t < N; ++t, ++seq) {
-        const uint32_t st = seq % kStages;
-        if (!mbar_wait(&full[st], (seq / kStages) & 1u)) timed_out = true;
-        const StageT& S = ring[st];
-        const int i = S.node, code = S.code;
-        const int src = (code & 255) - 1, push = (code >> 8) - 1;
-        const float al = S.alpha, be = S.beta, vv = S.v[rl];
-        float kf[CPL], qf[CPL];
+    __syncthreads();
+
+    const TIO* kb = k + nh0 * DK + lane * CPL;
+    const TIO* qb = q + nh0 * DK + lane * CPL;
+    const TIO* vb = v + nh0 * dv + r;
+    const TS* s0row = S0 + (((size_t)b * H + h) * dv + r) * DK + lane * CPL;
+    TIO* out_r = out + nh0 * dv + r;
+    TS* st_r = states + (nh0 * dv + r) * DK + lane * CPL;
+    auto fetch = [&](int t, Raw<TIO, CPL>& x) {
+      x.e = sc.ent[t < N ? t : N - 1];
+      const int node = x.e.x;
+      x.load(kb + node * kq_stride, qb + node * kq_stride, vb + node * node_stride);
+    };
+    float cur[CPL];
+    // One node: parent state -> output and S_i (kept in cur), checkpoint, optional push.  All
+    // three dot products use the parent state, so they share one reduction:
+    //   (S_p k)_r, (S_p q)_r, k.q  ->  w = beta (v_r - alpha (S_p k)_r),
+    //   o_r = (S_i q)_r = alpha (S_p q)_r + w (k.q),   S_i = alpha S_p + w k^T.
+    auto body = [&](const Raw<TIO, CPL>& x) {
+      const int i = x.e.x;
+      const int src = (x.e.y & 255) - 1, push = (x.e.y >> 8) - 1;
+      const float al = __int_as_float(x.e.z), be = __int_as_float(x.e.w);
+      if (src == 0) {
+        load_vec<CPL>(s0row, cur);  // a root starts from the committed state
+      } else if (src > 0) {
 #pragma unroll
         for (int j = 0; j < Q4; ++j) {
-          const float4 a4 = reinterpret_cast<const float4*>(S.k + lane * CPL)[j];
-          const float4 b4 = reinterpret_cast<const float4*>(S.q + lane * CPL)[j];
-          kf[4 * j] = a4.x; kf[4 * j + 1] = a4.y; kf[4 * j + 2] = a4.z; kf[4 * j + 3] = a4.w;
-          qf[4 * j] = b4.x; qf[4 * j + 1] = b4.y; qf[4 * j + 2] = b4.z; qf[4 * j + 3] = b4.w;
-        }
-        __syncwarp();
-        if ((tid % 32) == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
-        if (src == 0) {
-          load_vec<CPL>(s0row, cur);  // a root starts from the committed state
-        } else if (src > 0) {
-#pragma unroll
-          for (int j = 0; j < Q4; ++j) {
-            const float4 f = stack[((src - 1) * Q4 + j) * kCompute + tid];
-            cur[4 * j] = f.x; cur[4 * j + 1] = f.y; cur[4 * j + 2] = f.z; cur[4 * j + 3] = f.w;
-          }
-        }
-        // All three dot products use the parent state, so they share one reduction:
-        //   (S_p k)_r, (S_p q)_r, k.q  ->  w = beta (v_r - alpha (S_p k)_r),
-        //   o_r = (S_i q)_r = alpha (S_p q)_r + w (k.q),   S_i = alpha S_p + w k^T.
-        float pk0 = 0.f, pk1 = 0.f, pq0 = 0.f, pq1 = 0.f, kq0 = 0.f, kq1 = 0.f;
-#pragma unroll
-        for (int e = 0; e < CPL; e += 2) {
-          pk0 = fmaf(cur[e], kf[e], pk0);
-          pk1 = fmaf(cur[e + 1], kf[e + 1], pk1);
-          pq0 = fmaf(cur[e], qf[e], pq0);
-          pq1 = fmaf(cur[e + 1], qf[e + 1], pq1);
-          kq0 = fmaf(kf[e], qf[e], kq0);
-          kq1 = fmaf(kf[e + 1], qf[e + 1], kq1);
-        }
-        float pk = pk0 + pk1, pq = pq0 + pq1, kq = kq0 + kq1;
-#pragma unroll
-        for (int o = kLPR / 2; o > 0; o >>= 1) {
-          pk += __shfl_xor_sync(0xffffffffu, pk, o);
-          pq += __shfl_xor_sync(0xffffffffu, pq, o);
-          kq += __shfl_xor_sync(0xffffffffu, kq, o);
-        }
-        const float w = be * (vv - al * pk);                  // pseudo-value w_i[r]
-        if (lane == 0) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * pq + w * kq) * q_scale);
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) cur[e] = fmaf(w, kf[e], al * cur[e]);
-        store_vec_cs<CPL>(st_r + (size_t)i * state_stride, cur);
-        if (push > 0) {
-#pragma unroll
-          for (int j = 0; j < Q4; ++j)
-            stack[((push - 1) * Q4 + j) * kCompute + tid] =
-                make_float4(cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
+          const float4 f = stack[((src - 1) * Q4 + j) * kThreads + tid];
+          cur[4 * j] = f.x; cur[4 * j + 1] = f.y; cur[4 * j + 2] = f.z; cur[4 * j + 3] = f.w;
         }
       }
+      float kf[CPL], qf[CPL];
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) { kf[e] = x.kf(e); qf[e] = x.qf(e); }
+      float pk0 = 0.f, pk1 = 0.f, pq0 = 0.f, pq1 = 0.f, kq0 = 0.f, kq1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < CPL; e += 2) {
+        pk0 = fmaf(cur[e], kf[e], pk0);
+        pk1 = fmaf(cur[e + 1], kf[e + 1], pk1);
+        pq0 = fmaf(cur[e], qf[e], pq0);
+        pq1 = fmaf(cur[e + 1], qf[e + 1], pq1);
+        kq0 = fmaf(kf[e], qf[e], kq0);
+        kq1 = fmaf(kf[e + 1], qf[e + 1], kq1);
+      }
+      float pk = pk0 + pk1, pq = pq0 + pq1, kq = kq0 + kq1;
+#pragma unroll
+      for (int o = kLPR / 2; o > 0; o >>= 1) {
+        pk += __shfl_xor_sync(0xffffffffu, pk, o);
+        pq += __shfl_xor_sync(0xffffffffu, pq, o);
+        kq += __shfl_xor_sync(0xffffffffu, kq, o);
+      }
+      const float w = be * (x.v - al * pk);                 // pseudo-value w_i[r]
+      if (lane == 0) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * pq + w * kq) * q_scale);
+#pragma unroll
+      for (int e = 0; e < CPL; ++e) cur[e] = fmaf(w, kf[e], al * cur[e]);
+      store_vec_cs<CPL>(st_r + (size_t)i * state_stride, cur);
+      if (push > 0) {
+#pragma unroll
+        for (int j = 0; j < Q4; ++j)
+          stack[((push - 1) * Q4 + j) * kThreads + tid] =
+              make_float4(cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
+      }
+    };
+    // Three register buffers rotate by unrolling, so each prefetch stays in flight for two
+    // nodes (a register copy would wait for it).
+    Raw<TIO, CPL> ra, rb, rc;
+    fetch(0, ra);
+    fetch(1, rb);
+    for (int t = 0; t < N; t += 3) {
+      fetch(t + 2, rc);
+      body(ra);
+      if (t + 1 >= N) break;
+      fetch(t + 3, ra);
+      body(rb);
+      if (t + 2 >= N) break;
+      fetch(t + 4, rb);
+      body(rc);
     }
   }
-  if (timed_out) a.err[b] = TV_ERR_TIMEOUT;
 }
 
 template <typename TIO, typename TS, int DK>
 cudaError_t launch_fork_t(const GdnArgs& a, void* states, cudaStream_t s) {
   auto kern = gdn_fork_kernel<TIO, TS, DK>;
   const int nslots = slots_for(a.N);
-  size_t stack = (size_t)nslots * (DK / kLPR / 4) * kCompute * sizeof(float4);
+  size_t stack = (size_t)nslots * (DK / kLPR / 4) * kThreads * sizeof(float4);
   if (stack < sizeof(BuildScratch)) stack = sizeof(BuildScratch);
-  const size_t smem = sizeof(Sched) + 2 * kStages * sizeof(uint64_t) + kStages * sizeof(Stage<DK>) + stack;
+  const size_t smem = sizeof(Sched) + stack;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int occ = 0;

@@ -44,17 +44,19 @@ struct TcHead {
 
 __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* __restrict__ pseudo_v,
                                                              float* __restrict__ log_gamma, int cap, int Npad,
-                                                             uint32_t tmem_cols,
+                                                             uint32_t tmem_cols, int v_in_smem,
                                                              const __grid_constant__ CUtensorMap mS0,
                                                              const __grid_constant__ CUtensorMap mK,
-                                                             const __grid_constant__ CUtensorMap mQ) {
+                                                             const __grid_constant__ CUtensorMap mQ,
+                                                             const __grid_constant__ CUtensorMap mV) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 1024-byte aligned tiles
   unsigned char* sA = smem;                                  // S_0: 2 k-blocks x 128 rows x 128 B
   unsigned char* sKQ = smem + kTileA;                        // K: 2 x Npad x 128 B, then Q: same
   const uint32_t kq_bytes = (uint32_t)Npad * 128u;           // one k-block of K or Q
-  TcHead& hd = *reinterpret_cast<TcHead*>(sKQ + 4 * kq_bytes);
+  unsigned char* sV = sKQ + 4 * kq_bytes;                    // V: 2 x Npad x 128 B (when it fits)
+  TcHead& hd = *reinterpret_cast<TcHead*>(sV + (v_in_smem ? 2 * kq_bytes : 0));
   int* pent = reinterpret_cast<int*>(&hd + 1);               // (node << 8) | path node, per entry
   float* cK = reinterpret_cast<float*>(pent + cap);
   float* cQ = cK + cap;
@@ -78,11 +80,12 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   const uint32_t tmem = hd.tmem_base;
 
   if (tid == 0) {
-    mbar_arrive_expect_tx(&hd.tma_bar, kTileA + 4 * kq_bytes);
+    mbar_arrive_expect_tx(&hd.tma_bar, kTileA + (v_in_smem ? 6 : 4) * kq_bytes);
     for (int kb = 0; kb < 2; ++kb) {
       tma_load_2d(sA + kb * (kTileA / 2), &mS0, kb * 64, (b * H + h) * kD, &hd.tma_bar);
       tma_load_4d(sKQ + kb * kq_bytes, &mK, kb * 64, h, 0, b, &hd.tma_bar);
       tma_load_4d(sKQ + (2 + kb) * kq_bytes, &mQ, kb * 64, h, 0, b, &hd.tma_bar);
+      if (v_in_smem) tma_load_4d(sV + kb * kq_bytes, &mV, kb * 64, h, 0, b, &hd.tma_bar);
     }
   }
 
@@ -90,19 +93,22 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   int status = load_and_check_tree(a.parents + (size_t)b * N, N, hd.par, &hd.flag);
   if (!status) {
     for (int i = tid; i <= N; i += kThreads) hd.lvl_cnt[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < N; i += kThreads) {
-      const int d = node_depth(hd.par, i);
-      hd.depth[i] = d;
-      atomicMax(&hd.maxdepth, d);
-      atomicAdd(&hd.lvl_cnt[d], 1);
-      float lg = 0.f;
-      for (int j = i; j >= 0; j = hd.par[j]) lg += logf(__ldg(a.alpha + ((size_t)b * N + j) * H + h));
-      hd.lg[i] = lg;
-      hd.gam[i] = expf(lg);
+    for (int i = tid; i < N; i += kThreads) {  // log(alpha) and beta, one load each
+      hd.gam[i] = logf(__ldg(a.alpha + ((size_t)b * N + i) * H + h));
       hd.beta[i] = __ldg(a.beta + ((size_t)b * N + i) * H + h);
     }
     __syncthreads();
+    for (int i = tid; i < N; i += kThreads) {
+      int d = 0;
+      float lg = hd.gam[i];
+      for (int j = hd.par[i]; j >= 0; j = hd.par[j]) { lg += hd.gam[j]; ++d; }
+      hd.depth[i] = d;
+      atomicMax(&hd.maxdepth, d);
+      atomicAdd(&hd.lvl_cnt[d], 1);
+      hd.lg[i] = lg;
+    }
+    __syncthreads();
+    for (int i = tid; i < N; i += kThreads) hd.gam[i] = expf(hd.lg[i]);
     if (warp == 0) {  // exclusive scans of (depth + 1) over nodes and of node counts over depths
       int carry = 0;
       for (int base = 0; base < N; base += 32) {
@@ -238,7 +244,14 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
           const int col = nodes[x] < 0 ? 0 : nodes[x];
           dk[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)col);
           dq[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)(Npad + col));
-          vv[x] = nodes[x] < 0 ? 0.f : to_f32(v[(((size_t)b * N + nodes[x]) * H + h) * kD + r]);
+          if (v_in_smem) {  // v[node][r] from the swizzled V tile
+            const int n = col, c = r % 64;
+            const bf16* p = reinterpret_cast<const bf16*>(sV + (r / 64) * kq_bytes + n * 128 +
+                                                          (((c / 8) ^ (n & 7)) << 4)) + (c % 8);
+            vv[x] = nodes[x] < 0 ? 0.f : to_f32(*p);
+          } else {
+            vv[x] = nodes[x] < 0 ? 0.f : to_f32(v[(((size_t)b * N + col) * H + h) * kD + r]);
+          }
         }
         tmem_wait_ld();
 #pragma unroll
@@ -283,7 +296,9 @@ cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma
   while (cols < (uint32_t)(2 * Npad)) cols <<= 1;
   int cap = a.N * (a.N + 1) / 2;
   if (cap > kPathCap) cap = kPathCap;
-  size_t smem = 1024 + kTileA + (size_t)4 * Npad * 128 + sizeof(TcHead) + (size_t)cap * 12;
+  const size_t base = 1024 + kTileA + (size_t)4 * Npad * 128 + sizeof(TcHead) + (size_t)cap * 12;
+  const int v_in_smem = base + (size_t)2 * Npad * 128 <= 227 * 1024;
+  size_t smem = base + (v_in_smem ? (size_t)2 * Npad * 128 : 0);
   auto kern = gdn_wy_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   if (e != cudaSuccess) return e;
@@ -296,7 +311,7 @@ cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma
     smem += 8 * 1024;
     if (smem > 227 * 1024) smem = 227 * 1024;
   }
-  CUtensorMap mS0, mK, mQ;
+  CUtensorMap mS0, mK, mQ, mV;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.B * a.H * kD};
     const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
@@ -309,8 +324,9 @@ cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)Npad, 1};
     if (!make_map_bf16_sw128(&mK, a.k, 4, dims, strides, box)) return cudaErrorInvalidValue;
     if (!make_map_bf16_sw128(&mQ, a.q, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16_sw128(&mV, a.v, 4, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  kern<<<a.B * a.H, kThreads, smem, s>>>(a, pseudo_v, log_gamma, cap, Npad, cols, mS0, mK, mQ);
+  kern<<<a.B * a.H, kThreads, smem, s>>>(a, pseudo_v, log_gamma, cap, Npad, cols, v_in_smem, mS0, mK, mQ, mV);
   return cudaGetLastError();
 }
 
