@@ -3,10 +3,10 @@
 One step is one pass of every step of the hot path over one batch of synthetic inputs:
 
   * tree prepare for the batch's draft trees;
-  * the 24-layer gated-DeltaNet stack of config 2 (B=64 sequences, 40-node k=3 d=3 trees,
+  * the 24-layer gated-DeltaNet stack at batch 64 (B=64 sequences, 40-node k=3 d=3 trees,
     H=16, d=128, bf16) in fork/checkpoint mode -- verify all 24 layers, then commit all 24 --
     and in TreeWY mode -- verify all 24, then commit all 24 (separate S_0 buffers per mode);
-  * one tree-masked attention layer of config 3 (B=32, 16q/4kv, hd 256, bf16, paged prefixes
+  * one tree-masked attention layer at batch 32 (B=32, 16q/4kv, hd 256, bf16, paged prefixes
     P ~ U[2048, 32768], 40-node trees) followed by the KV compaction of its accepted paths.
 
 ``value`` = GDN node-layer verifications per second over the whole step (64 x 40 nodes x 24
@@ -34,8 +34,8 @@ sys.path.insert(0, ROOT)
 
 LAYERS = 24
 METRIC = "tree-verified draft nodes/s per GDN layer; HBM GB/s & tensor util vs roofline"
-WORKLOAD = ("config 2: 24 GDN layers, B=64, N=40 (k=3 d=3), H=16, dk=dv=128, bf16, fork+commit and "
-            "TreeWY+commit; config 3: tree attention B=32, 16q/4kv, hd=256, paged P~U[2048,32768], N=40, "
+WORKLOAD = ("GDN stack: 24 GDN layers, B=64, N=40 (k=3 d=3), H=16, dk=dv=128, bf16, fork+commit and "
+            "TreeWY+commit; paged attention: tree attention B=32, 16q/4kv, hd=256, paged P~U[2048,32768], N=40, "
             "+ KV compaction")
 
 
@@ -182,11 +182,11 @@ class Round:
         self.dev = dev
         seed = 1000 * rank
         self.layers = layers
-        self.gdn_host = [W.cfg2_layer(layer=l, seed=seed) for l in range(layers)]
+        self.gdn_host = [W.stack_b64_layer(layer=l, seed=seed) for l in range(layers)]
         c0 = self.gdn_host[0]
         self.B, self.N, self.H, self.dk, self.dv = c0.shape
         B, N, H, dk, dv = self.B, self.N, self.H, self.dk, self.dv
-        self.attn_host = W.cfg3(seed=seed)
+        self.attn_host = W.paged_attn_b32_case(seed=seed)
         a = self.attn_host
         self.aB, self.aN, self.Hq, self.Hkv, self.hd = a.shape
 
@@ -313,7 +313,7 @@ class Round:
 
 
 class OraclePool:
-    """The fp64 oracle, as it stands, on every host core: one config-2 sequence (40 nodes,
+    """The fp64 oracle, as it stands, on every host core: one sequence of the batch-64 GDN stack (40 nodes,
     16 heads, one GDN layer) per task through ``oracle.gdn.verify_by_depth``, in spawned worker
     processes with single-threaded BLAS.  Started before any GPU work."""
 
@@ -348,7 +348,7 @@ class OraclePool:
                 break
         dt = time.perf_counter() - t0
         return {"value": done * 40 / dt, "unit": "nodes/s", "cores": self.cores, "kind": "oracle",
-                "sample": f"{done} config-2 sequences (40 nodes x 16 heads, one GDN layer, bf16 inputs in fp64) "
+                "sample": f"{done} sequences of the batch-64 GDN stack (40 nodes x 16 heads, one GDN layer, bf16 inputs in fp64) "
                           f"through the oracle's depth-by-depth schedule in {dt:.1f} s"}
 
     def close(self):
@@ -360,7 +360,7 @@ _ORACLE_CACHE = {}
 
 def _oracle_init():
     import workloads as W
-    _ORACLE_CACHE["inp"] = W.cfg2_layer(layer=0).oracle_inputs()
+    _ORACLE_CACHE["inp"] = W.stack_b64_layer(layer=0).oracle_inputs()
 
 
 def _oracle_sequence(b):

@@ -41,8 +41,8 @@ def test_printed_example_tree():
 
 
 def test_config1_tree_and_chain():
-    _check_attn(W.cfg1_attn("tree"))
-    _check_attn(W.cfg1_attn("chain"))
+    _check_attn(W.single_layer_attn_case("tree"))
+    _check_attn(W.single_layer_attn_case("chain"))
 
 
 @pytest.mark.parametrize("hd", [64, 128, 256])
@@ -66,8 +66,8 @@ def test_wide_tree_many_words():
 
 
 def test_config3_full_size_sampled():
-    """Config 3 at full size: B=32, 16q/4kv, hd 256, P ~ U[2048, 32768] paged, 40-node trees."""
-    case = W.cfg3()
+    """Paged attention at full size: B=32, 16q/4kv, hd 256, P ~ U[2048, 32768] paged, 40-node trees."""
+    case = W.paged_attn_b32_case()
     res = _check_attn(case, batch=[0, int(np.argmax(case.prefix_len.numpy())), 31])
     # compaction of the same cache, every sequence, bit-exact
     f = _gpu.attn_f64(case)
@@ -89,7 +89,7 @@ def test_config3_full_size_sampled():
 
 @pytest.mark.parametrize("N,B", [(40, 4), (128, 2)])
 def test_config4_attention_layer_sampled(N, B):
-    case = W.cfg4_attn_layer(N, B)
+    case = W.sweep_attn_layer(N, B)
     _check_attn(case, batch=[0, B - 1])
 
 

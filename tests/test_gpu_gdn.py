@@ -1,7 +1,7 @@
 """GPU vs fp64 oracle: GDN tree verify (fork and TreeWY modes) and commit, through the C ABI.
 
-Small cases are compared element by element over every output; the full-size config-2 and
-config-4 cases (the launch configuration the benchmark times) are compared on sampled
+Small cases are compared element by element over every output; the full-size batch-64 stack layer and
+the wide-tree sweep cases (the launch configuration the benchmark times) are compared on sampled
 (sequence, node) outputs the oracle computes one by one.
 """
 import numpy as np
@@ -64,12 +64,12 @@ def _check_all(case, modes=("fork", "wy")):
 
 
 def test_config0_fp32():
-    _check_all(W.cfg0())
+    _check_all(W.small_fp32_case())
 
 
 @pytest.mark.parametrize("tree", ["chain", "tree"])
 def test_config1_bf16(tree):
-    _check_all(W.cfg1_gdn(tree))
+    _check_all(W.single_layer_gdn_case(tree))
 
 
 @pytest.mark.parametrize("io,state", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "f32")])
@@ -168,13 +168,13 @@ def _sampled_check(case, n_seq, n_nodes, seed):
 
 
 def test_config2_full_size_sampled():
-    """One config-2 layer at its full size: B=64, N=40 (k=3 d=3), H=16, d=128, bf16."""
-    _sampled_check(W.cfg2_layer(layer=0), n_seq=3, n_nodes=5, seed=2)
+    """One layer of the batch-64 GDN stack at its full size: B=64, N=40 (k=3 d=3), H=16, d=128, bf16."""
+    _sampled_check(W.stack_b64_layer(layer=0), n_seq=3, n_nodes=5, seed=2)
 
 
 @pytest.mark.parametrize("N,B", [(15, 8), (64, 8), (256, 4)])
 def test_config4_trees_sampled(N, B):
-    _sampled_check(W.cfg4_gdn_layer(N, B), n_seq=2, n_nodes=4, seed=N)
+    _sampled_check(W.sweep_gdn_layer(N, B), n_seq=2, n_nodes=4, seed=N)
 
 
 def test_malformed_tree_only_fails_its_sequence():
@@ -222,7 +222,7 @@ def test_commit_rejects_bad_paths_and_leaves_state():
 
 
 def test_host_side_argument_errors():
-    case = W.cfg0()
+    case = W.small_fp32_case()
     x = _gpu.gdn_inputs(case)
     out = torch.empty_like(x["v"])
     st = torch.empty((1, 7, 2, 64, 64), device="cuda")

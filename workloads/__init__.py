@@ -274,31 +274,31 @@ def attn_case(trees: list[list[int]], prefix_lens: list[int], Hq: int, Hkv: int,
 
 
 # ----------------------------------------------------------------------------- configs
-def cfg0(seed: int = 0) -> GDNCase:
+def small_fp32_case(seed: int = 0) -> GDNCase:
     """Single GDN layer, batch 1, H=2, d=64, fp32, tree k=2 d=2 (7 nodes)."""
     return gdn_case([[-1, 0, 0, 1, 1, 2, 2]], H=2, dk=64, dv=64, io="f32", state="f32", seed=seed)
 
 
-def cfg1_gdn(tree: str = "tree", seed: int = 0) -> GDNCase:
+def single_layer_gdn_case(tree: str = "tree", seed: int = 0) -> GDNCase:
     """One GDN layer, H=16, d=128, bf16, batch 1; ``tree`` = "chain" (5 nodes) or "tree" (k=2 d=3)."""
     t = chain(5) if tree == "chain" else full_tree(2, 3)
     return gdn_case([t], H=16, dk=128, dv=128, io="bf16", state="bf16", seed=seed)
 
 
-def cfg1_attn(tree: str = "tree", seed: int = 0) -> AttnCase:
-    """One tree attention layer on the config-1 tree: 16q/4kv, hd 128, prefix 4096, theta 1e6."""
+def single_layer_attn_case(tree: str = "tree", seed: int = 0) -> AttnCase:
+    """One tree attention layer on the single-layer workload's tree (or chain): 16q/4kv, hd 128, prefix 4096, theta 1e6."""
     t = chain(5) if tree == "chain" else full_tree(2, 3)
     return attn_case([t], [4096], Hq=16, Hkv=4, hd=128, seed=seed, rope_theta=1e6)
 
 
-def cfg2_layer(layer: int = 0, B: int = 64, seed: int = 0) -> GDNCase:
-    """One of the 24 independent config-2 GDN layers: B=64, H=16, d=128, bf16, k=3 d=3 trees."""
+def stack_b64_layer(layer: int = 0, B: int = 64, seed: int = 0) -> GDNCase:
+    """One of the 24 independent GDN layers of the batch-64 stack: B=64, H=16, d=128, bf16, k=3 d=3 trees."""
     t = full_tree(3, 3)
     return gdn_case([t] * B, H=16, dk=128, dv=128, io="bf16", state="bf16",
                     seed=seed * 1000 + layer)
 
 
-def cfg3(B: int = 32, seed: int = 0, pmin: int = 2048, pmax: int = 32768) -> AttnCase:
+def paged_attn_b32_case(B: int = 32, seed: int = 0, pmin: int = 2048, pmax: int = 32768) -> AttnCase:
     """Tree attention + compaction: B=32, 16q/4kv, hd 256, bf16, P ~ U{2048..32768}, k=3 d=3,
     accepted length 1..4."""
     rng = np.random.default_rng(seed + 7)
@@ -308,17 +308,17 @@ def cfg3(B: int = 32, seed: int = 0, pmin: int = 2048, pmax: int = 32768) -> Att
                      path_max_len=4)
 
 
-def cfg4_trees(N: int, B: int, seed: int = 0) -> list[list[int]]:
-    """Config-4 random dynamic trees (1..4 children per node, depth <= 8), one per sequence."""
+def sweep_trees(N: int, B: int, seed: int = 0) -> list[list[int]]:
+    """Wide-tree sweep: random dynamic trees (1..4 children per node, depth <= 8), one per sequence."""
     rng = np.random.default_rng(seed + 4000 + N)
     return [random_tree(N, rng) for _ in range(B)]
 
 
-def cfg4_gdn_layer(N: int, B: int, layer: int = 0, seed: int = 0) -> GDNCase:
-    return gdn_case(cfg4_trees(N, B, seed), H=16, dk=128, dv=128, io="bf16", state="bf16",
+def sweep_gdn_layer(N: int, B: int, layer: int = 0, seed: int = 0) -> GDNCase:
+    return gdn_case(sweep_trees(N, B, seed), H=16, dk=128, dv=128, io="bf16", state="bf16",
                     seed=seed * 1000 + 100 + layer)
 
 
-def cfg4_attn_layer(N: int, B: int, layer: int = 0, seed: int = 0) -> AttnCase:
-    return attn_case(cfg4_trees(N, B, seed), [8192] * B, Hq=16, Hkv=4, hd=128,
+def sweep_attn_layer(N: int, B: int, layer: int = 0, seed: int = 0) -> AttnCase:
+    return attn_case(sweep_trees(N, B, seed), [8192] * B, Hq=16, Hkv=4, hd=128,
                      seed=seed * 1000 + 500 + layer, rope_theta=1e6)
