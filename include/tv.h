@@ -68,7 +68,9 @@ enum tv_status {
   TV_ERR_CUDA = -5,
   TV_ERR_TIMEOUT = -6,
   TV_ERR_CAPACITY = -7,     /* block table too short for prefix_len + N slots */
-  TV_ERR_BAD_BLOCK = -8     /* a block-table entry outside [0, num_blocks) */
+  TV_ERR_BAD_BLOCK = -8,    /* a block-table entry outside [0, num_blocks) */
+  TV_ERR_SCRATCH = -9       /* tv_tree_attn_static: the call needs more than
+                               TV_STATIC_SCRATCH_BYTES of scratch */
 };
 
 enum tv_dtype { TV_F32 = 0, TV_BF16 = 1 };
@@ -76,6 +78,7 @@ enum tv_mode { TV_MODE_FORK = 0, TV_MODE_WY = 1 };
 
 #define TV_MAX_NODES 256
 #define TV_BLOCK_SIZE 16
+#define TV_STATIC_SCRATCH_BYTES (64u << 20) /* scratch array of tv_tree_attn_static: 64 MiB */
 
 /* Human-readable name of a tv_status code (static string, never NULL). */
 TV_API const char* tv_status_string(int status);
@@ -220,6 +223,32 @@ TV_API int tv_tree_attn(const void* q, const void* k_new, const void* v_new, voi
                  const int32_t* prefix_len, const int32_t* parents, int B, int N, int Hq,
                  int Hkv, int hd, int block_size, float rope_theta, float sm_scale, void* out,
                  void* workspace, size_t workspace_bytes, int32_t* err, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * tv_tree_attn_static -- tv_tree_attn without a workspace and without any allocation.
+ *
+ * The pages have no counterpart: this is a deployment variant of tv_tree_attn, for callers
+ * that cannot hand the library a workspace (e.g. code that must not allocate).  Arguments,
+ * layouts, results and the err codes are those of tv_tree_attn; the workspace is replaced by
+ * one device array of TV_STATIC_SCRATCH_BYTES (64 MiB) owned by the library.
+ *
+ *  - Size limit: when tv_tree_attn_workspace_size(B, N, Hq, Hkv, hd, max_blocks, block_size)
+ *    exceeds TV_STATIC_SCRATCH_BYTES the call returns TV_ERR_SCRATCH before any CUDA call
+ *    and launches nothing; use tv_tree_attn with a workspace for such sizes.
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress; a failure returns TV_ERR_CUDA) and caches it.  That lookup may
+ *    load a module, so make the first call on each device in set-up code, before any stream
+ *    capture.
+ *  - Shared state: the scratch is one array per device for the whole process.  Its contents
+ *    persist between calls; nothing in it has to start at zero (every call writes each
+ *    scratch entry it reads).  Two calls whose execution overlaps on the same device (other
+ *    streams, other host threads) race on it: serialise them, e.g. on one stream.
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_tree_attn_static(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
+                        const int32_t* prefix_len, const int32_t* parents, int B, int N, int Hq,
+                        int Hkv, int hd, int block_size, float rope_theta, float sm_scale,
+                        void* out, int32_t* err, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * tv_kv_compact -- keep the accepted path's KV, in place.

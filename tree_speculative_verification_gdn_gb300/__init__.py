@@ -29,16 +29,18 @@ TV_ERR_CUDA = -5
 TV_ERR_TIMEOUT = -6
 TV_ERR_CAPACITY = -7
 TV_ERR_BAD_BLOCK = -8
+TV_ERR_SCRATCH = -9
 TV_F32 = 0
 TV_BF16 = 1
 TV_MODE_FORK = 0
 TV_MODE_WY = 1
 TV_MAX_NODES = 256
 TV_BLOCK_SIZE = 16
+TV_STATIC_SCRATCH_BYTES = 64 << 20
 
 EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_prepare",
             "tv_gdn_tree_verify_fork", "tv_gdn_tree_verify_wy", "tv_gdn_commit",
-            "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_kv_compact")
+            "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -56,6 +58,8 @@ _SIGNATURES = {
     "tv_tree_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "tv_tree_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _P, _P, _Z,
                           _P, _P]),
+    "tv_tree_attn_static": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _P,
+                                 _P, _P]),
     "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
 }
 
@@ -167,6 +171,21 @@ def tv_tree_attn(q, k_new, v_new, k_cache, v_cache, block_table, prefix_len, par
         max_blocks, _ptr(prefix_len), _ptr(parents), B, N, Hq, Hkv, hd, bs, float(rope_theta), float(scale),
         _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(err),
         _stream(stream)), "tv_tree_attn")
+
+
+def tv_tree_attn_static(q, k_new, v_new, k_cache, v_cache, block_table, prefix_len, parents, out,
+                        err, rope_theta: float, sm_scale: float | None = None, stream=None) -> None:
+    """``tv_tree_attn`` on the library's static scratch (no workspace, no allocation).  Raises
+    TVError with TV_ERR_SCRATCH when the call needs more than TV_STATIC_SCRATCH_BYTES."""
+    B, N, Hq, hd = q.shape
+    Hkv = k_new.shape[2]
+    num_blocks, _, bs, _ = k_cache.shape
+    max_blocks = block_table.shape[1]
+    scale = hd ** -0.5 if sm_scale is None else sm_scale
+    _check(lib.tv_tree_attn_static(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table),
+        max_blocks, _ptr(prefix_len), _ptr(parents), B, N, Hq, Hkv, hd, bs, float(rope_theta), float(scale),
+        _ptr(out), _ptr(err), _stream(stream)), "tv_tree_attn_static")
 
 
 def tv_kv_compact(k_cache, v_cache, block_table, prefix_len, parents, accepted_path, accepted_len,

@@ -31,6 +31,12 @@ int cuda_status(cudaError_t e) {
   return TV_ERR_CUDA;
 }
 
+}  // namespace
+
+int tv::cuda_status_of(cudaError_t e) { return cuda_status(e); }
+
+namespace {
+
 bool a16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool a4(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool dim_ok(int d) { return d == 64 || d == 128; }
@@ -70,6 +76,7 @@ const char* tv_status_string(int status) {
     case TV_ERR_TIMEOUT: return "device wait timed out";
     case TV_ERR_CAPACITY: return "block table too short for prefix_len + N slots";
     case TV_ERR_BAD_BLOCK: return "block-table entry outside the cache";
+    case TV_ERR_SCRATCH: return "request needs more than the static scratch of TV_STATIC_SCRATCH_BYTES";
     default: return "unknown status";
   }
 }

@@ -11,6 +11,8 @@
 namespace tv {
 
 int device_sm_count();
+// TV_OK for cudaSuccess; otherwise records e for tv_last_cuda_error and returns TV_ERR_CUDA.
+int cuda_status_of(cudaError_t e);
 
 struct GdnArgs {
   const void* q;
