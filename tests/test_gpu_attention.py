@@ -40,7 +40,7 @@ def test_printed_example_tree():
     _check_attn(case)
 
 
-def test_config1_tree_and_chain():
+def test_single_layer_tree_and_chain():
     _check_attn(W.single_layer_attn_case("tree"))
     _check_attn(W.single_layer_attn_case("chain"))
 
@@ -65,7 +65,7 @@ def test_wide_tree_many_words():
     _check_attn(case)
 
 
-def test_config3_full_size_sampled():
+def test_paged_b32_full_size_sampled():
     """Paged attention at full size: B=32, 16q/4kv, hd 256, P ~ U[2048, 32768] paged, 40-node trees."""
     case = W.paged_attn_b32_case()
     res = _check_attn(case, batch=[0, int(np.argmax(case.prefix_len.numpy())), 31])
@@ -88,7 +88,7 @@ def test_config3_full_size_sampled():
 
 
 @pytest.mark.parametrize("N,B", [(40, 4), (128, 2)])
-def test_config4_attention_layer_sampled(N, B):
+def test_wide_tree_attention_layer_sampled(N, B):
     case = W.sweep_attn_layer(N, B)
     _check_attn(case, batch=[0, B - 1])
 

@@ -63,12 +63,12 @@ def _check_all(case, modes=("fork", "wy")):
     return res
 
 
-def test_config0_fp32():
+def test_small_fp32_layer():
     _check_all(W.small_fp32_case())
 
 
 @pytest.mark.parametrize("tree", ["chain", "tree"])
-def test_config1_bf16(tree):
+def test_single_layer_bf16(tree):
     _check_all(W.single_layer_gdn_case(tree))
 
 
@@ -167,13 +167,13 @@ def _sampled_check(case, n_seq, n_nodes, seed):
     _gpu.assert_close(w["out"], W.f64(f["out"]), io, "wy vs fork, all outputs")
 
 
-def test_config2_full_size_sampled():
+def test_stack_layer_full_size_sampled():
     """One layer of the batch-64 GDN stack at its full size: B=64, N=40 (k=3 d=3), H=16, d=128, bf16."""
     _sampled_check(W.stack_b64_layer(layer=0), n_seq=3, n_nodes=5, seed=2)
 
 
 @pytest.mark.parametrize("N,B", [(15, 8), (64, 8), (256, 4)])
-def test_config4_trees_sampled(N, B):
+def test_wide_tree_sweep_sampled(N, B):
     _sampled_check(W.sweep_gdn_layer(N, B), n_seq=2, n_nodes=4, seed=N)
 
 

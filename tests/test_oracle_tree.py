@@ -52,7 +52,7 @@ def test_tree_sizes_from_pages(golden):
         assert T.is_valid_tree(parents)
 
 
-def test_full_trees_match_configs():
+def test_full_trees_match_workload_sizes():
     assert W.full_tree(2, 2) == [-1, 0, 0, 1, 1, 2, 2]
     assert len(W.full_tree(2, 3)) == 15
     assert len(W.full_tree(3, 3)) == 40

@@ -6,14 +6,16 @@
 // and every S_i is written out (the checkpoint the commit step restores).
 //
 // The rows of S (value index r) evolve independently: row r only needs k_i, q_i, v_i[r],
-// alpha_i, beta_i.  A CTA therefore owns a slab of 16 rows of one (sequence, head), keeps
-// their fp32 state on chip and walks the whole tree once, depth-first, instead of one launch
-// per depth reading every parent snapshot back from HBM.  HBM traffic is the floor: S_0 read
-// once per root, each checkpoint written once.  Each row is held by 8 lanes (dk/8 columns
-// each), so a dot product costs 3 shuffles.  Every warp walks the tree on its own -- no
-// barrier inside the node loop -- with the next two nodes' k, q and v prefetched into
-// registers; the CTA's warps share one (sequence, head), so k and q come from L1 after the
-// first warp's read.
+// alpha_i, beta_i.  A CTA owns a slab of 16 rows of one (sequence, head) at a time (the grid
+// is persistent: a few CTAs per sequence loop over its (head, slab) items), keeps their fp32
+// state on chip and walks the whole tree once, depth-first, instead of one launch per depth
+// reading every parent snapshot back from HBM.  HBM traffic is the floor: S_0 read once per
+// root, each checkpoint written once.  Each row is held by 8 lanes (dk/8 columns each, in
+// interleaved 8-column chunks), so a row dot product costs 3 shuffles; k.q, the same for every
+// row, comes from a per-item table.  Column pairs use the paired fp32 FMA.  Every warp walks
+// the tree on its own -- no barrier inside the node loop -- with the next two nodes' k, q and
+// v prefetched into registers; the CTA's warps share one (sequence, head), so k and q come
+// from L1 after the first warp's read.
 //
 // Depth-first order visits a node's light children first and its heaviest child (largest
 // subtree) last.  A branching node pushes its state to a shared-memory slot that its later
@@ -32,6 +34,10 @@ constexpr int kLPR = 8;                 // lanes per state row
 constexpr int kRows = 16;               // state rows per CTA
 constexpr int kThreads = kLPR * kRows;  // 128
 constexpr int kSlots = 7;               // on-chip state slots 1..7 (S_0 is re-read for a root)
+// Column ownership: lane l of a row holds the chunks of 8 columns starting at l * 8 + j * kStride
+// (j = 0 .. CPL / 8 - 1), so one chunk-wide access by the 8 lanes of a row covers kStride
+// contiguous columns: full 32-byte sectors for every load and store of k, q, S_0 and states.
+constexpr int kStride = 8 * kLPR;
 
 // What the node loop needs from the schedule, plus the current item's decay / write strength.
 struct Sched {
@@ -40,6 +46,7 @@ struct Sched {
   int push[TV_MAX_NODES];    // slot the node's own state goes to (-1: not needed later)
   // per depth-first position t: {node, (src + 1) | (push + 1) << 8, alpha bits, beta bits}
   int4 ent[TV_MAX_NODES];
+  float kq[TV_MAX_NODES];    // per depth-first position: k_i . q_i of the current item's head
   int flag, maxslot, pad0, pad1;
 };
 // Scratch of the schedule builder; it lives in the (not yet used) state-stack region.
@@ -135,13 +142,13 @@ struct Raw;
 template <int CPL>
 struct Raw<bf16, CPL> {
   uint32_t k[CPL / 2], q[CPL / 2];
-  float v;
+  float v, kq;
   int4 e;  // schedule entry of the node
   __device__ __forceinline__ void load(const bf16* kp, const bf16* qp, const bf16* vp) {
 #pragma unroll
     for (int j = 0; j < CPL / 8; ++j) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(kp) + j);
-      const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp) + j);
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(kp + j * kStride));
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + j * kStride));
       k[4 * j] = a.x; k[4 * j + 1] = a.y; k[4 * j + 2] = a.z; k[4 * j + 3] = a.w;
       q[4 * j] = c.x; q[4 * j + 1] = c.y; q[4 * j + 2] = c.z; q[4 * j + 3] = c.w;
     }
@@ -153,11 +160,14 @@ struct Raw<bf16, CPL> {
 template <int CPL>
 struct Raw<float, CPL> {
   float k[CPL], q[CPL];
-  float v;
+  float v, kq;
   int4 e;  // schedule entry of the node
   __device__ __forceinline__ void load(const float* kp, const float* qp, const float* vp) {
-    load_vec<CPL>(kp, k);
-    load_vec<CPL>(qp, q);
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) {
+      load_vec<8>(kp + j * kStride, k + 8 * j);
+      load_vec<8>(qp + j * kStride, q + 8 * j);
+    }
     v = __ldg(vp);
   }
   __device__ __forceinline__ float kf(int e) const { return k[e]; }
@@ -207,67 +217,96 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
       sc.ent[t].z = __float_as_int(__ldg(a.alpha + nh));
       sc.ent[t].w = __float_as_int(__ldg(a.beta + nh));
     }
+    // k_i . q_i is the same for every row of the head: 8 threads per node compute it once.
+    // The loop bound is warp-uniform, so every lane takes part in the shuffles.
+    for (int t0 = 0; t0 < N; t0 += kThreads / kLPR) {
+      const int t = t0 + tid / kLPR;
+      float dot = 0.f;
+      if (t < N) {
+        const size_t nh = nh0 + (size_t)sc.order[t] * H;
+        Raw<TIO, CPL> x;
+        x.load(k + nh * DK + lane * 8, q + nh * DK + lane * 8, v + nh * dv);
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) dot = fmaf(x.kf(e), x.qf(e), dot);
+      }
+      dot = group_sum<kLPR>(dot);
+      if (t < N && lane == 0) sc.kq[t] = dot;
+    }
     __syncthreads();
 
-    const TIO* kb = k + nh0 * DK + lane * CPL;
-    const TIO* qb = q + nh0 * DK + lane * CPL;
+    const TIO* kb = k + nh0 * DK + lane * 8;
+    const TIO* qb = q + nh0 * DK + lane * 8;
     const TIO* vb = v + nh0 * dv + r;
-    const TS* s0row = S0 + (((size_t)b * H + h) * dv + r) * DK + lane * CPL;
+    const TS* s0row = S0 + (((size_t)b * H + h) * dv + r) * DK + lane * 8;
     TIO* out_r = out + nh0 * dv + r;
-    TS* st_r = states + (nh0 * dv + r) * DK + lane * CPL;
+    TS* st_r = states + (nh0 * dv + r) * DK + lane * 8;
     auto fetch = [&](int t, Raw<TIO, CPL>& x) {
       x.e = sc.ent[t < N ? t : N - 1];
+      x.kq = sc.kq[t < N ? t : N - 1];
       const int node = x.e.x;
       x.load(kb + node * kq_stride, qb + node * kq_stride, vb + node * node_stride);
     };
-    float cur[CPL];
-    // One node: parent state -> output and S_i (kept in cur), checkpoint, optional push.  All
-    // three dot products use the parent state, so they share one reduction:
-    //   (S_p k)_r, (S_p q)_r, k.q  ->  w = beta (v_r - alpha (S_p k)_r),
-    //   o_r = (S_i q)_r = alpha (S_p q)_r + w (k.q),   S_i = alpha S_p + w k^T.
+    float2 cur[CPL / 2];  // the row's state, column pairs (2e, 2e + 1)
+    // One node: parent state -> output and S_i (kept in cur), checkpoint, optional push.  The
+    // two row dot products use the parent state, so they share one reduction:
+    //   (S_p k)_r, (S_p q)_r  ->  w = beta (v_r - alpha (S_p k)_r),
+    //   o_r = (S_i q)_r = alpha (S_p q)_r + w (k.q),   S_i = alpha S_p + w k^T,
+    // with k.q from the per-item table.  Column pairs go through the paired fp32 FMA.
     auto body = [&](const Raw<TIO, CPL>& x) {
       const int i = x.e.x;
       const int src = (x.e.y & 255) - 1, push = (x.e.y >> 8) - 1;
       const float al = __int_as_float(x.e.z), be = __int_as_float(x.e.w);
       if (src == 0) {
-        load_vec<CPL>(s0row, cur);  // a root starts from the committed state
+        float f[CPL];
+#pragma unroll
+        for (int j = 0; j < CPL / 8; ++j) load_vec<8>(s0row + j * kStride, f + 8 * j);  // a root starts from S_0
+#pragma unroll
+        for (int e = 0; e < CPL / 2; ++e) cur[e] = make_float2(f[2 * e], f[2 * e + 1]);
       } else if (src > 0) {
 #pragma unroll
         for (int j = 0; j < Q4; ++j) {
           const float4 f = stack[((src - 1) * Q4 + j) * kThreads + tid];
-          cur[4 * j] = f.x; cur[4 * j + 1] = f.y; cur[4 * j + 2] = f.z; cur[4 * j + 3] = f.w;
+          cur[2 * j] = make_float2(f.x, f.y);
+          cur[2 * j + 1] = make_float2(f.z, f.w);
         }
       }
-      float kf[CPL], qf[CPL];
+      float2 kf[CPL / 2], qf[CPL / 2];
 #pragma unroll
-      for (int e = 0; e < CPL; ++e) { kf[e] = x.kf(e); qf[e] = x.qf(e); }
-      float pk0 = 0.f, pk1 = 0.f, pq0 = 0.f, pq1 = 0.f, kq0 = 0.f, kq1 = 0.f;
-#pragma unroll
-      for (int e = 0; e < CPL; e += 2) {
-        pk0 = fmaf(cur[e], kf[e], pk0);
-        pk1 = fmaf(cur[e + 1], kf[e + 1], pk1);
-        pq0 = fmaf(cur[e], qf[e], pq0);
-        pq1 = fmaf(cur[e + 1], qf[e + 1], pq1);
-        kq0 = fmaf(kf[e], qf[e], kq0);
-        kq1 = fmaf(kf[e + 1], qf[e + 1], kq1);
+      for (int e = 0; e < CPL / 2; ++e) {
+        kf[e] = make_float2(x.kf(2 * e), x.kf(2 * e + 1));
+        qf[e] = make_float2(x.qf(2 * e), x.qf(2 * e + 1));
       }
-      float pk = pk0 + pk1, pq = pq0 + pq1, kq = kq0 + kq1;
+      float2 pk0 = make_float2(0.f, 0.f), pk1 = pk0, pq0 = pk0, pq1 = pk0;
+#pragma unroll
+      for (int e = 0; e < CPL / 2; e += 2) {
+        pk0 = __ffma2_rn(cur[e], kf[e], pk0);
+        pq0 = __ffma2_rn(cur[e], qf[e], pq0);
+        pk1 = __ffma2_rn(cur[e + 1], kf[e + 1], pk1);
+        pq1 = __ffma2_rn(cur[e + 1], qf[e + 1], pq1);
+      }
+      float pk = (pk0.x + pk1.x) + (pk0.y + pk1.y), pq = (pq0.x + pq1.x) + (pq0.y + pq1.y);
 #pragma unroll
       for (int o = kLPR / 2; o > 0; o >>= 1) {
         pk += __shfl_xor_sync(0xffffffffu, pk, o);
         pq += __shfl_xor_sync(0xffffffffu, pq, o);
-        kq += __shfl_xor_sync(0xffffffffu, kq, o);
       }
       const float w = be * (x.v - al * pk);                 // pseudo-value w_i[r]
-      if (lane == 0) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * pq + w * kq) * q_scale);
+      if (lane == 0) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * pq + w * x.kq) * q_scale);
+      const float2 al2 = make_float2(al, al), w2 = make_float2(w, w);
 #pragma unroll
-      for (int e = 0; e < CPL; ++e) cur[e] = fmaf(w, kf[e], al * cur[e]);
-      store_vec_cs<CPL>(st_r + (size_t)i * state_stride, cur);
+      for (int e = 0; e < CPL / 2; ++e) cur[e] = __ffma2_rn(w2, kf[e], __fmul2_rn(al2, cur[e]));
+      {
+        float f[CPL];
+#pragma unroll
+        for (int e = 0; e < CPL / 2; ++e) { f[2 * e] = cur[e].x; f[2 * e + 1] = cur[e].y; }
+#pragma unroll
+        for (int j = 0; j < CPL / 8; ++j) store_vec_cs<8>(st_r + (size_t)i * state_stride + j * kStride, f + 8 * j);
+      }
       if (push > 0) {
 #pragma unroll
         for (int j = 0; j < Q4; ++j)
           stack[((push - 1) * Q4 + j) * kThreads + tid] =
-              make_float4(cur[4 * j], cur[4 * j + 1], cur[4 * j + 2], cur[4 * j + 3]);
+              make_float4(cur[2 * j].x, cur[2 * j].y, cur[2 * j + 1].x, cur[2 * j + 1].y);
       }
     };
     // Three register buffers rotate by unrolling, so each prefetch stays in flight for two
