@@ -16,107 +16,180 @@ constexpr int kThreads = 256;
 
 struct PathCheck {
   int par[TV_MAX_NODES];
+  int path[TV_MAX_NODES];  // the first min(Lmax, N) entries of the sequence's path
   int flag;
   int status;
   int L;
   int last;
 };
 
-// Checks tree and accepted path of sequence b with the whole CTA.  Returns the status (same in
-// every thread); on success pc.L / pc.last hold the length and the accepted node.
+// Checks tree and accepted path of sequence b with the whole CTA.  The path entries and its
+// length are loaded together with the parents, so the check itself reads shared memory only.
+// Returns the status (same in every thread); on success pc.L / pc.last hold the length and
+// the accepted node, and pc.path[0 .. L-1] the path.  A valid path has distinct nodes, so
+// L <= N.
 __device__ int check_path(const CommitArgs& a, int b, PathCheck& pc) {
-  int st = load_and_check_tree(a.parents + (size_t)b * a.N, a.N, pc.par, &pc.flag);
+  const int cap = a.Lmax < a.N ? a.Lmax : a.N;
+  for (int r = threadIdx.x; r < cap; r += blockDim.x) pc.path[r] = a.path[(size_t)b * a.Lmax + r];
+  if (threadIdx.x == 0) pc.L = a.path_len[b];
+  int st = load_and_check_tree(a.parents + (size_t)b * a.N, a.N, pc.par, &pc.flag);  // barriers inside
   if (st) return st;
   if (threadIdx.x == 0) {
-    const int L = a.path_len[b];
-    int ok = (L >= 1 && L <= a.Lmax);
+    const int L = pc.L;
+    int ok = (L >= 1 && L <= cap);
     int prev = -1;
     for (int r = 0; ok && r < L; ++r) {
-      const int node = a.path[(size_t)b * a.Lmax + r];
+      const int node = pc.path[r];
       ok = (node >= 0 && node < a.N && pc.par[node] == prev);
       prev = node;
     }
     pc.status = ok ? 0 : TV_ERR_BAD_PATH;
-    pc.L = L;
     pc.last = prev;
   }
   __syncthreads();
   return pc.status;
 }
 
-// One CTA per (sequence, head): copy the accepted checkpoint over S_0.
+constexpr int kMaxVec = 16;  // 16-byte vectors per thread: a 128 x 128 fp32 tile over 256 threads
+
+// One CTA per (sequence, head): copy the accepted checkpoint over S_0.  The tile is loaded into
+// registers from the node the (not yet checked) path names, clamped into [0, N), while the path
+// is being checked; it is stored only if the check passes, and then that node is the accepted
+// one.
 template <typename TS>
 __global__ void __launch_bounds__(kThreads) commit_fork_kernel(CommitArgs a) {
   __shared__ PathCheck pc;
   const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int L0 = a.path_len[b];
+  int guess = (L0 >= 1 && L0 <= a.Lmax) ? a.path[(size_t)b * a.Lmax + L0 - 1] : 0;
+  guess = guess < 0 ? 0 : (guess >= a.N ? a.N - 1 : guess);
+  const size_t tile = (size_t)a.dv * a.dk * sizeof(TS);  // bytes, a multiple of 16
+  const int nvec = (int)(tile / 16);                      // <= kMaxVec * kThreads
+  const uint4* src = reinterpret_cast<const uint4*>(
+      static_cast<const char*>(a.node_states) + ((((size_t)b * a.N + guess) * a.H + h) * tile));
+  uint4 buf[kMaxVec];
+#pragma unroll
+  for (int u = 0; u < kMaxVec; ++u) {
+    const int j = threadIdx.x + u * kThreads;
+    if (j < nvec) buf[u] = __ldg(src + j);
+  }
   const int st = check_path(a, b, pc);
   if (h == 0 && threadIdx.x == 0) a.err[b] = st;
-  if (st) return;
-  const size_t tile = (size_t)a.dv * a.dk * sizeof(TS);  // bytes, a multiple of 16
-  const uint4* src = reinterpret_cast<const uint4*>(
-      static_cast<const char*>(a.node_states) + ((((size_t)b * a.N + pc.last) * a.H + h) * tile));
+  if (st || pc.last != guess) return;  // pc.last == guess whenever the path is valid
   uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.S0) + ((size_t)b * a.H + h) * tile);
-  for (size_t j = threadIdx.x; j < tile / 16; j += kThreads) dst[j] = __ldg(src + j);
+#pragma unroll
+  for (int u = 0; u < kMaxVec; ++u) {
+    const int j = threadIdx.x + u * kThreads;
+    if (j < nvec) dst[j] = buf[u];
+  }
 }
 
 constexpr int kLPR = 8;
-constexpr int kRows = 32;  // rows of S_0 per CTA in WY mode
+constexpr int kRows = 32;          // rows of S_0 per pass of a CTA in WY mode
+constexpr int kStride = 8 * kLPR;  // lane l holds columns l * 8 + j * kStride .. + 7
 
-// One CTA per (sequence, head, 32-row slab): S_0 <- gamma_a S_0 + sum_r Gamma w k^T.
+// One CTA per (sequence, head): S_0 <- gamma_a S_0 + sum_r Gamma w k^T.  Thread (row rl, lane)
+// owns rows rl, rl + 32, ... of the head.  All of them are loaded before the path check; the
+// path's log(gamma), w rows and keys are then fetched in one phase into shared memory.
 template <typename TIO, typename TS, int DK>
-__global__ void __launch_bounds__(kThreads) commit_wy_kernel(CommitArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) commit_wy_kernel(CommitArgs a) {
   constexpr int CPL = DK / kLPR;
   __shared__ PathCheck pc;
   __shared__ float coef[TV_MAX_NODES];
-  __shared__ int nodes[TV_MAX_NODES];
-  extern __shared__ float wsm[];  // [L][kRows]
-  const int slabs = a.dv / kRows;
-  const int b = blockIdx.x / (a.H * slabs), h = (blockIdx.x / slabs) % a.H, slab = blockIdx.x % slabs;
-  const int st = check_path(a, b, pc);
-  if (h == 0 && slab == 0 && threadIdx.x == 0) a.err[b] = st;
-  if (st) return;
-  const int L = pc.L, N = a.N, H = a.H;
-  const float lga = a.log_gamma[((size_t)b * N + pc.last) * H + h];
-  for (int r = threadIdx.x; r < L; r += kThreads) {
-    const int node = a.path[(size_t)b * a.Lmax + r];
-    nodes[r] = node;
-    coef[r] = expf(lga - a.log_gamma[((size_t)b * N + node) * H + h]);
-  }
-  __syncthreads();
-  for (int x = threadIdx.x; x < L * kRows; x += kThreads) {
-    const int r = x / kRows, row = x % kRows;
-    wsm[x] = a.pseudo_v[(((size_t)b * N + nodes[r]) * H + h) * a.dv + slab * kRows + row];
-  }
-  __syncthreads();
+  __shared__ float lga_s;
+  extern __shared__ __align__(16) unsigned char dyn[];  // w [cap][dv] fp32, then k [cap][DK]
+  constexpr int P = 4;                 // passes of 32 rows: dv <= 128
+  const int passes = a.dv / kRows;
+  const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int N = a.N, H = a.H, dv = a.dv;
+  const int cap = a.Lmax < N ? a.Lmax : N;
+  float* wsm = reinterpret_cast<float*>(dyn);
+  TIO* ksm = reinterpret_cast<TIO*>(dyn + (size_t)cap * dv * sizeof(float));
+
   const int lane8 = threadIdx.x % kLPR, rl = threadIdx.x / kLPR;
-  const int row = slab * kRows + rl;
-  TS* s0 = static_cast<TS*>(a.S0) + (((size_t)b * H + h) * a.dv + row) * DK + lane8 * CPL;
-  const TIO* k = static_cast<const TIO*>(a.k);
-  float cur[CPL];
-  load_vec_rw<CPL>(s0, cur);
+  TS* s0 = static_cast<TS*>(a.S0) + (((size_t)b * H + h) * dv + rl) * DK + lane8 * 8;
+  // The rows as stored (8-column chunks of 16 or 32 bytes), converted only when they are used.
+  constexpr int VPC = 8 * (int)sizeof(TS) / 16;  // 16-byte vectors per chunk
+  uint4 raw[P][CPL / 8][VPC];
+#pragma unroll
+  for (int p = 0; p < P; ++p)
+    if (p < passes)
+#pragma unroll
+      for (int j = 0; j < CPL / 8; ++j)
+#pragma unroll
+        for (int u = 0; u < VPC; ++u)
+          raw[p][j][u] = reinterpret_cast<const uint4*>(s0 + (size_t)p * kRows * DK + j * kStride)[u];
+
+  const int st = check_path(a, b, pc);
+  if (h == 0 && threadIdx.x == 0) a.err[b] = st;
+  if (st) return;
+  const int L = pc.L;
+  if (threadIdx.x == 0) lga_s = a.log_gamma[((size_t)b * N + pc.last) * H + h];
+  for (int r = threadIdx.x; r < L; r += kThreads) coef[r] = a.log_gamma[((size_t)b * N + pc.path[r]) * H + h];
+  for (int x = threadIdx.x; x < L * dv; x += kThreads) {
+    const int r = x / dv, rr = x % dv;
+    wsm[x] = a.pseudo_v[(((size_t)b * N + pc.path[r]) * H + h) * dv + rr];
+  }
+  constexpr int KV = DK * (int)sizeof(TIO) / 16;  // 16-byte vectors per key
+  for (int x = threadIdx.x; x < L * KV; x += kThreads) {
+    const int r = x / KV, c = x % KV;
+    reinterpret_cast<uint4*>(ksm + (size_t)r * DK)[c] =
+        __ldg(reinterpret_cast<const uint4*>(static_cast<const TIO*>(a.k) + (((size_t)b * N + pc.path[r]) * H + h) * DK) + c);
+  }
+  __syncthreads();
+  const float lga = lga_s;
   const float gam = expf(lga);
 #pragma unroll
-  for (int e = 0; e < CPL; ++e) cur[e] *= gam;
-  for (int r = 0; r < L; ++r) {
-    float kf[CPL];
-    load_vec<CPL>(k + (((size_t)b * N + nodes[r]) * H + h) * DK + lane8 * CPL, kf);
-    const float c = coef[r] * wsm[r * kRows + rl];
+  for (int p = 0; p < P; ++p) {
+    if (p >= passes) break;
+    float cur[CPL];
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) cur[e] = fmaf(c, kf[e], cur[e]);
+    for (int j = 0; j < CPL / 8; ++j) {
+      if constexpr (sizeof(TS) == 2) {
+        unpack8(raw[p][j][0], cur + 8 * j);
+      } else {
+        const uint4 x0 = raw[p][j][0], x1 = raw[p][j][VPC - 1];
+        cur[8 * j] = __uint_as_float(x0.x); cur[8 * j + 1] = __uint_as_float(x0.y);
+        cur[8 * j + 2] = __uint_as_float(x0.z); cur[8 * j + 3] = __uint_as_float(x0.w);
+        cur[8 * j + 4] = __uint_as_float(x1.x); cur[8 * j + 5] = __uint_as_float(x1.y);
+        cur[8 * j + 6] = __uint_as_float(x1.z); cur[8 * j + 7] = __uint_as_float(x1.w);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) cur[e] *= gam;
+    for (int r = 0; r < L; ++r) {
+      const float c = expf(lga - coef[r]) * wsm[r * dv + p * kRows + rl];
+      const TIO* kr = ksm + (size_t)r * DK + lane8 * 8;
+#pragma unroll
+      for (int j = 0; j < CPL / 8; ++j) {
+        float kf[8];
+        if constexpr (sizeof(TIO) == 2) {
+          unpack8(*reinterpret_cast<const uint4*>(kr + j * kStride), kf);
+        } else {
+          const float4 x0 = *reinterpret_cast<const float4*>(kr + j * kStride);
+          const float4 x1 = *reinterpret_cast<const float4*>(kr + j * kStride + 4);
+          kf[0] = x0.x; kf[1] = x0.y; kf[2] = x0.z; kf[3] = x0.w;
+          kf[4] = x1.x; kf[5] = x1.y; kf[6] = x1.z; kf[7] = x1.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cur[8 * j + e] = fmaf(c, kf[e], cur[8 * j + e]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) store_vec<8>(s0 + (size_t)p * kRows * DK + j * kStride, cur + 8 * j);
   }
-  store_vec<CPL>(s0, cur);
 }
 
 template <typename TIO, typename TS, int DK>
 cudaError_t launch_wy_t(const CommitArgs& a, cudaStream_t s) {
-  const int max_len = a.Lmax < a.N ? a.Lmax : a.N;  // a valid path has distinct nodes
-  const size_t smem = (size_t)max_len * kRows * sizeof(float);
+  const int cap = a.Lmax < a.N ? a.Lmax : a.N;  // a valid path has distinct nodes
+  const size_t smem = (size_t)cap * (a.dv * sizeof(float) + DK * sizeof(TIO));
   auto kern = commit_wy_kernel<TIO, TS, DK>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<a.B * a.H * (a.dv / kRows), kThreads, smem, s>>>(a);
+  kern<<<a.B * a.H, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,8 @@
-// Bulk asynchronous copies (global -> shared) completed through shared-memory mbarriers, in
-// inline PTX for sm_100-family GPUs.  Every wait is bounded: a wait that gives up reports it so
-// the kernel can flag an error and leave instead of hanging.
+// Asynchronous copies (global -> shared) in inline PTX for sm_100-family GPUs: bulk copies
+// completed through shared-memory mbarriers, and per-thread cp.async copies completed through
+// commit groups.  Every mbarrier wait is bounded: a wait that gives up reports it so the kernel
+// can flag an error and leave instead of hanging.  A cp.async group wait needs no bound: it
+// returns once the thread's own copies have landed.
 #pragma once
 
 #include <stdint.h>
@@ -55,5 +57,20 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+
+// Per-thread asynchronous copy of 16 bytes (L2 only) or of 4 / 8 / 16 bytes (through L1);
+// both addresses aligned to the size.
+__device__ __forceinline__ void cp_async_16_cg(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+template <int BYTES>
+__device__ __forceinline__ void cp_async_ca(void* dst, const void* src) {
+  static_assert(BYTES == 4 || BYTES == 8 || BYTES == 16, "cp.async size");
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_addr(dst)), "l"(src), "n"(BYTES) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 }  // namespace tv
