@@ -42,6 +42,8 @@ struct TcHead {
   int lvl_nodes[TV_MAX_NODES];     // nodes grouped by depth
 };
 
+static_assert(sizeof(TcHead) % 8 == 0, "the path-entry table after the head is 8-byte aligned");
+
 __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* __restrict__ pseudo_v,
                                                              float* __restrict__ log_gamma, int cap, int Npad,
                                                              uint32_t tmem_cols, int v_in_smem,
@@ -57,9 +59,10 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   const uint32_t kq_bytes = (uint32_t)Npad * 128u;           // one k-block of K or Q
   unsigned char* sV = sKQ + 4 * kq_bytes;                    // V: 2 x Npad x 128 B (when it fits)
   TcHead& hd = *reinterpret_cast<TcHead*>(sV + (v_in_smem ? 2 * kq_bytes : 0));
-  int* pent = reinterpret_cast<int*>(&hd + 1);               // (node << 8) | path node, per entry
-  float* cK = reinterpret_cast<float*>(pent + cap);
-  float* cQ = cK + cap;
+  // Per (node, path entry) pair e, root first: coef[e] = {c_ij, e_ij} and pent[e] = (node << 8) |
+  // path node.
+  float2* coef = reinterpret_cast<float2*>(&hd + 1);
+  int* pent = reinterpret_cast<int*>(coef + cap);
   float* wsm = reinterpret_cast<float*>(sKQ);                // [N][128], after the MMAs are done
 
   const int N = a.N, H = a.H;
@@ -211,8 +214,7 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
       if (valid && gl == 0) {
         const int t = e - hd.off[i];
         const float G = expf(hd.lg[i] - hd.lg[j]);
-        cK[e] = (t < hd.depth[i]) ? hd.beta[i] * G * kk : 0.f;
-        cQ[e] = a.q_scale * G * qk;
+        coef[e] = make_float2((t < hd.depth[i]) ? hd.beta[i] * G * kk : 0.f, a.q_scale * G * qk);
       }
     }
   }
@@ -254,20 +256,38 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
           }
         }
         tmem_wait_ld();
+        // Every node of the level has depth d: walk the d ancestors of all kBatch nodes together
+        // (independent chains), accumulating both the solve and the ancestors' share of the output
+        // from one read of each ancestor's w.
+        float w[kBatch], ov[kBatch];
+        int o[kBatch];
+#pragma unroll
+        for (int x = 0; x < kBatch; ++x) {
+          const int i = nodes[x] < 0 ? 0 : nodes[x];
+          const float gam = hd.gam[i];
+          o[x] = hd.off[i];
+          w[x] = hd.beta[i] * (vv[x] - gam * __uint_as_float(dk[x]));
+          ov[x] = q_scale * gam * __uint_as_float(dq[x]);
+        }
+        for (int t = 0; t < d; ++t) {
+#pragma unroll
+          for (int x = 0; x < kBatch; ++x) {
+            if (nodes[x] < 0) continue;
+            const float2 c = coef[o[x] + t];
+            const float wj = wsm[(pent[o[x] + t] & 255) * kD + r];
+            w[x] = fmaf(-c.x, wj, w[x]);
+            ov[x] = fmaf(c.y, wj, ov[x]);
+          }
+        }
 #pragma unroll
         for (int x = 0; x < kBatch; ++x) {
           const int i = nodes[x];
           if (i < 0) continue;
-          const float gam = hd.gam[i];
-          const int dd = hd.depth[i], o = hd.off[i];
-          float w = hd.beta[i] * (vv[x] - gam * __uint_as_float(dk[x]));
-          for (int t = 0; t < dd; ++t) w -= cK[o + t] * wsm[(pent[o + t] & 255) * kD + r];
-          wsm[i * kD + r] = w;
-          float ov = q_scale * gam * __uint_as_float(dq[x]);
-          for (int t = 0; t <= dd; ++t) ov = fmaf(cQ[o + t], wsm[(pent[o + t] & 255) * kD + r], ov);
+          wsm[i * kD + r] = w[x];
+          const float ovx = fmaf(coef[o[x] + d].y, w[x], ov[x]);
           const size_t ni = ((size_t)b * N + i) * H + h;
-          out[ni * kD + r] = from_f32<bf16>(ov);
-          pseudo_v[ni * kD + r] = w;
+          out[ni * kD + r] = from_f32<bf16>(ovx);
+          pseudo_v[ni * kD + r] = w[x];
         }
       }
       __syncthreads();
