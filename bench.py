@@ -86,6 +86,22 @@ def compact_bytes(path_lens, Hkv, hd, e=2):
     return sum(path_lens) * Hkv * hd * e * 2 * 2   # K and V, read + write
 
 
+# ----------------------------------------------------------------------------- multi-rank
+def max_over_ranks(dist, ms: float, device: str) -> float:
+    """The slowest rank's time (every rank gets it); ``dist`` None means a single process."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank (weak scaling)."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------------------- helpers
 def kernel_traffic(row: str):
     """dram read+write bytes per launch of a row's main kernel from ``profiles/traffic.txt``, a
@@ -426,11 +442,7 @@ def run_ours(args) -> None:
     t_end.record(stream)
     barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), "cuda")
     ms_per_step = total_ms / args.steps
     step_ms = sorted(s.elapsed_time(e) for s, e in steps_ev)
     row_ms = {r: sum(s.elapsed_time(e) for s, e in ev[r]) / args.steps for r in rnd.rows}
@@ -449,14 +461,9 @@ def run_ours(args) -> None:
             rnd.step_e2e()
         e.record(stream)
         barrier()
-        e2e_ms = s.elapsed_time(e) / args.steps
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        nodes = rnd.B * rnd.N * rnd.layers * 2 * world
-        e2e = {"value": nodes / (e2e_ms * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        e2e_ms = max_over_ranks(dist, s.elapsed_time(e) / args.steps, "cuda")
+        e2e = {"value": whole_job_rate(rnd.B * rnd.N * rnd.layers * 2, world, e2e_ms), "unit": "nodes/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     peaks = load_peaks()
     B, N, H, dk, dv = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv
@@ -487,8 +494,7 @@ def run_ours(args) -> None:
     roof = {"kernel": dom, "bound": "hbm", "achieved": rows[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": rows[dom]["frac_hbm"], "traffic": kernel_traffic(dom),
             "peak_source": peaks["source"] + " (copy, burst)"}
-    nodes_per_step = B * N * rnd.layers * 2 * world
-    value = nodes_per_step / (ms_per_step * 1e-3)
+    value = whole_job_rate(B * N * rnd.layers * 2, world, ms_per_step)
     mem = {"fork_checkpoint_bytes": rnd.fork_state_bytes, "wy_pseudo_value_bytes": rnd.wy_state_bytes,
            "pages_bytes_per_checkpoint": checkpoint_bytes(24, 16, 128, 128, 2),
            "pages_accounting_fork_bytes": checkpoint_bytes(24, 16, 128, 128, 2) * B * N,
