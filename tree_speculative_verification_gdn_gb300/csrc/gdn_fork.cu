@@ -208,9 +208,34 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     const int i = sc.order[t];
     sc.ent[t] = make_int4(i, (sc.src[i] + 1) | ((sc.push[i] + 1) << 8), 0, 0);
   }
+  // Pulls one item's inputs into L2 ahead of use: alpha, beta, k and q of every node, the
+  // slab's v rows and S_0 rows.  The node loop's register prefetch then waits on L2, not HBM.
+  auto prefetch_item = [&](int it) {
+    const int hh = it / slabs, r0 = (it % slabs) * kRows;
+    const size_t n0 = (size_t)b * N * H + hh;
+    const int kq_lines = DK * (int)sizeof(TIO) / 128 > 0 ? DK * (int)sizeof(TIO) / 128 : 1;
+    const int per_node = 2 * kq_lines + 1;       // k lines, q lines, the slab's v rows
+    for (int x = tid; x < N * per_node; x += kThreads) {
+      const int t = x / per_node, c = x % per_node;
+      const size_t nh = n0 + (size_t)t * H;
+      const void* p = c < kq_lines ? (const void*)(k + nh * DK + c * (128 / sizeof(TIO)))
+                    : c < 2 * kq_lines ? (const void*)(q + nh * DK + (c - kq_lines) * (128 / sizeof(TIO)))
+                                       : (const void*)(v + nh * dv + r0);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+    const int s0_lines = kRows * DK * (int)sizeof(TS) / 128;
+    for (int x = tid; x < s0_lines; x += kThreads)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(S0 + (((size_t)b * H + hh) * dv + r0) * DK) + x * 128));
+    for (int x = tid; x < (N * H + 31) / 32; x += kThreads) {  // alpha and beta of the sequence
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.alpha + (size_t)b * N * H + x * 32));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beta + (size_t)b * N * H + x * 32));
+    }
+  };
+  if (g < items) prefetch_item(g);
   for (int item = g; item < items; item += ctas_per_seq) {
     const int h = item / slabs, r = (item % slabs) * kRows + rl;
     const size_t nh0 = (size_t)b * N * H + h;    // (b, node 0, h)
+    if (item + ctas_per_seq < items) prefetch_item(item + ctas_per_seq);
     __syncthreads();                             // the previous item is done with alpha / beta
     for (int t = tid; t < N; t += kThreads) {
       const size_t nh = nh0 + (size_t)sc.ent[t].x * H;
@@ -311,18 +336,14 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     };
     // Three register buffers rotate by unrolling, so each prefetch stays in flight for two
     // nodes (a register copy would wait for it).
-    Raw<TIO, CPL> ra, rb, rc;
+    Raw<TIO, CPL> ra, rb;
     fetch(0, ra);
-    fetch(1, rb);
-    for (int t = 0; t < N; t += 3) {
-      fetch(t + 2, rc);
+    for (int t = 0; t < N; t += 2) {
+      fetch(t + 1, rb);
       body(ra);
       if (t + 1 >= N) break;
-      fetch(t + 3, ra);
+      fetch(t + 2, ra);
       body(rb);
-      if (t + 2 >= N) break;
-      fetch(t + 4, rb);
-      body(rc);
     }
   }
 }
