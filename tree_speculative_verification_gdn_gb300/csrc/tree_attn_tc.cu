@@ -33,7 +33,9 @@ constexpr float kRescale = 8.0f;  // log2 headroom of the lazily raised running 
 
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[2];
+  uint64_t k_full[2];
+  uint64_t v_full[2];
+  uint64_t k_empty[2];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
@@ -53,7 +55,7 @@ struct Layout {
   static constexpr uint32_t V0 = K0 + 2 * KVB;
   static constexpr uint32_t P0 = V0 + 2 * KVB;
   static constexpr uint32_t BARS = P0 + 2 * PB;
-  static constexpr uint32_t TOTAL = BARS + 128;
+  static constexpr uint32_t TOTAL = BARS + 256;
   static constexpr uint32_t TMEM_COLS = (HD + 2 * KT <= 256) ? 256 : 512;
 };
 
@@ -101,7 +103,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bar.q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar.kv_full[s], 1);
+      mbar_init(&bar.k_full[s], 1);
+      mbar_init(&bar.v_full[s], 1);
+      mbar_init(&bar.k_empty[s], 1);
       mbar_init(&bar.s_full[s], 1);
       mbar_init(&bar.p_full[s], kRows);
       mbar_init(&bar.pv_done[s], 1);
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tO = bar.tmem_base;          // columns [0, HD): output accumulator
   const uint32_t tS = bar.tmem_base + HD;     // columns [HD, HD + 2 KT): two S buffers
   unsigned char* sQ = sm + L::Q;
-  int issued = 0;  // K/V tiles whose loads the producer started
+  int issued_k = 0, issued_v = 0;  // K and V tiles whose loads the producer started
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
@@ -126,56 +130,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < HD / 64; ++c) tma_load_5d(sQ + c * L::QCHUNK, &mQ, c * 64, 0, kvh, mt * npt, b, &bar.q_full);
       const int last_lb = (total - 1) / 16;
       const int* table = a.block_table + (size_t)b * a.max_blocks;
-      for (int j = 0; j < T; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !wait_or_abort(&bar.pv_done[st], ((j - 2) >> 1) & 1, abort)) break;
-        mbar_arrive_expect_tx(&bar.kv_full[st], 2 * L::KVB);
-        issued = j + 1;
-        const int lb0 = (lo + j * KT) / 16;
+      // K (or V) tile j into stage j & 1: four 16-token pages, each HD / 64 boxes of 64 columns.
+      auto load_tile = [&](const CUtensorMap* map, uint32_t region, int j, uint64_t* full) {
+        const int st = j & 1, lb0 = (lo + j * KT) / 16;
+        mbar_arrive_expect_tx(full, L::KVB);
         for (int p = 0; p < KT / 16; ++p) {
           const int blk = table[min(lb0 + p, last_lb)];
-          for (int c = 0; c < HD / 64; ++c) {
-            tma_load_4d(sm + L::K0 + st * L::KVB + c * L::KVCHUNK + p * 2048, &mK, c * 64, 0, kvh, blk,
-                        &bar.kv_full[st]);
-            tma_load_4d(sm + L::V0 + st * L::KVB + c * L::KVCHUNK + p * 2048, &mV, c * 64, 0, kvh, blk,
-                        &bar.kv_full[st]);
-          }
+          for (int c = 0; c < HD / 64; ++c)
+            tma_load_4d(sm + region + st * L::KVB + c * L::KVCHUNK + p * 2048, map, c * 64, 0, kvh, blk, full);
         }
+      };
+      // Keys run one tile ahead of values: the keys' stage frees when S of the tile two back is
+      // done, the values' stage when its PV is done.
+      load_tile(&mK, L::K0, 0, &bar.k_full[0]);
+      issued_k = 1;
+      for (int j = 0; j < T; ++j) {
+        const int jk = j + 1;
+        if (jk < T) {
+          if (jk >= 2 && !wait_or_abort(&bar.k_empty[jk & 1], ((jk - 2) >> 1) & 1, abort)) break;
+          load_tile(&mK, L::K0, jk, &bar.k_full[jk & 1]);
+          issued_k = jk + 1;
+        }
+        if (j >= 2 && !wait_or_abort(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort)) break;
+        load_tile(&mV, L::V0, j, &bar.v_full[j & 1]);
+        issued_v = j + 1;
       }
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
+    // Event-driven: S of the next tile as soon as its keys have landed and its TMEM buffer is
+    // free (the softmax of the tile two back has read it, which the PV of that tile implies);
+    // PV of the oldest tile as soon as its P and values are ready.
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(128, KT), idO = idesc_bf16_f32(128, HD, true);
       const uint32_t q0 = smem_addr(sQ);
-      auto issue_pv = [&](int pj) {
-        const int ps = pj & 1;
-        if (!wait_or_abort(&bar.p_full[ps], (pj >> 1) & 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t p0 = smem_addr(sm + L::P0 + ps * L::PB), v0 = smem_addr(sm + L::V0 + ps * L::KVB);
-#pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk)
-          mma_bf16(tO, sw128_desc(p0 + kk * 32), sw128_mn_desc(v0 + kk * 2048, L::KVCHUNK), idO,
-                   (pj > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar.pv_done[ps]);
-        return true;
-      };
       bool ok = wait_or_abort(&bar.q_full, 0, abort);
-      for (int j = 0; ok && j < T; ++j) {
-        const int st = j & 1;
-        if (!wait_or_abort(&bar.kv_full[st], (j >> 1) & 1, abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k0 = smem_addr(sm + L::K0 + st * L::KVB);
-        for (int c = 0; c < HD / 64; ++c) {
+      int ns = 0, np = 0;
+      uint32_t idle = 0;
+      while (ok && np < T) {
+        bool progressed = false;
+        if (ns < T && ns < np + 2 && mbar_test(&bar.k_full[ns & 1], (ns >> 1) & 1)) {
+          tc_fence_after();
+          const int st = ns & 1;
+          const uint32_t k0 = smem_addr(sm + L::K0 + st * L::KVB);
+          for (int c = 0; c < HD / 64; ++c) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tS + st * KT, sw128_desc(q0 + c * L::QCHUNK + ks * 32), sw128_desc(k0 + c * L::KVCHUNK + ks * 32),
-                     idS, (c | ks) ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16(tS + st * KT, sw128_desc(q0 + c * L::QCHUNK + ks * 32),
+                       sw128_desc(k0 + c * L::KVCHUNK + ks * 32), idS, (c | ks) ? 1u : 0u);
+          }
+          mma_commit(&bar.s_full[st]);
+          mma_commit(&bar.k_empty[st]);
+          ++ns;
+          progressed = true;
         }
-        mma_commit(&bar.s_full[st]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        if (np < ns && mbar_test(&bar.p_full[np & 1], (np >> 1) & 1) &&
+            mbar_test(&bar.v_full[np & 1], (np >> 1) & 1)) {
+          tc_fence_after();
+          const int ps = np & 1;
+          const uint32_t p0 = smem_addr(sm + L::P0 + ps * L::PB), v0 = smem_addr(sm + L::V0 + ps * L::KVB);
+#pragma unroll
+          for (int kk = 0; kk < KT / 16; ++kk)
+            mma_bf16(tO, sw128_desc(p0 + kk * 32), sw128_mn_desc(v0 + kk * 2048, L::KVCHUNK), idO,
+                     (np > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar.pv_done[ps]);
+          ++np;
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle > (1u << 22)) {
+          *abort = 1;
+          ok = false;
+        } else if (idle > 64) {
+          __nanosleep(64);
+          if ((idle & 255) == 0 && *abort) ok = false;
+        }
       }
-      if (ok) issue_pv(T - 1);
     }
   } else {
     // ------------------------------------------------------------ softmax, one row per thread
@@ -279,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l += psum;
       if (base + KT > hi) {  // zero V rows past the chunk end: their P is 0 but contents are unknown
-        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.kv_full[st], (j >> 1) & 1, abort))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.v_full[st], (j >> 1) & 1, abort))) { ok = false; break; }
         const int first = hi - base;
         unsigned char* v0 = sm + L::V0 + st * L::KVB;
         for (int idx = r; idx < (KT - first) * (HD / 8); idx += kRows) {
@@ -318,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 4 && lane == 0) {
       mbar_wait(&bar.q_full, 0);
-      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) mbar_wait(&bar.kv_full[j & 1], (j >> 1) & 1);
+      for (int j = issued_k - 2 < 0 ? 0 : issued_k - 2; j < issued_k; ++j) mbar_wait(&bar.k_full[j & 1], (j >> 1) & 1);
+      for (int j = issued_v - 2 < 0 ? 0 : issued_v - 2; j < issued_v; ++j) mbar_wait(&bar.v_full[j & 1], (j >> 1) & 1);
     }
     if (tid == 0) a.err[b] = TV_ERR_TIMEOUT;
   }
