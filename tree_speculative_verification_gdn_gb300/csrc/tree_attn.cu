@@ -73,16 +73,43 @@ __global__ void attn_check_kernel(AttnArgs a) {
   if (threadIdx.x == 0) a.err[b] = st;
 }
 
-// One CTA per (sequence, node).
-__global__ void attn_rope_kernel(AttnArgs a, bf16* __restrict__ qrot) {
+// Inverse frequencies theta^(-2c/hd), c < hd/2, computed once per call in fp64 on the host and
+// passed as fp32 (hi, lo) pairs: hi + lo carries about 48 bits.
+struct RopeTable {
+  float2 inv[128];
+};
+
+// One CTA per (sequence, node).  The angle pos * inv is formed as a double-float product (the
+// FMA gives the rounding error of pos * hi exactly) and reduced modulo 2 pi with the three-part
+// Cody-Waite split 2 pi = C1 + C2 + C3, C1 = 25/4 having 5 significant bits so that k * C1 is
+// exact for every k < 2^19 (positions below 2^21); the reduced angle is then within a few ulp
+// before the fp32 sincos.
+__global__ void attn_rope_kernel(AttnArgs a, bf16* __restrict__ qrot, const __grid_constant__ RopeTable tab) {
+  constexpr float C1 = 6.25f, C2 = 3.318530693650246e-2f, C3 = 2.430837753308879e-10f;
+  constexpr float kInv2Pi = 0.15915494309189535f;
+  __shared__ float2 cs[128];  // (cos, sin) of each pair index c
   const int b = blockIdx.x / a.N, i = blockIdx.x % a.N;
   if (a.err[b]) return;
   const int32_t* par = a.parents + (size_t)b * a.N;
   int depth = 0;
   for (int j = par[i]; j >= 0; j = par[j]) ++depth;
   const int P = a.prefix_len[b];
-  const long long pos = (long long)P + depth;
+  const float pos = (float)(P + depth);  // exact: positions stay below 2^24
   const int hd = a.hd, half = hd / 2, bs = a.block_size;
+  for (int c = threadIdx.x; c < half; c += blockDim.x) {
+    const float2 iv = tab.inv[c];
+    const float hi = pos * iv.x;
+    const float lo = fmaf(pos, iv.x, -hi) + pos * iv.y;
+    const float k = rintf(hi * kInv2Pi);
+    float r = fmaf(-k, C1, hi);
+    r = fmaf(-k, C2, r);
+    r = fmaf(-k, C3, r);
+    r += lo;
+    float sn, cn;
+    sincosf(r, &sn, &cn);
+    cs[c] = make_float2(cn, sn);
+  }
+  __syncthreads();
   const int slot = P + i;
   const int blk = a.block_table[(size_t)b * a.max_blocks + slot / bs];
   const bf16* q = static_cast<const bf16*>(a.q) + ((size_t)b * a.N + i) * a.Hq * hd;
@@ -91,27 +118,32 @@ __global__ void attn_rope_kernel(AttnArgs a, bf16* __restrict__ qrot) {
   bf16* qo = qrot + ((size_t)b * a.N + i) * a.Hq * hd;
   bf16* kc = static_cast<bf16*>(a.k_cache);
   bf16* vc = static_cast<bf16*>(a.v_cache);
-  const double two_pi = 6.283185307179586;
-  for (int c = threadIdx.x; c < half; c += blockDim.x) {
-    // Angle in fp64, reduced to [-pi, pi] before the fp32 sin/cos: positions reach ~33K.
-    const double inv = pow((double)a.rope_theta, -2.0 * c / hd);
-    const double ang = (double)pos * inv;
-    const float red = (float)(ang - two_pi * rint(ang / two_pi));
-    float sn, cs;
-    sincosf(red, &sn, &cs);
-    for (int h = 0; h < a.Hq; ++h) {
-      const float x1 = to_f32(q[h * hd + c]), x2 = to_f32(q[h * hd + c + half]);
-      qo[h * hd + c] = from_f32<bf16>(x1 * cs - x2 * sn);
-      qo[h * hd + c + half] = from_f32<bf16>(x2 * cs + x1 * sn);
-    }
-    for (int g = 0; g < a.Hkv; ++g) {
-      const float x1 = to_f32(kn[g * hd + c]), x2 = to_f32(kn[g * hd + c + half]);
+  // Every (head, column pair c, c + 1) of q and k: rotate-half pairs (x_c, x_{c + half}).
+  const int hp = half / 2;
+  for (int x = threadIdx.x; x < (a.Hq + a.Hkv) * hp; x += blockDim.x) {
+    const int h = x / hp, c = 2 * (x % hp);
+    const float2 t0 = cs[c], t1 = cs[c + 1];
+    const bf16* src;
+    bf16* dst;
+    if (h < a.Hq) {
+      src = q + (size_t)h * hd;
+      dst = qo + (size_t)h * hd;
+    } else {
+      const int g = h - a.Hq;
       const size_t row = (((size_t)blk * a.Hkv + g) * bs + slot % bs) * hd;
-      kc[row + c] = from_f32<bf16>(x1 * cs - x2 * sn);
-      kc[row + c + half] = from_f32<bf16>(x2 * cs + x1 * sn);
-      vc[row + c] = vn[g * hd + c];
-      vc[row + c + half] = vn[g * hd + c + half];
+      src = kn + (size_t)g * hd;
+      dst = kc + row;
+      *reinterpret_cast<uint32_t*>(vc + row + c) = *reinterpret_cast<const uint32_t*>(vn + (size_t)g * hd + c);
+      *reinterpret_cast<uint32_t*>(vc + row + c + half) =
+          *reinterpret_cast<const uint32_t*>(vn + (size_t)g * hd + c + half);
     }
+    const uint32_t u1 = *reinterpret_cast<const uint32_t*>(src + c);
+    const uint32_t u2 = *reinterpret_cast<const uint32_t*>(src + c + half);
+    const float a0 = bf16lo(u1), a1 = bf16hi(u1), b0 = bf16lo(u2), b1 = bf16hi(u2);
+    float o1[2] = {a0 * t0.x - b0 * t0.y, a1 * t1.x - b1 * t1.y};
+    float o2[2] = {b0 * t0.x + a0 * t0.y, b1 * t1.x + a1 * t1.y};
+    *reinterpret_cast<uint32_t*>(dst + c) = pack_bf16x2(o1[0], o1[1]);
+    *reinterpret_cast<uint32_t*>(dst + c + half) = pack_bf16x2(o2[0], o2[1]);
   }
 }
 
@@ -278,7 +310,13 @@ cudaError_t launch_tree_attn(const AttnArgs& a, void* workspace, size_t workspac
   if (workspace_bytes < p.total) return cudaErrorInvalidValue;
   char* ws = static_cast<char*>(workspace);
   attn_check_kernel<<<a.B, 128, 0, s>>>(a);
-  attn_rope_kernel<<<a.B * a.N, 128, 0, s>>>(a, reinterpret_cast<bf16*>(ws + p.off_qrot));
+  RopeTable tab;
+  for (int c = 0; c < a.hd / 2; ++c) {
+    const double inv = pow((double)a.rope_theta, -2.0 * c / a.hd);
+    tab.inv[c].x = (float)inv;
+    tab.inv[c].y = (float)(inv - (double)tab.inv[c].x);
+  }
+  attn_rope_kernel<<<a.B * a.N, 128, 0, s>>>(a, reinterpret_cast<bf16*>(ws + p.off_qrot), tab);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (attn_tc_supported(a))
