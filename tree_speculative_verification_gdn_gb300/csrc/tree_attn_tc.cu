@@ -30,12 +30,15 @@ constexpr int kRows = 128;        // query rows per CTA
 constexpr int kThreads = 192;     // warps 0-3 softmax, warp 4 TMA, warp 5 MMA
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale = 8.0f;  // log2 headroom of the lazily raised running max
+constexpr int kKStages = 2;       // key tiles in the ring
+constexpr int kVStages = 3;       // value tiles in the ring
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[2];
-  uint64_t v_full[2];
-  uint64_t k_empty[2];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
@@ -44,17 +47,17 @@ struct Bars {
   int abort;
 };
 
+static_assert(sizeof(Bars) <= 256, "barriers fit their reserved region");
+
 template <int HD>
 struct Layout {
   static constexpr uint32_t QCHUNK = kRows * 128;    // one 64-column chunk of Q
   static constexpr uint32_t KVCHUNK = KT * 128;      // one 64-column chunk of a K or V tile
   static constexpr uint32_t KVB = HD / 64 * KVCHUNK; // one K (or V) tile
-  static constexpr uint32_t PB = kRows * KT * 2;     // one P tile
   static constexpr uint32_t Q = 0;
-  static constexpr uint32_t K0 = Q + HD / 64 * QCHUNK;
-  static constexpr uint32_t V0 = K0 + 2 * KVB;
-  static constexpr uint32_t P0 = V0 + 2 * KVB;
-  static constexpr uint32_t BARS = P0 + 2 * PB;
+  static constexpr uint32_t K0 = Q + HD / 64 * QCHUNK;  // kKStages key tiles
+  static constexpr uint32_t V0 = K0 + kKStages * KVB;   // kVStages value tiles
+  static constexpr uint32_t BARS = V0 + kVStages * KVB;
   static constexpr uint32_t TOTAL = BARS + 256;
   static constexpr uint32_t TMEM_COLS = (HD + 2 * KT <= 256) ? 256 : 512;
 };
@@ -102,10 +105,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&bar.q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bar.k_full[s], 1);
-      mbar_init(&bar.v_full[s], 1);
       mbar_init(&bar.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bar.v_full[s], 1);
+      mbar_init(&bar.v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.s_full[s], 1);
       mbar_init(&bar.p_full[s], kRows);
       mbar_init(&bar.pv_done[s], 1);
@@ -124,43 +132,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   int issued_k = 0, issued_v = 0;  // K and V tiles whose loads the producer started
 
   if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer (whole warp)
+    // Lane 0 posts a tile's expected bytes; then lane p < KT / 16 issues the boxes of the tile's
+    // page p.  Each of those lanes reads the block ids of its page of the next key tile and of
+    // the next value tile as soon as the current ones are issued, so no table read waits.
+    const int last_lb = (total - 1) / 16;
+    const int* table = a.block_table + (size_t)b * a.max_blocks;
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar.q_full, (uint32_t)(HD * G * npt * 2));
       for (int c = 0; c < HD / 64; ++c) tma_load_5d(sQ + c * L::QCHUNK, &mQ, c * 64, 0, kvh, mt * npt, b, &bar.q_full);
-      const int last_lb = (total - 1) / 16;
-      const int* table = a.block_table + (size_t)b * a.max_blocks;
-      // K (or V) tile j into stage j & 1: four 16-token pages, each HD / 64 boxes of 64 columns.
-      auto load_tile = [&](const CUtensorMap* map, uint32_t region, int j, uint64_t* full) {
-        const int st = j & 1, lb0 = (lo + j * KT) / 16;
-        mbar_arrive_expect_tx(full, L::KVB);
-        for (int p = 0; p < KT / 16; ++p) {
-          const int blk = table[min(lb0 + p, last_lb)];
-          for (int c = 0; c < HD / 64; ++c)
-            tma_load_4d(sm + region + st * L::KVB + c * L::KVCHUNK + p * 2048, map, c * 64, 0, kvh, blk, full);
-        }
-      };
-      // Keys run one tile ahead of values: the keys' stage frees when S of the tile two back is
-      // done, the values' stage when its PV is done.
-      load_tile(&mK, L::K0, 0, &bar.k_full[0]);
-      issued_k = 1;
-      for (int j = 0; j < T; ++j) {
-        const int jk = j + 1;
-        if (jk < T) {
-          if (jk >= 2 && !wait_or_abort(&bar.k_empty[jk & 1], ((jk - 2) >> 1) & 1, abort)) break;
-          load_tile(&mK, L::K0, jk, &bar.k_full[jk & 1]);
-          issued_k = jk + 1;
-        }
-        if (j >= 2 && !wait_or_abort(&bar.pv_done[j & 1], ((j - 2) >> 1) & 1, abort)) break;
-        load_tile(&mV, L::V0, j, &bar.v_full[j & 1]);
-        issued_v = j + 1;
+    }
+    auto page_blk = [&](int j) {  // block id of this lane's page of tile j
+      return (lane < KT / 16 && j < T) ? table[min((lo + j * KT) / 16 + lane, last_lb)] : 0;
+    };
+    // K (or V) tile j into stage st from block id blk of this lane's page: four 16-token pages,
+    // each HD / 64 boxes of 64 columns.
+    auto load_tile = [&](const CUtensorMap* map, uint32_t region, int st, int blk, uint64_t* full) {
+      if (lane == 0) mbar_arrive_expect_tx(full, L::KVB);
+      __syncwarp();
+      if (lane < KT / 16)
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_4d(sm + region + st * L::KVB + c * L::KVCHUNK + lane * 2048, map, c * 64, 0, kvh, blk, full);
+    };
+    auto wait_all = [&](uint64_t* w, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_or_abort(w, parity, abort));
+    };
+    // Keys run kKStages - 1 tiles ahead of values: a key stage frees when S of its previous
+    // tile is done, a value stage when the PV of its previous tile is done.
+    int kblk = page_blk(0), vblk = kblk;
+    for (int jk = 0; jk < kKStages - 1 && jk < T; ++jk) {
+      load_tile(&mK, L::K0, jk, kblk, &bar.k_full[jk]);
+      issued_k = jk + 1;
+      kblk = page_blk(jk + 1);
+    }
+    for (int j = 0; j < T; ++j) {
+      const int jk = j + kKStages - 1;
+      if (jk < T) {
+        if (jk >= kKStages && !wait_all(&bar.k_empty[jk % kKStages], ((jk - kKStages) / kKStages) & 1)) break;
+        load_tile(&mK, L::K0, jk % kKStages, kblk, &bar.k_full[jk % kKStages]);
+        issued_k = jk + 1;
+        kblk = page_blk(jk + 1);
       }
+      if (j >= kVStages && !wait_all(&bar.v_empty[j % kVStages], ((j - kVStages) / kVStages) & 1)) break;
+      load_tile(&mV, L::V0, j % kVStages, vblk, &bar.v_full[j % kVStages]);
+      issued_v = j + 1;
+      vblk = page_blk(j + 1);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
     // Event-driven: S of the next tile as soon as its keys have landed and its TMEM buffer is
-    // free (the softmax of the tile two back has read it, which the PV of that tile implies);
-    // PV of the oldest tile as soon as its P and values are ready.
+    // free -- the PV of the tile two back, which reads that tile's P from the same columns, has
+    // been issued (MMAs run in issue order, so it reads P before this S overwrites it); PV of the
+    // oldest tile as soon as its P and values are ready.
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(128, KT), idO = idesc_bf16_f32(128, HD, true);
       const uint32_t q0 = smem_addr(sQ);
@@ -169,10 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t idle = 0;
       while (ok && np < T) {
         bool progressed = false;
-        if (ns < T && ns < np + 2 && mbar_test(&bar.k_full[ns & 1], (ns >> 1) & 1)) {
+        if (ns < T && ns < np + 2 && mbar_test(&bar.k_full[ns % kKStages], (ns / kKStages) & 1)) {
           tc_fence_after();
-          const int st = ns & 1;
-          const uint32_t k0 = smem_addr(sm + L::K0 + st * L::KVB);
+          const int st = ns & 1, ks3 = ns % kKStages;
+          const uint32_t k0 = smem_addr(sm + L::K0 + ks3 * L::KVB);
           for (int c = 0; c < HD / 64; ++c) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -180,20 +203,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                        sw128_desc(k0 + c * L::KVCHUNK + ks * 32), idS, (c | ks) ? 1u : 0u);
           }
           mma_commit(&bar.s_full[st]);
-          mma_commit(&bar.k_empty[st]);
+          mma_commit(&bar.k_empty[ks3]);
           ++ns;
           progressed = true;
         }
         if (np < ns && mbar_test(&bar.p_full[np & 1], (np >> 1) & 1) &&
-            mbar_test(&bar.v_full[np & 1], (np >> 1) & 1)) {
+            mbar_test(&bar.v_full[np % kVStages], (np / kVStages) & 1)) {
           tc_fence_after();
-          const int ps = np & 1;
-          const uint32_t p0 = smem_addr(sm + L::P0 + ps * L::PB), v0 = smem_addr(sm + L::V0 + ps * L::KVB);
+          const int ps = np & 1, vs = np % kVStages;
+          // P of the tile sits in TMEM over the first KT / 2 columns of its S buffer.
+          const uint32_t v0 = smem_addr(sm + L::V0 + vs * L::KVB);
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk)
-            mma_bf16(tO, sw128_desc(p0 + kk * 32), sw128_mn_desc(v0 + kk * 2048, L::KVCHUNK), idO,
-                     (np > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_tmem_a(tO, tS + ps * KT + kk * 8, sw128_mn_desc(v0 + kk * 2048, L::KVCHUNK), idO,
+                            (np > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bar.pv_done[ps]);
+          mma_commit(&bar.v_empty[vs]);
           ++np;
           progressed = true;
         }
@@ -286,39 +311,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = rescale_o ? l * ex2_approx(m_used - mx) : 0.f;
         m_used = mx;
       }
-      if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[st], ((j - 2) >> 1) & 1, abort))) {
-        ok = false;
-        break;
-      }
-      unsigned char* prow = sm + L::P0 + st * L::PB + r * 128;
+      // P in bf16 pairs over the first KT / 2 columns of this tile's S buffer (already read).
+      uint32_t pk[KT / 2];
       float psum = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        float pv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float sv = s[ch * 8 + e];
-          // masked keys: 2^(-inf) = 0; a row with nothing visible yet keeps m_used = -inf
-          pv[e] = (m_used == -INFINITY) ? 0.f : ex2_approx(sv - m_used);
-        }
-        const uint4 packed = pack8(pv);
-        float back[8];
-        unpack8(packed, back);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) psum += back[e];
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = packed;
+      for (int e = 0; e < KT / 2; ++e) {
+        // masked keys: 2^(-inf) = 0; a row with nothing visible yet keeps m_used = -inf
+        const float p0 = (m_used == -INFINITY) ? 0.f : ex2_approx(s[2 * e] - m_used);
+        const float p1 = (m_used == -INFINITY) ? 0.f : ex2_approx(s[2 * e + 1] - m_used);
+        pk[e] = pack_bf16x2(p0, p1);
+        psum += bf16lo(pk[e]) + bf16hi(pk[e]);  // the sum of what PV will use
       }
+      tmem_st32(tS + lane_base + st * KT, pk);
       l += psum;
       if (base + KT > hi) {  // zero V rows past the chunk end: their P is 0 but contents are unknown
-        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.v_full[st], (j >> 1) & 1, abort))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_or_abort(&bar.v_full[j % kVStages], (j / kVStages) & 1, abort))) {
+          ok = false;
+          break;
+        }
         const int first = hi - base;
-        unsigned char* v0 = sm + L::V0 + st * L::KVB;
+        unsigned char* v0 = sm + L::V0 + (j % kVStages) * L::KVB;
         for (int idx = r; idx < (KT - first) * (HD / 8); idx += kRows) {
           const int kr = first + idx / (HD / 8), rem = idx % (HD / 8);
           *reinterpret_cast<uint4*>(v0 + (rem / 8) * L::KVCHUNK + kr * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async();
       }
-      fence_proxy_async();
       tc_fence_before();
       mbar_arrive(&bar.p_full[st]);
     }
@@ -349,8 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 4 && lane == 0) {
       mbar_wait(&bar.q_full, 0);
-      for (int j = issued_k - 2 < 0 ? 0 : issued_k - 2; j < issued_k; ++j) mbar_wait(&bar.k_full[j & 1], (j >> 1) & 1);
-      for (int j = issued_v - 2 < 0 ? 0 : issued_v - 2; j < issued_v; ++j) mbar_wait(&bar.v_full[j & 1], (j >> 1) & 1);
+      for (int j = issued_k - kKStages < 0 ? 0 : issued_k - kKStages; j < issued_k; ++j)
+        mbar_wait(&bar.k_full[j % kKStages], (j / kKStages) & 1);
+      for (int j = issued_v - kVStages < 0 ? 0 : issued_v - kVStages; j < issued_v; ++j)
+        mbar_wait(&bar.v_full[j % kVStages], (j / kVStages) & 1);
     }
     if (tid == 0) a.err[b] = TV_ERR_TIMEOUT;
   }
