@@ -212,10 +212,13 @@ class Round:
         # per-round inputs (copied from host in the end-to-end measurement)
         self.in_gdn = [dict(q=d(c.q), k=d(c.k), v=d(c.v), alpha=d(c.alpha), beta=d(c.beta)) for c in self.gdn_host]
         self.parents = d(c0.parents)
-        self.path, self.path_len = d(c0.path), d(c0.path_len)
+        # draft and target tokens under which the on-device accept walk takes the sampled paths
+        draft, target = W.walk_tokens(c0.trees, c0.path.numpy(), c0.path_len.numpy(), seed=seed + 1)
+        self.tokens = dict(draft=d(draft), target=d(target))
         self.in_attn = dict(q=d(a.q), k_new=d(a.k_new), v_new=d(a.v_new), block_table=d(a.block_table),
-                            prefix_len=d(a.prefix_len), parents=d(a.parents), path=d(a.path),
-                            path_len=d(a.path_len))
+                            prefix_len=d(a.prefix_len), parents=d(a.parents))
+        draft, target = W.walk_tokens(a.trees, a.path.numpy(), a.path_len.numpy(), seed=seed + 2)
+        self.a_tokens = dict(draft=d(draft), target=d(target))
         # resident state
         self.S0_fork = [d(c.S0) for c in self.gdn_host]
         self.S0_wy = [d(c.S0) for c in self.gdn_host]
@@ -232,6 +235,13 @@ class Round:
         self.lg = [torch.empty((B, N, H), dtype=torch.float32, device=dev) for _ in range(layers)]
         self.wy_state_bytes = torch.cuda.memory_allocated() - mem0
         i32 = torch.int32
+        # accepted paths: written by the accept walk each round, read by the commits / compaction
+        self.path = torch.empty(c0.path.shape, dtype=i32, device=dev)
+        self.path_len = torch.empty((B,), dtype=i32, device=dev)
+        self.next_tok = torch.empty((B,), dtype=i32, device=dev)
+        self.a_path = torch.empty(a.path.shape, dtype=i32, device=dev)
+        self.a_path_len = torch.empty((self.aB,), dtype=i32, device=dev)
+        self.a_next_tok = torch.empty((self.aB,), dtype=i32, device=dev)
         self.depth = torch.empty((B, N), dtype=i32, device=dev)
         self.mask = torch.empty((B, N, (N + 31) // 32), dtype=i32, device=dev)
         self.err = torch.zeros((16, max(B, self.aB)), dtype=i32, device=dev)
@@ -240,9 +250,9 @@ class Round:
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.slot_map = torch.empty(a.path.shape, dtype=i32, device=dev)
         self.new_len = torch.empty((self.aB,), dtype=i32, device=dev)
-        self.rows = ["tree_prepare", "fork_verify", "fork_commit", "wy_verify", "wy_commit", "tree_attn",
-                     "kv_compact"]
-        self.launches_per_step = 1 + layers * 4 + 4 + 1
+        self.rows = ["tree_prepare", "fork_verify", "accept_walk", "fork_commit", "wy_verify", "wy_commit",
+                     "tree_attn", "kv_compact"]
+        self.launches_per_step = 1 + layers * 4 + 4 + 1 + 2
 
     def step(self, ev=None):
         """One verify round.  ``ev``: optional dict row -> list of (start, end) event pairs."""
@@ -266,6 +276,10 @@ class Round:
             mark("fork_verify", lambda: tv.tv_gdn_tree_verify_fork(
                 x["q"], x["k"], x["v"], x["alpha"], x["beta"], self.S0_fork[l], self.parents, self.o_fork[l],
                 self.states[l], err[1, :B]))
+        # the target's tokens pick the accepted path on the device (one walk feeds both modes' commits)
+        mark("accept_walk", lambda: tv.tv_accept_walk(
+            self.parents, self.tokens["draft"], self.tokens["target"], self.path, self.path_len, self.next_tok,
+            err[7, :B]))
         for l in range(self.layers):
             mark("fork_commit", lambda: tv.tv_gdn_commit(
                 tv.TV_MODE_FORK, self.path, self.path_len, self.parents, self.S0_fork[l], err[2, :B],
@@ -285,9 +299,12 @@ class Round:
         mark("tree_attn", lambda: tv.tv_tree_attn(
             a["q"], a["k_new"], a["v_new"], self.k_cache, self.v_cache, a["block_table"], a["prefix_len"],
             a["parents"], self.a_out, self.ws, err[5, :aB], rope_theta=1e6))
+        mark("accept_walk", lambda: tv.tv_accept_walk(
+            a["parents"], self.a_tokens["draft"], self.a_tokens["target"], self.a_path, self.a_path_len,
+            self.a_next_tok, err[8, :aB]))
         mark("kv_compact", lambda: tv.tv_kv_compact(
-            self.k_cache, self.v_cache, a["block_table"], a["prefix_len"], a["parents"], a["path"], a["path_len"],
-            self.slot_map, self.new_len, err[6, :aB]))
+            self.k_cache, self.v_cache, a["block_table"], a["prefix_len"], a["parents"], self.a_path,
+            self.a_path_len, self.slot_map, self.new_len, err[6, :aB]))
 
     # end-to-end: per-round inputs from pinned host memory, outputs back to pinned host memory
     def host_buffers(self):
@@ -295,15 +312,17 @@ class Round:
         pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
         self.h_in = [{k: pin(v) for k, v in x.items()} for x in self.in_gdn]
         self.h_attn = {k: pin(v) for k, v in self.in_attn.items()}
-        self.h_parents, self.h_path, self.h_path_len = pin(self.parents), pin(self.path), pin(self.path_len)
+        self.h_parents = pin(self.parents)
+        self.h_tokens = [{k: pin(v) for k, v in x.items()} for x in (self.tokens, self.a_tokens)]
         self.h_o_fork = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.o_fork]
         self.h_o_wy = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.o_wy]
         self.h_a_out = torch.empty(self.a_out.shape, dtype=self.a_out.dtype).pin_memory()
         self.h_err = torch.empty(self.err.shape, dtype=self.err.dtype).pin_memory()
-        self.h_small = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (self.slot_map, self.new_len)]
+        self.h_small = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                        for t in (self.slot_map, self.new_len, self.next_tok, self.a_next_tok)]
         h2d = sum(t.numel() * t.element_size() for x in self.h_in for t in x.values())
         h2d += sum(t.numel() * t.element_size() for t in self.h_attn.values())
-        h2d += sum(t.numel() * t.element_size() for t in (self.h_parents, self.h_path, self.h_path_len))
+        h2d += self.h_parents.numel() * 4 + sum(t.numel() * 4 for x in self.h_tokens for t in x.values())
         d2h = sum(t.numel() * t.element_size() for t in self.h_o_fork + self.h_o_wy)
         d2h += self.h_a_out.numel() * 2 + self.h_err.numel() * 4 + sum(t.numel() * 4 for t in self.h_small)
         return h2d, d2h
@@ -315,8 +334,9 @@ class Round:
         for k in self.in_attn:
             self.in_attn[k].copy_(self.h_attn[k], non_blocking=True)
         self.parents.copy_(self.h_parents, non_blocking=True)
-        self.path.copy_(self.h_path, non_blocking=True)
-        self.path_len.copy_(self.h_path_len, non_blocking=True)
+        for dst, src in zip((self.tokens, self.a_tokens), self.h_tokens):
+            for k in dst:
+                dst[k].copy_(src[k], non_blocking=True)
         self.step()
         for h, d in zip(self.h_o_fork, self.o_fork):
             h.copy_(d, non_blocking=True)
@@ -324,8 +344,8 @@ class Round:
             h.copy_(d, non_blocking=True)
         self.h_a_out.copy_(self.a_out, non_blocking=True)
         self.h_err.copy_(self.err, non_blocking=True)
-        self.h_small[0].copy_(self.slot_map, non_blocking=True)
-        self.h_small[1].copy_(self.new_len, non_blocking=True)
+        for h, d in zip(self.h_small, (self.slot_map, self.new_len, self.next_tok, self.a_next_tok)):
+            h.copy_(d, non_blocking=True)
 
 
 class OraclePool:
@@ -478,6 +498,8 @@ def run_ours(args) -> None:
         "wy_commit": gdn_bytes(B, N, H, dk, dv, 2, 2, "commit_wy", L_sum),
         "tree_attn": attn_bytes(plens, rnd.aN, rnd.Hq, rnd.Hkv, rnd.hd),
         "kv_compact": compact_bytes([int(x) for x in a.path_len], rnd.Hkv, rnd.hd),
+        # per call, the two calls averaged: parents, draft and target tokens in; path, length, next out
+        "accept_walk": ((B + rnd.aB) * N * 12 + (B + rnd.aB) * (a.path.shape[1] + 2) * 4) // 2,
     }
     a_flops = attn_flops(plens, [_depths(t) for t in a.trees], rnd.Hq, rnd.hd)
     rows = {}

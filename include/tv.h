@@ -276,6 +276,28 @@ TV_API int tv_kv_compact(void* k_cache, void* v_cache, int num_blocks, const int
                   int Hkv, int hd, int block_size, int32_t* slot_map, int32_t* new_len,
                   int32_t* err, tv_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * tv_accept_walk -- greedy acceptance of B draft trees, on the device.
+ *
+ * Source: handbook chapter 树形草稿与 EAGLE, §实现, tree_speculative_generate: from node 0,
+ * while the target model's token at the current node equals the draft token of one of its
+ * children, step to the lowest-numbered such child; the target's token at the last accepted
+ * node is the next token.  The walk also stops once Lmax nodes are accepted.  Its output feeds
+ * tv_gdn_commit and tv_kv_compact without a host round trip.
+ *
+ *   parents        [B, N] int32   in
+ *   draft_tokens   [B, N] int32   in  token proposed at each node
+ *   target_tokens  [B, N] int32   in  token the target model chose at each node (its argmax)
+ *   accepted_path  [B, Lmax] int32 out path[0] = 0, path[r] a child of path[r-1]; -1 past the
+ *                                      length
+ *   accepted_len   [B] int32      out 1 <= len <= Lmax (0 on error)
+ *   next_token     [B] int32      out target_tokens[b][path[len-1]] (-1 on error)
+ *   err            [B] int32      out 0 or TV_ERR_BAD_TREE
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_accept_walk(const int32_t* parents, const int32_t* draft_tokens, const int32_t* target_tokens,
+                          int B, int N, int Lmax, int32_t* accepted_path, int32_t* accepted_len,
+                          int32_t* next_token, int32_t* err, tv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

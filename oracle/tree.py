@@ -12,7 +12,7 @@ Sources
   needs every parent first; its breadth-first draft builder produces such numbering).
 * Accepted path: the chapter's accept walk starts at a root and steps from parent to child
   (§实现, ``tree_speculative_generate``); the qwen35-tree-spec post restores the state of the
-  last accepted token (§五, 用途 2).
+  last accepted token (§五, 用途 2).  ``accept_walk`` is that walk on given target tokens.
 """
 from __future__ import annotations
 
@@ -88,3 +88,28 @@ def is_valid_path(parents, path, length: int) -> bool:
         if int(parents[node]) != want:
             return False
     return True
+
+
+def accept_walk(parents, draft_tokens, target_tokens, lmax: int):
+    """Greedy acceptance of one draft tree (handbook chapter 树形草稿与 EAGLE, §实现,
+    ``tree_speculative_generate``): start at node 0; while the target's token at the current
+    node equals the draft token of one of its children, step to the lowest-numbered such child.
+    Stops when no child matches or the path holds ``lmax`` nodes.
+
+    ``target_tokens[i]`` is the target model's chosen token at node i (its argmax).  Returns
+    (path as a list of nodes, next token = the target's token at the last accepted node).
+    """
+    path = [0]
+    node = 0
+    while len(path) < lmax:
+        want = int(target_tokens[node])
+        nxt = None
+        for c in range(len(parents)):          # lowest index first
+            if int(parents[c]) == node and int(draft_tokens[c]) == want:
+                nxt = c
+                break
+        if nxt is None:
+            break
+        path.append(nxt)
+        node = nxt
+    return path, int(target_tokens[node])

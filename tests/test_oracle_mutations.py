@@ -180,3 +180,48 @@ def _compact_descending_in_place(k_cache, v_cache, block_table, prefix_len, pare
 def test_compaction_mutant_is_caught(monkeypatch):
     monkeypatch.setattr(A, "kv_compact", _compact_descending_in_place)
     assert _run_pins(_ATTN_PINS) >= 1
+
+
+# ----------------------------------------------------------------------------- accept walk
+import test_oracle_tree as PT  # noqa: E402
+
+_WALK_PINS = [f for n, f in vars(PT).items() if n.startswith("test_accept_walk")]
+_WALK = T.accept_walk  # the unmutated walk, for mutants that alter only its result
+
+
+def _walk_highest_child(parents, draft_tokens, target_tokens, lmax):
+    path, node = [0], 0
+    while len(path) < lmax:
+        cs = [c for c in range(len(parents)) if parents[c] == node and draft_tokens[c] == target_tokens[node]]
+        if not cs:
+            break
+        node = cs[-1]
+        path.append(node)
+    return path, int(target_tokens[node])
+
+
+def _walk_target_at_child(parents, draft_tokens, target_tokens, lmax):
+    path, node = [0], 0
+    while len(path) < lmax:
+        cs = [c for c in range(len(parents)) if parents[c] == node and draft_tokens[c] == target_tokens[c]]
+        if not cs:
+            break
+        node = cs[0]
+        path.append(node)
+    return path, int(target_tokens[node])
+
+
+def _walk_next_token_at_root(parents, draft_tokens, target_tokens, lmax):
+    path, _ = _WALK(parents, draft_tokens, target_tokens, lmax)
+    return path, int(target_tokens[0])
+
+
+def _walk_ignores_lmax(parents, draft_tokens, target_tokens, lmax):
+    return _WALK(parents, draft_tokens, target_tokens, 10 ** 6)
+
+
+@pytest.mark.parametrize("mutant", [_walk_highest_child, _walk_target_at_child, _walk_next_token_at_root,
+                                    _walk_ignores_lmax])
+def test_accept_walk_mutants_are_caught(monkeypatch, mutant):
+    monkeypatch.setattr(T, "accept_walk", mutant)
+    assert _run_pins(_WALK_PINS) >= 1

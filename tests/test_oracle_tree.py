@@ -115,3 +115,49 @@ def test_accepted_path_generator_gives_valid_paths():
     for _ in range(50):
         p = W.random_accepted_path(t, rng, 4)
         assert 1 <= len(p) <= 4 and T.is_valid_path(t, p, len(p))
+
+
+# ----------------------------------------------------------------------------- accept walk
+def test_accept_walk_hand_example():
+    # 6-node tree of the handbook's printed example; tokens chosen so that the target at the
+    # root predicts node 2's token, at node 2 predicts node 5's token, at node 5 nothing.
+    parents = [-1, 0, 0, 1, 1, 2]
+    draft = [9, 5, 6, 7, 8, 7]
+    target = [6, 0, 7, 0, 0, 1]
+    path, nxt = T.accept_walk(parents, draft, target, 8)
+    assert path == [0, 2, 5] and nxt == 1
+
+
+def test_accept_walk_chain_and_no_match():
+    chain = [-1, 0, 1, 2, 3]
+    draft = [10, 11, 12, 13, 14]
+    assert T.accept_walk(chain, draft, [11, 12, 13, 14, 99], 8) == ([0, 1, 2, 3, 4], 99)
+    assert T.accept_walk(chain, draft, [50, 12, 13, 14, 99], 8) == ([0], 50)   # nothing at the root
+    assert T.accept_walk(chain, draft, [11, 12, 13, 14, 99], 3) == ([0, 1, 2], 13)  # stops at lmax
+    assert T.accept_walk([-1], [3], [4], 1) == ([0], 4)
+
+
+def test_accept_walk_prefers_lowest_numbered_matching_child():
+    parents = [-1, 0, 0, 0, 2, 3]
+    draft = [0, 7, 5, 5, 1, 2]     # nodes 2 and 3 both carry token 5
+    target = [5, 0, 9, 2, 0, 0]    # the root predicts 5: node 2 wins over node 3
+    assert T.accept_walk(parents, draft, target, 8) == ([0, 2], 9)
+
+
+def test_accept_walk_properties_on_random_trees():
+    rng = np.random.default_rng(5)
+    for trial in range(60):
+        n = int(rng.integers(1, 80))
+        parents = W.random_tree(n, rng)
+        draft = rng.integers(0, 4, size=n)     # small vocabulary: ties among siblings happen
+        target = rng.integers(0, 4, size=n)
+        lmax = int(rng.integers(1, 10))
+        path, nxt = T.accept_walk(parents, draft, target, lmax)
+        assert T.is_valid_path(parents, path, len(path)) and path[0] == 0 and len(path) <= lmax
+        for a, b in zip(path, path[1:]):
+            assert draft[b] == target[a]
+            assert b == min(c for c in range(n) if parents[c] == a and draft[c] == target[a])
+        last = path[-1]
+        no_match = not any(parents[c] == last and draft[c] == target[last] for c in range(n))
+        assert len(path) == lmax or no_match
+        assert nxt == target[last]

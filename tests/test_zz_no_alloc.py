@@ -3,6 +3,8 @@
 Its results must equal tv_tree_attn's (same kernels, same split plan) bit for bit.  The
 module runs last (file name) and also on its own: it builds everything it uses.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -94,12 +96,18 @@ def test_repeat_call_gives_same_result_and_allocates_nothing():
             d["prefix_len"], d["parents"], out, err)
     tv.tv_tree_attn_static(*args, rope_theta=case.rope_theta)
     torch.cuda.synchronize()
-    free_before, _ = torch.cuda.mem_get_info()
-    alloc_before = torch.cuda.memory_allocated()
-    tv.tv_tree_attn_static(*args, rope_theta=case.rope_theta)
-    torch.cuda.synchronize()
-    free_after, _ = torch.cuda.mem_get_info()
+    gc.collect()  # tensors of earlier tests must not be freed inside the measured call
+    gc.disable()
+    try:
+        free_before, _ = torch.cuda.mem_get_info()
+        alloc_before = torch.cuda.memory_allocated()
+        tv.tv_tree_attn_static(*args, rope_theta=case.rope_theta)
+        torch.cuda.synchronize()
+        free_after, _ = torch.cuda.mem_get_info()
+        alloc_after = torch.cuda.memory_allocated()
+    finally:
+        gc.enable()
     assert free_after == free_before
-    assert torch.cuda.memory_allocated() == alloc_before
+    assert alloc_after == alloc_before
     assert (err.cpu() == 0).all()
     assert torch.equal(out.cpu().view(torch.int16), first[0].view(torch.int16))

@@ -40,7 +40,8 @@ TV_STATIC_SCRATCH_BYTES = 64 << 20
 
 EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_prepare",
             "tv_gdn_tree_verify_fork", "tv_gdn_tree_verify_wy", "tv_gdn_commit",
-            "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact")
+            "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact",
+            "tv_accept_walk")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -60,6 +61,7 @@ _SIGNATURES = {
                           _P, _P]),
     "tv_tree_attn_static": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _P,
                                  _P, _P]),
+    "tv_accept_walk": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
 }
 
@@ -198,3 +200,13 @@ def tv_kv_compact(k_cache, v_cache, block_table, prefix_len, parents, accepted_p
         _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table), max_blocks, _ptr(prefix_len),
         _ptr(parents), N, _ptr(accepted_path), _ptr(accepted_len), Lmax, B, Hkv, hd, bs, _ptr(slot_map),
         _ptr(new_len), _ptr(err), _stream(stream)), "tv_kv_compact")
+
+
+def tv_accept_walk(parents, draft_tokens, target_tokens, accepted_path, accepted_len, next_token, err,
+                   stream=None) -> None:
+    """parents, draft_tokens, target_tokens [B,N] int32 -> accepted_path [B,Lmax], accepted_len [B],
+    next_token [B], err [B] (all int32)."""
+    B, N = parents.shape
+    _check(lib.tv_accept_walk(_ptr(parents), _ptr(draft_tokens), _ptr(target_tokens), B, N, accepted_path.shape[1],
+                              _ptr(accepted_path), _ptr(accepted_len), _ptr(next_token), _ptr(err), _stream(stream)),
+           "tv_accept_walk")

@@ -178,4 +178,16 @@ int tv_kv_compact(void* k_cache, void* v_cache, int num_blocks, const int32_t* b
   return cuda_status(tv::launch_kv_compact(a, stream));
 }
 
+int tv_accept_walk(const int32_t* parents, const int32_t* draft_tokens, const int32_t* target_tokens, int B,
+                   int N, int Lmax, int32_t* accepted_path, int32_t* accepted_len, int32_t* next_token,
+                   int32_t* err, tv_stream_t stream) {
+  if (!a4(parents) || !a4(draft_tokens) || !a4(target_tokens) || !a4(accepted_path) || !a4(accepted_len) ||
+      !a4(next_token) || !a4(err))
+    return TV_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || Lmax < 1) return TV_ERR_INVALID_ARG;
+  if (N > TV_MAX_NODES) return TV_ERR_UNSUPPORTED;
+  tv::AcceptArgs a{parents, draft_tokens, target_tokens, B, N, Lmax, accepted_path, accepted_len, next_token, err};
+  return cuda_status(tv::launch_accept_walk(a, stream));
+}
+
 }  // extern "C"

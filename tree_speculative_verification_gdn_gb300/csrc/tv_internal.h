@@ -100,4 +100,16 @@ struct CompactArgs {
 };
 cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t s);
 
+struct AcceptArgs {
+  const int32_t* parents;
+  const int32_t* draft;
+  const int32_t* target;
+  int B, N, Lmax;
+  int32_t* path;
+  int32_t* len;
+  int32_t* next_token;
+  int32_t* err;
+};
+cudaError_t launch_accept_walk(const AcceptArgs& a, cudaStream_t s);
+
 }  // namespace tv

@@ -101,6 +101,32 @@ def random_accepted_path(parents: list[int], rng: np.random.Generator,
     return path[:length]
 
 
+def walk_tokens(trees: list[list[int]], paths: np.ndarray, path_len: np.ndarray, seed: int,
+                vocab: int = 151936) -> tuple[torch.Tensor, torch.Tensor]:
+    """Draft and target tokens ``[B, N]`` int32 under which the greedy accept walk takes exactly
+    the given paths: draft tokens are distinct within a tree; along the path the target token
+    of each node is the draft token of the next path node; at the path's last node it matches
+    no child; elsewhere it is random."""
+    rng = np.random.default_rng(seed)
+    B, N = len(trees), max(len(t) for t in trees)
+    draft = np.zeros((B, N), dtype=np.int32)
+    target = np.zeros((B, N), dtype=np.int32)
+    for b, parents in enumerate(trees):
+        n = len(parents)
+        draft[b, :n] = rng.choice(vocab, size=n, replace=False)
+        target[b, :n] = rng.integers(0, vocab, size=n)
+        L = int(path_len[b])
+        for r in range(L - 1):
+            target[b, paths[b, r]] = draft[b, paths[b, r + 1]]
+        last = int(paths[b, L - 1])
+        kids = {int(draft[b, c]) for c in range(n) if parents[c] == last}
+        t = int(rng.integers(0, vocab))
+        while t in kids:
+            t = int(rng.integers(0, vocab))
+        target[b, last] = t
+    return torch.from_numpy(draft), torch.from_numpy(target)
+
+
 # ----------------------------------------------------------------------------- dtypes
 def round_to(x: np.ndarray, dtype: str) -> torch.Tensor:
     """fp32 numpy -> CPU torch tensor in the storage dtype (round-to-nearest-even)."""
