@@ -408,6 +408,52 @@ def _oracle_sequence(b):
     return b
 
 
+def selective_fork_report(rnd, torch, tv, iters: int = 3) -> dict:
+    """Fork mode with selective snapshots (qwen35-tree-spec §六, 选择性 Fork) on the same 24-layer
+    stack, timed apart from the step: nodes with draft confidence above 0.95 keep no snapshot
+    (synthetic confidences, about half of the nodes above the threshold), and the commit
+    replays from the deepest kept snapshot of the accepted path."""
+    import numpy as np
+    B, N, H, dk, dv, L = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv, rnd.layers
+    rng = np.random.default_rng(99)
+    high = rng.random((B, N)) < 0.5
+    conf_np = np.where(high, rng.uniform(0.951, 1.0, (B, N)), rng.uniform(0.0, 0.95, (B, N))).astype(np.float32)
+    kept = int((conf_np <= 0.95).sum(axis=1).max())
+    conf = torch.from_numpy(conf_np).to(rnd.dev)
+    states = torch.empty((B, kept, H, dv, dk), dtype=torch.bfloat16, device=rnd.dev)
+    slot = torch.empty((B, N), dtype=torch.int32, device=rnd.dev)
+    S0 = [s.clone() for s in rnd.S0_fork]
+    out = torch.empty_like(rnd.o_fork[0])
+    err = torch.zeros((2, B), dtype=torch.int32, device=rnd.dev)
+
+    def once(ev=None):
+        for l in range(L):
+            x = rnd.in_gdn[l]
+            s, m, e = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            s.record()
+            tv.tv_gdn_tree_verify_fork_selective(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S0[l], rnd.parents,
+                                                 conf, 0.95, out, states, slot, err[0])
+            m.record()
+            tv.tv_gdn_commit_selective(rnd.path, rnd.path_len, rnd.parents, states, slot, x["k"], x["v"], x["alpha"],
+                                       x["beta"], S0[l], err[1])
+            e.record()
+            if ev is not None:
+                ev.append((s, m, e))
+    once()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(iters):
+        once(ev)
+    torch.cuda.synchronize()
+    assert int(err.abs().sum()) == 0, err
+    v_ms = sum(s.elapsed_time(m) for s, m, _ in ev) / len(ev)
+    c_ms = sum(m.elapsed_time(e) for _, m, e in ev) / len(ev)
+    full = B * N * H * dv * dk * 2
+    return {"threshold": 0.95, "kept_fraction": round(float((conf_np <= 0.95).mean()), 4),
+            "snapshot_bytes_per_layer": B * kept * H * dv * dk * 2, "full_checkpoint_bytes_per_layer": full,
+            "verify_ms_per_layer": round(v_ms, 5), "commit_ms_per_layer": round(c_ms, 5)}
+
+
 def run_ours(args) -> None:
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -485,6 +531,7 @@ def run_ours(args) -> None:
         e2e = {"value": whole_job_rate(rnd.B * rnd.N * rnd.layers * 2, world, e2e_ms), "unit": "nodes/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
+    selective = selective_fork_report(rnd, torch, tv)
     peaks = load_peaks()
     B, N, H, dk, dv = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv
     L_sum = int(rnd.gdn_host[0].path_len.sum())
@@ -530,7 +577,8 @@ def run_ours(args) -> None:
                        "l2": "working set >> 129 MB L2 (fork checkpoints 1.3 GB per layer)",
                        "parallelism": f"replicas x{world}"},
             "gpu_launches": rnd.launches_per_step * args.steps, "clocks": clk, "roofline": roof,
-            "rows": rows, "state_memory": mem, "e2e": e2e, "cpu_baseline": cpu_base}
+            "rows": rows, "state_memory": mem, "selective_fork": selective, "e2e": e2e,
+            "cpu_baseline": cpu_base}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

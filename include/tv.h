@@ -187,6 +187,41 @@ TV_API int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* 
                   int dv, int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * tv_gdn_tree_verify_fork_selective / tv_gdn_commit_selective -- fork mode with selective
+ * snapshots.
+ *
+ * Source: qwen35-tree-spec §六, 选择性 Fork: a node whose draft confidence is above a
+ * threshold (0.95 on the page) is processed without keeping a snapshot -- it is almost
+ * surely accepted, so it needs no rollback point -- which cuts the snapshot count.
+ *
+ * Verify: as tv_gdn_tree_verify_fork, except that node i keeps its snapshot only if
+ * confidence[b][i] <= threshold.  Kept snapshots are numbered 0, 1, ... in node order:
+ *   confidence   [B, N] fp32                 in
+ *   node_states  [B, capacity, H, dv, dk]    out snapshot of the node with slot s at index s
+ *   slot         [B, N] int32                out snapshot index of each node, -1 if none (all
+ *                                            -1 for a sequence that reports an error)
+ *   err          [B] int32                   out 0, TV_ERR_BAD_TREE, TV_ERR_UNSUPPORTED, or
+ *                                            TV_ERR_CAPACITY (more than capacity kept; the
+ *                                            sequence is skipped)
+ *   1 <= capacity <= N.
+ * Commit: S0[b] <- state of the last accepted node, resumed from the deepest node of the
+ * accepted path that kept a snapshot (S0[b] itself if none did) and replayed along the rest of
+ * the path with k, v, alpha, beta of the verify call.  Path rules and err as tv_gdn_commit
+ * (fork mode).
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_gdn_tree_verify_fork_selective(const void* q, const void* k, const void* v, const float* alpha,
+                                             const float* beta, const void* S0, const int32_t* parents,
+                                             const float* confidence, float threshold, int capacity, int B,
+                                             int N, int H, int dk, int dv, int io_dtype, int state_dtype,
+                                             float q_scale, void* out, void* node_states, int32_t* slot,
+                                             int32_t* err, tv_stream_t stream);
+TV_API int tv_gdn_commit_selective(const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,
+                                   const int32_t* parents, const void* node_states, const int32_t* slot,
+                                   int capacity, const void* k, const void* v, const float* alpha,
+                                   const float* beta, void* S0, int B, int N, int H, int dk, int dv,
+                                   int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * tv_tree_attn -- tree-masked GQA attention over a paged KV prefix.
  *
  * Source: handbook chapter 树形草稿与 EAGLE, §实现, forward_with_mask: q and k of the new

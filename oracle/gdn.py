@@ -21,6 +21,11 @@ Sources
   depth-by-depth schedule (§四, 逐深度处理), kept as a second, independent algorithm.
 * Commit.  After verification the state goes back to that of the last accepted node and
   the other snapshots are dropped (§五 用途 2, §七 Step 4).
+* Selective fork.  The same post (§六, 选择性 Fork) skips the snapshot of a node whose draft
+  confidence exceeds a threshold (0.95 on the page): such a node is processed but keeps no
+  rollback point.  ``selective_slots`` numbers the kept snapshots in node order; a commit
+  whose accepted node kept no snapshot resumes from the deepest kept one on its path (or
+  S_0) -- which ``commit`` already states, since it replays the path.
 * Pseudo-values.  The TreeWY abstract (TreeWY: Speculative Verification for Gated DeltaNet
   Hybrids) keeps a small pseudo-value matrix instead of per-node states and rebuilds only
   the accepted state on commit.  Its derivation is not on the page.  The reading used
@@ -136,3 +141,18 @@ def commit(inp: dict, path: np.ndarray, path_len: np.ndarray) -> np.ndarray:
             continue
         out[b] = node_state(inp, b, int(path[b][L - 1]))[0]
     return out
+
+
+def selective_slots(confidence, threshold: float, capacity: int):
+    """Snapshot slots of one tree under selective fork: node i keeps its snapshot unless its
+    confidence is above ``threshold``; kept snapshots take slots 0, 1, ... in node order.
+    Returns (slot per node, -1 where skipped; number kept; whether it fits ``capacity``)."""
+    slots, kept = [], 0
+    for c in confidence:
+        if float(c) > threshold:
+            slots.append(-1)
+        else:
+            slots.append(kept)
+            kept += 1
+    return slots, kept, kept <= capacity
+

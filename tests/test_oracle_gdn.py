@@ -205,3 +205,12 @@ def test_commit_takes_last_accepted_state_and_skips_bad_paths():
     assert np.allclose(out[0], S[0, 6], atol=1e-15)
     assert np.allclose(out[1], S[1, 0], atol=1e-15)
     assert np.array_equal(out[2], inp["S0"][2])     # 3 is not a child of 0: unchanged
+
+
+def test_selective_slots_number_kept_snapshots_in_node_order():
+    # the page's rule: confidence above the threshold -> no snapshot; at the threshold -> kept
+    slots, kept, fits = G.selective_slots([0.5, 0.99, 0.2, 0.96, 0.95, 0.951], 0.95, 3)
+    assert slots == [0, -1, 1, -1, 2, -1] and kept == 3 and fits
+    assert G.selective_slots([0.5, 0.2, 0.1], 0.95, 2)[2] is False       # 3 kept > capacity 2
+    assert G.selective_slots([0.99, 0.97], 0.95, 0) == ([-1, -1], 0, True)  # nothing kept
+    assert G.selective_slots([0.3] * 4, 1.0, 4) == ([0, 1, 2, 3], 4, True)  # threshold 1: all kept

@@ -41,7 +41,7 @@ TV_STATIC_SCRATCH_BYTES = 64 << 20
 EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_prepare",
             "tv_gdn_tree_verify_fork", "tv_gdn_tree_verify_wy", "tv_gdn_commit",
             "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact",
-            "tv_accept_walk")
+            "tv_accept_walk", "tv_gdn_tree_verify_fork_selective", "tv_gdn_commit_selective")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -61,6 +61,10 @@ _SIGNATURES = {
                           _P, _P]),
     "tv_tree_attn_static": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _P,
                                  _P, _P]),
+    "tv_gdn_tree_verify_fork_selective": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I, _I,
+                                              _F, _P, _P, _P, _P, _P]),
+    "tv_gdn_commit_selective": (_I, [_P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                    _P, _P]),
     "tv_accept_walk": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
 }
@@ -131,6 +135,30 @@ def tv_gdn_tree_verify_fork(q, k, v, alpha, beta, S0, parents, out, node_states,
         _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(parents), B, N, H, dk, dv,
         _DTYPES[q.dtype], _DTYPES[S0.dtype], float(q_scale), _ptr(out), _ptr(node_states), _ptr(err),
         _stream(stream)), "tv_gdn_tree_verify_fork")
+
+
+def tv_gdn_tree_verify_fork_selective(q, k, v, alpha, beta, S0, parents, confidence, threshold: float, out,
+                                      node_states, slot, err, q_scale: float = 1.0, stream=None) -> None:
+    """Fork mode keeping snapshots only of nodes with confidence <= threshold: node_states
+    [B, capacity, H, dv, dk] (capacity = node_states.shape[1]), slot [B, N] int32."""
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(lib.tv_gdn_tree_verify_fork_selective(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(parents), _ptr(confidence),
+        float(threshold), node_states.shape[1], B, N, H, dk, dv, _DTYPES[q.dtype], _DTYPES[S0.dtype],
+        float(q_scale), _ptr(out), _ptr(node_states), _ptr(slot), _ptr(err), _stream(stream)),
+        "tv_gdn_tree_verify_fork_selective")
+
+
+def tv_gdn_commit_selective(accepted_path, accepted_len, parents, node_states, slot, k, v, alpha, beta, S0, err,
+                            stream=None) -> None:
+    """Commit after tv_gdn_tree_verify_fork_selective (replays from the deepest kept snapshot)."""
+    B, H, dv, dk = S0.shape
+    N = parents.shape[1]
+    _check(lib.tv_gdn_commit_selective(
+        _ptr(accepted_path), _ptr(accepted_len), accepted_path.shape[1], _ptr(parents), _ptr(node_states),
+        _ptr(slot), node_states.shape[1], _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), B, N, H, dk, dv,
+        _DTYPES[k.dtype], _DTYPES[S0.dtype], _ptr(err), _stream(stream)), "tv_gdn_commit_selective")
 
 
 def tv_gdn_tree_verify_wy(q, k, v, alpha, beta, S0, parents, out, pseudo_v, log_gamma, err,

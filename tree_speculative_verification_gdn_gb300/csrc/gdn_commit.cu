@@ -180,6 +180,91 @@ __global__ void __launch_bounds__(kThreads, 3) commit_wy_kernel(CommitArgs a) {
   }
 }
 
+// Commit after a selective fork (qwen35-tree-spec §六, 选择性 Fork): one CTA per (sequence,
+// head).  The accepted path is resumed from its deepest node that kept a snapshot (S_0 if none)
+// and the rest of the path is replayed with the gated delta rule,
+//     S <- alpha_j S + w k_j^T,   w = beta_j (v_j - alpha_j S k_j),
+// thread (row rl, lane) holding rows rl, rl + 32, ... in the interleaved 8-column chunks.
+template <typename TIO, typename TS, int DK>
+__global__ void __launch_bounds__(kThreads) commit_replay_kernel(CommitArgs a, ReplayArgs rp) {
+  constexpr int CPL = DK / kLPR;
+  __shared__ PathCheck pc;
+  __shared__ int start_r;      // path index of the snapshot resumed from (-1: S_0)
+  __shared__ int start_slot;
+  __shared__ float al_s[TV_MAX_NODES], be_s[TV_MAX_NODES];
+  extern __shared__ __align__(16) float ksm[];  // keys of the replayed nodes, [steps][DK]
+  const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int N = a.N, H = a.H, dv = a.dv;
+  const int st = check_path(a, b, pc);
+  if (h == 0 && threadIdx.x == 0) a.err[b] = st;
+  if (st) return;
+  const int L = pc.L;
+  if (threadIdx.x == 0) {
+    int r0 = -1, sl = -1;
+    for (int r = L - 1; r >= 0; --r) {
+      const int s = rp.slot[(size_t)b * N + pc.path[r]];
+      if (s >= 0 && s < rp.capacity) { r0 = r; sl = s; break; }
+    }
+    start_r = r0;
+    start_slot = sl;
+  }
+  __syncthreads();
+  const int r0 = start_r, steps = L - 1 - r0;
+  for (int x = threadIdx.x; x < steps; x += kThreads) {
+    const size_t nh = ((size_t)b * N + pc.path[r0 + 1 + x]) * H + h;
+    al_s[x] = rp.alpha[nh];
+    be_s[x] = rp.beta[nh];
+  }
+  for (int x = threadIdx.x; x < steps * DK; x += kThreads) {
+    const int t = x / DK, c = x % DK;
+    ksm[x] = to_f32(static_cast<const TIO*>(a.k)[(((size_t)b * N + pc.path[r0 + 1 + t]) * H + h) * DK + c]);
+  }
+  __syncthreads();
+  const int lane8 = threadIdx.x % kLPR, rl = threadIdx.x / kLPR;
+  const TS* src = r0 < 0 ? static_cast<const TS*>(a.S0) + ((size_t)b * H + h) * dv * DK
+                         : static_cast<const TS*>(a.node_states) + (((size_t)b * rp.capacity + start_slot) * H + h) * dv * DK;
+  TS* dst = static_cast<TS*>(a.S0) + ((size_t)b * H + h) * dv * DK;
+  const TIO* v = static_cast<const TIO*>(rp.v);
+  for (int p = 0; p < dv / kRows; ++p) {  // the same trip count in every thread
+    const int row = p * kRows + rl;
+    float cur[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) load_vec_rw<8>(src + (size_t)row * DK + lane8 * 8 + j * kStride, cur + 8 * j);
+    for (int t = 0; t < steps; ++t) {
+      const float* kt = ksm + t * DK + lane8 * 8;
+      float pk = 0.f;
+#pragma unroll
+      for (int j = 0; j < CPL / 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) pk = fmaf(cur[8 * j + e], kt[j * kStride + e], pk);
+      pk = group_sum<kLPR>(pk);
+      const float al = al_s[t];
+      const size_t nh = ((size_t)b * N + pc.path[r0 + 1 + t]) * H + h;
+      const float w = be_s[t] * (to_f32(v[nh * dv + row]) - al * pk);
+#pragma unroll
+      for (int j = 0; j < CPL / 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cur[8 * j + e] = fmaf(w, kt[j * kStride + e], al * cur[8 * j + e]);
+    }
+    __syncthreads();  // every thread has read its source rows before any S_0 row is written
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) store_vec<8>(dst + (size_t)row * DK + lane8 * 8 + j * kStride, cur + 8 * j);
+  }
+}
+
+template <typename TIO, typename TS, int DK>
+cudaError_t launch_replay_t(const CommitArgs& a, const ReplayArgs& r, cudaStream_t s) {
+  const int cap = a.Lmax < a.N ? a.Lmax : a.N;
+  const size_t smem = (size_t)cap * DK * sizeof(float);
+  auto kern = commit_replay_kernel<TIO, TS, DK>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<a.B * a.H, kThreads, smem, s>>>(a, r);
+  return cudaGetLastError();
+}
+
 template <typename TIO, typename TS, int DK>
 cudaError_t launch_wy_t(const CommitArgs& a, cudaStream_t s) {
   const int cap = a.Lmax < a.N ? a.Lmax : a.N;  // a valid path has distinct nodes
@@ -194,6 +279,14 @@ cudaError_t launch_wy_t(const CommitArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_gdn_commit_replay(const CommitArgs& a, const ReplayArgs& r, cudaStream_t s) {
+  if (a.io == TV_F32 && a.state == TV_F32)
+    return a.dk == 64 ? launch_replay_t<float, float, 64>(a, r, s) : launch_replay_t<float, float, 128>(a, r, s);
+  if (a.io == TV_BF16 && a.state == TV_BF16)
+    return a.dk == 64 ? launch_replay_t<bf16, bf16, 64>(a, r, s) : launch_replay_t<bf16, bf16, 128>(a, r, s);
+  return a.dk == 64 ? launch_replay_t<bf16, float, 64>(a, r, s) : launch_replay_t<bf16, float, 128>(a, r, s);
+}
 
 cudaError_t launch_gdn_commit(const CommitArgs& a, cudaStream_t s) {
   if (a.mode == TV_MODE_FORK) {

@@ -44,7 +44,8 @@ struct Sched {
   int order[TV_MAX_NODES];   // node at each depth-first position
   int src[TV_MAX_NODES];     // where the parent state comes from: -1 registers, 0 S_0, else a slot
   int push[TV_MAX_NODES];    // slot the node's own state goes to (-1: not needed later)
-  // per depth-first position t: {node, (src + 1) | (push + 1) << 8, alpha bits, beta bits}
+  // per depth-first position t: {node, (src + 1) | (push + 1) << 8 | (snapshot slot + 1) << 16,
+  // alpha bits, beta bits}
   int4 ent[TV_MAX_NODES];
   float kq[TV_MAX_NODES];    // per depth-first position: k_i . q_i of the current item's head
   int flag, maxslot, pad0, pad1;
@@ -59,7 +60,8 @@ struct BuildScratch {
   int acc[TV_MAX_NODES];     // running offset of light children
   int before[TV_MAX_NODES];  // nodes of earlier siblings' subtrees
   int pre[TV_MAX_NODES];     // depth-first position
-  int maxdepth, root_acc;
+  int slot[TV_MAX_NODES];    // snapshot slot of each node (selective fork), -1: none
+  int maxdepth, root_acc, kept;
 };
 
 // Depth-first schedule of one tree, built by the whole CTA.  Returns 0, TV_ERR_BAD_TREE or
@@ -176,7 +178,7 @@ struct Raw<float, CPL> {
 
 template <typename TIO, typename TS, int DK>
 __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __restrict__ states,
-                                                            int ctas_per_seq, int nslots) {
+                                                            int ctas_per_seq, int nslots, ForkSelect sel) {
   constexpr int CPL = DK / kLPR;  // columns per lane
   constexpr int Q4 = CPL / 4;     // float4 per lane per slot
   extern __shared__ __align__(128) unsigned char smem[];
@@ -189,6 +191,29 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
   const int tid = threadIdx.x;
   int status = build_schedule(a.parents + (size_t)b * N, N, sc, scratch);
   if (!status && sc.maxslot > nslots) status = TV_ERR_UNSUPPORTED;
+  // Snapshot slots (selective fork): nodes at or below the confidence threshold, numbered in
+  // node order by one warp's ballot scan; otherwise slot = node.
+  if (sel.confidence != nullptr) {
+    if (tid < 32) {
+      int carry = 0;
+      for (int base = 0; base < N; base += 32) {
+        const int i = base + tid;
+        const bool keep = i < N && sel.confidence[(size_t)b * N + i] <= sel.threshold;
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        if (i < N) scratch.slot[i] = keep ? carry + __popc(m & ((1u << tid) - 1u)) : -1;
+        carry += __popc(m);
+      }
+      if (tid == 0) scratch.kept = carry;
+    }
+    __syncthreads();
+    if (!status && scratch.kept > sel.capacity) status = TV_ERR_CAPACITY;
+    // a sequence that is skipped keeps no snapshot: its commit then replays from S_0
+    if (g == 0 && sel.slot != nullptr)
+      for (int i = tid; i < N; i += kThreads) sel.slot[(size_t)b * N + i] = status ? -1 : scratch.slot[i];
+  } else {
+    for (int i = tid; i < N; i += kThreads) scratch.slot[i] = i;
+    __syncthreads();
+  }
   if (g == 0 && tid == 0) a.err[b] = status;
   if (status) return;
 
@@ -206,7 +231,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
 
   for (int t = tid; t < N; t += kThreads) {
     const int i = sc.order[t];
-    sc.ent[t] = make_int4(i, (sc.src[i] + 1) | ((sc.push[i] + 1) << 8), 0, 0);
+    sc.ent[t] = make_int4(i, (sc.src[i] + 1) | ((sc.push[i] + 1) << 8) | ((scratch.slot[i] + 1) << 16), 0, 0);
   }
   // Pulls one item's inputs into L2 ahead of use: alpha, beta, k and q of every node, the
   // slab's v rows and S_0 rows.  The node loop's register prefetch then waits on L2, not HBM.
@@ -264,7 +289,8 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     const TIO* vb = v + nh0 * dv + r;
     const TS* s0row = S0 + (((size_t)b * H + h) * dv + r) * DK + lane * 8;
     TIO* out_r = out + nh0 * dv + r;
-    TS* st_r = states + (nh0 * dv + r) * DK + lane * 8;
+    // snapshots of this sequence: [capacity][H][dv][dk]
+    TS* st_r = states + ((((size_t)b * sel.capacity) * H + h) * dv + r) * DK + lane * 8;
     auto fetch = [&](int t, Raw<TIO, CPL>& x) {
       x.e = sc.ent[t < N ? t : N - 1];
       x.kq = sc.kq[t < N ? t : N - 1];
@@ -279,7 +305,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     // with k.q from the per-item table.  Column pairs go through the paired fp32 FMA.
     auto body = [&](const Raw<TIO, CPL>& x) {
       const int i = x.e.x;
-      const int src = (x.e.y & 255) - 1, push = (x.e.y >> 8) - 1;
+      const int src = (x.e.y & 255) - 1, push = ((x.e.y >> 8) & 255) - 1, slot = (x.e.y >> 16) - 1;
       const float al = __int_as_float(x.e.z), be = __int_as_float(x.e.w);
       if (src == 0) {
         float f[CPL];
@@ -324,8 +350,10 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
         float f[CPL];
 #pragma unroll
         for (int e = 0; e < CPL / 2; ++e) { f[2 * e] = cur[e].x; f[2 * e + 1] = cur[e].y; }
+        if (slot >= 0) {
 #pragma unroll
-        for (int j = 0; j < CPL / 8; ++j) store_vec_cs<8>(st_r + (size_t)i * state_stride + j * kStride, f + 8 * j);
+          for (int j = 0; j < CPL / 8; ++j) store_vec_cs<8>(st_r + (size_t)slot * state_stride + j * kStride, f + 8 * j);
+        }
       }
       if (push > 0) {
 #pragma unroll
@@ -349,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
 }
 
 template <typename TIO, typename TS, int DK>
-cudaError_t launch_fork_t(const GdnArgs& a, void* states, cudaStream_t s) {
+cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel, cudaStream_t s) {
   auto kern = gdn_fork_kernel<TIO, TS, DK>;
   const int nslots = slots_for(a.N);
   size_t stack = (size_t)nslots * (DK / kLPR / 4) * kThreads * sizeof(float4);
@@ -365,22 +393,22 @@ cudaError_t launch_fork_t(const GdnArgs& a, void* states, cudaStream_t s) {
   int per_seq = slots / a.B;
   if (per_seq < 1) per_seq = 1;
   if (per_seq > items) per_seq = items;
-  kern<<<a.B * per_seq, kThreads, smem, s>>>(a, static_cast<TS*>(states), per_seq, nslots);
+  kern<<<a.B * per_seq, kThreads, smem, s>>>(a, static_cast<TS*>(states), per_seq, nslots, sel);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, cudaStream_t s) {
+cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, const ForkSelect& sel, cudaStream_t s) {
   static_assert(sizeof(Sched) % 16 == 0, "stack must start 16-byte aligned");
   if (a.io == TV_F32 && a.state == TV_F32)
-    return a.dk == 64 ? launch_fork_t<float, float, 64>(a, node_states, s)
-                      : launch_fork_t<float, float, 128>(a, node_states, s);
+    return a.dk == 64 ? launch_fork_t<float, float, 64>(a, node_states, sel, s)
+                      : launch_fork_t<float, float, 128>(a, node_states, sel, s);
   if (a.io == TV_BF16 && a.state == TV_BF16)
-    return a.dk == 64 ? launch_fork_t<bf16, bf16, 64>(a, node_states, s)
-                      : launch_fork_t<bf16, bf16, 128>(a, node_states, s);
-  return a.dk == 64 ? launch_fork_t<bf16, float, 64>(a, node_states, s)
-                    : launch_fork_t<bf16, float, 128>(a, node_states, s);
+    return a.dk == 64 ? launch_fork_t<bf16, bf16, 64>(a, node_states, sel, s)
+                      : launch_fork_t<bf16, bf16, 128>(a, node_states, sel, s);
+  return a.dk == 64 ? launch_fork_t<bf16, float, 64>(a, node_states, sel, s)
+                    : launch_fork_t<bf16, float, 128>(a, node_states, sel, s);
 }
 
 }  // namespace tv

@@ -101,7 +101,25 @@ int tv_gdn_tree_verify_fork(const void* q, const void* k, const void* v, const f
   if (st != TV_OK) return st;
   if (!a16(node_states)) return TV_ERR_INVALID_ARG;
   tv::GdnArgs a{q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale, out, err};
-  return cuda_status(tv::launch_gdn_fork(a, node_states, stream));
+  const tv::ForkSelect all{nullptr, 0.f, N, nullptr};
+  return cuda_status(tv::launch_gdn_fork(a, node_states, all, stream));
+}
+
+int tv_gdn_tree_verify_fork_selective(const void* q, const void* k, const void* v, const float* alpha,
+                                      const float* beta, const void* S0, const int32_t* parents,
+                                      const float* confidence, float threshold, int capacity, int B, int N,
+                                      int H, int dk, int dv, int io_dtype, int state_dtype, float q_scale,
+                                      void* out, void* node_states, int32_t* slot, int32_t* err,
+                                      tv_stream_t stream) {
+  int st = gdn_common(q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale,
+                      out, err);
+  if (st != TV_OK) return st;
+  if (!a4(confidence) || !a4(slot) || !isfinite(threshold) || capacity < 1 || capacity > N)
+    return TV_ERR_INVALID_ARG;
+  if (!a16(node_states)) return TV_ERR_INVALID_ARG;
+  tv::GdnArgs a{q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale, out, err};
+  const tv::ForkSelect sel{confidence, threshold, capacity, slot};
+  return cuda_status(tv::launch_gdn_fork(a, node_states, sel, stream));
 }
 
 int tv_gdn_tree_verify_wy(const void* q, const void* k, const void* v, const float* alpha,
@@ -135,6 +153,24 @@ int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* accepte
   tv::CommitArgs a{mode, accepted_path, accepted_len, Lmax, parents, node_states, pseudo_v, log_gamma, k,
                    S0, B, N, H, dk, dv, io_dtype, state_dtype, err};
   return cuda_status(tv::launch_gdn_commit(a, stream));
+}
+
+int tv_gdn_commit_selective(const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,
+                            const int32_t* parents, const void* node_states, const int32_t* slot, int capacity,
+                            const void* k, const void* v, const float* alpha, const float* beta, void* S0, int B,
+                            int N, int H, int dk, int dv, int io_dtype, int state_dtype, int32_t* err,
+                            tv_stream_t stream) {
+  if (!a4(accepted_path) || !a4(accepted_len) || !a4(parents) || !a16(S0) || !a4(err) || !a16(node_states) ||
+      !a4(slot) || !a16(k) || !a4(v) || !a4(alpha) || !a4(beta))
+    return TV_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || H < 1 || Lmax < 1 || capacity < 1 || capacity > N) return TV_ERR_INVALID_ARG;
+  if (N > TV_MAX_NODES || !dim_ok(dk) || !dim_ok(dv)) return TV_ERR_UNSUPPORTED;
+  int st = gdn_dtypes(io_dtype, state_dtype);
+  if (st != TV_OK) return st;
+  tv::CommitArgs a{TV_MODE_FORK, accepted_path, accepted_len, Lmax, parents, node_states, nullptr, nullptr, k,
+                   S0, B, N, H, dk, dv, io_dtype, state_dtype, err};
+  const tv::ReplayArgs r{slot, capacity, v, alpha, beta};
+  return cuda_status(tv::launch_gdn_commit_replay(a, r, stream));
 }
 
 size_t tv_tree_attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int block_size) {

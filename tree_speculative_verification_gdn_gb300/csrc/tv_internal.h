@@ -32,7 +32,16 @@ struct GdnArgs {
 cudaError_t launch_tree_prepare(const int32_t* parents, int B, int N, int32_t* depth,
                                 uint32_t* mask_bits, int32_t* err, cudaStream_t s);
 
-cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, cudaStream_t s);
+// Selective fork: a node keeps its snapshot only if its confidence is at most the threshold;
+// kept snapshots take slots 0, 1, ... in node order.  confidence == nullptr: every node keeps
+// its snapshot, at slot = node, and capacity = N.
+struct ForkSelect {
+  const float* confidence;  // [B, N] or nullptr
+  float threshold;
+  int capacity;             // snapshot slots per sequence in node_states [B, capacity, H, dv, dk]
+  int32_t* slot;            // [B, N] out (slot or -1), or nullptr
+};
+cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, const ForkSelect& sel, cudaStream_t s);
 
 // TreeWY verify: tcgen05 kernel for bf16 I/O and state with dk = dv = 128, CUDA-core kernel
 // for every other supported shape.
@@ -56,6 +65,16 @@ struct CommitArgs {
   int32_t* err;
 };
 cudaError_t launch_gdn_commit(const CommitArgs& a, cudaStream_t s);
+// Commit after a selective fork: resume from the deepest accepted node that kept a snapshot
+// (or S_0) and replay the rest of the path with its inputs.
+struct ReplayArgs {
+  const int32_t* slot;  // [B, N] from the selective fork
+  int capacity;
+  const void* v;
+  const float* alpha;
+  const float* beta;
+};
+cudaError_t launch_gdn_commit_replay(const CommitArgs& a, const ReplayArgs& r, cudaStream_t s);
 
 struct AttnArgs {
   const void* q;
