@@ -454,6 +454,39 @@ def selective_fork_report(rnd, torch, tv, iters: int = 3) -> dict:
             "verify_ms_per_layer": round(v_ms, 5), "commit_ms_per_layer": round(c_ms, 5)}
 
 
+def lazy_commit_report(rnd, torch, tv, iters: int = 3) -> dict:
+    """TreeWY with the previous round's commit fused into this round's verify, on the same
+    24-layer stack, timed apart from the step: each layer's last W, log(gamma), keys and the
+    accepted paths stand for the previous round."""
+    B, N, H, dv, L = rnd.B, rnd.N, rnd.H, rnd.dv, rnd.layers
+    S0 = [s.clone() for s in rnd.S0_wy]
+    out = torch.empty_like(rnd.o_wy[0])
+    pv = [torch.empty_like(p) for p in rnd.pv]
+    lg = [torch.empty_like(g) for g in rnd.lg]
+    err = torch.zeros((B,), dtype=torch.int32, device=rnd.dev)
+
+    def once(ev=None):
+        for l in range(L):
+            x = rnd.in_gdn[l]
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            tv.tv_gdn_tree_verify_wy_lazy(rnd.path, rnd.path_len, rnd.parents, rnd.pv[l], rnd.lg[l], x["k"], x["q"],
+                                          x["k"], x["v"], x["alpha"], x["beta"], S0[l], rnd.parents, out, pv[l], lg[l],
+                                          err)
+            e.record()
+            if ev is not None:
+                ev.append((s, e))
+    once()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(iters):
+        once(ev)
+    torch.cuda.synchronize()
+    assert int(err.abs().sum()) == 0, err
+    return {"fused_ms_per_layer": round(sum(s.elapsed_time(e) for s, e in ev) / len(ev), 5),
+            "bytes_saved_per_layer": B * H * dv * dv * 2}
+
+
 def run_ours(args) -> None:
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -532,6 +565,7 @@ def run_ours(args) -> None:
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     selective = selective_fork_report(rnd, torch, tv)
+    lazy = lazy_commit_report(rnd, torch, tv)
     peaks = load_peaks()
     B, N, H, dk, dv = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv
     L_sum = int(rnd.gdn_host[0].path_len.sum())
@@ -577,7 +611,7 @@ def run_ours(args) -> None:
                        "l2": "working set >> 129 MB L2 (fork checkpoints 1.3 GB per layer)",
                        "parallelism": f"replicas x{world}"},
             "gpu_launches": rnd.launches_per_step * args.steps, "clocks": clk, "roofline": roof,
-            "rows": rows, "state_memory": mem, "selective_fork": selective, "e2e": e2e,
+            "rows": rows, "state_memory": mem, "selective_fork": selective, "lazy_commit": lazy, "e2e": e2e,
             "cpu_baseline": cpu_base}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -161,6 +161,38 @@ TV_API int tv_gdn_tree_verify_wy(const void* q, const void* k, const void* v, co
                           int32_t* err, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * tv_gdn_tree_verify_wy_lazy -- TreeWY verify with the previous round's commit fused in.
+ *
+ * Source: TreeWY abstract (only the accepted state is rebuilt on commit).  The previous
+ * round's WY commit (see tv_gdn_commit, TV_MODE_WY) is applied to S0 while it is staged for
+ * this round's contraction, saving that commit's separate pass over the state:
+ *   S0[b] <- gamma_a S0[b] + sum_r Gamma_{a,path[r]} w_{path[r]} k_{path[r]}^T   (written back)
+ * then this round is verified exactly as tv_gdn_tree_verify_wy.  The committed S0 and all
+ * outputs equal tv_gdn_commit followed by tv_gdn_tree_verify_wy, bit for bit.
+ *
+ *   prev_path [B, Lmax], prev_len [B]         the previous round's accepted paths (1 <= len
+ *                                             <= min(Lmax, prev_N, 16))
+ *   prev_parents [B, prev_N]                  the previous round's trees (the path's links are
+ *                                             checked)
+ *   prev_pseudo_v [B, prev_N, H, dv] fp32, prev_log_gamma [B, prev_N, H] fp32, prev_k
+ *   [B, prev_N, H, dk]                        the previous round's W, log(gamma) and keys; they
+ *                                             may share memory with this round's pseudo_v /
+ *                                             log_gamma outputs
+ *   S0                                        in/out
+ *   other arguments as tv_gdn_tree_verify_wy
+ *   err [B]  0, TV_ERR_BAD_TREE, TV_ERR_BAD_PATH (previous path invalid: the sequence is
+ *            skipped, S0[b] untouched) or TV_ERR_UNSUPPORTED as tv_gdn_tree_verify_wy
+ * Supported: bf16 I/O and state, dk = dv = 128, N <= 240 (else TV_ERR_UNSUPPORTED).
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_gdn_tree_verify_wy_lazy(const int32_t* prev_path, const int32_t* prev_len, int Lmax,
+                                      const int32_t* prev_parents, int prev_N, const float* prev_pseudo_v,
+                                      const float* prev_log_gamma, const void* prev_k, const void* q,
+                                      const void* k, const void* v, const float* alpha, const float* beta,
+                                      void* S0, const int32_t* parents, int B, int N, int H, int dk, int dv,
+                                      int io_dtype, int state_dtype, float q_scale, void* out,
+                                      float* pseudo_v, float* log_gamma, int32_t* err, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * tv_gdn_commit -- write the accepted node's state back into S_0.
  *
  * Source: qwen35-tree-spec §五 用途 2 and §七 Step 4 (restore the state of the last accepted

@@ -26,6 +26,8 @@ Sources
   rollback point.  ``selective_slots`` numbers the kept snapshots in node order; a commit
   whose accepted node kept no snapshot resumes from the deepest kept one on its path (or
   S_0) -- which ``commit`` already states, since it replays the path.
+* Lazy commit.  ``verify_after_commit`` is the previous round's commit followed by this
+  round's verify from the committed state: the TreeWY kernel that fuses the two must equal it.
 * Pseudo-values.  The TreeWY abstract (TreeWY: Speculative Verification for Gated DeltaNet
   Hybrids) keeps a small pseudo-value matrix instead of per-node states and rebuilds only
   the accepted state on commit.  Its derivation is not on the page.  The reading used
@@ -155,4 +157,14 @@ def selective_slots(confidence, threshold: float, capacity: int):
             slots.append(kept)
             kept += 1
     return slots, kept, kept <= capacity
+
+
+def verify_after_commit(prev_inp: dict, prev_path: np.ndarray, prev_len: np.ndarray, inp: dict):
+    """The previous round's commit, then this round's verify from the committed state.
+    Returns (committed S_0 [B,H,dv,dk], outputs [B,N,H,dv])."""
+    S0 = commit(prev_inp, prev_path, prev_len)
+    cur = dict(inp)
+    cur["S0"] = S0
+    o, _ = verify(cur, want_states=False)
+    return S0, o
 

@@ -214,3 +214,29 @@ def test_selective_slots_number_kept_snapshots_in_node_order():
     assert G.selective_slots([0.5, 0.2, 0.1], 0.95, 2)[2] is False       # 3 kept > capacity 2
     assert G.selective_slots([0.99, 0.97], 0.95, 0) == ([-1, -1], 0, True)  # nothing kept
     assert G.selective_slots([0.3] * 4, 1.0, 4) == ([0, 1, 2, 3], 4, True)  # threshold 1: all kept
+
+
+def test_commit_then_verify_continues_the_sequence():
+    # Round 1 verifies a chain of m nodes and accepts all of them; round 2 verifies a chain of n
+    # nodes from the committed state.  Round 2's outputs must be those of nodes m .. m+n-1 of a
+    # single chain over both rounds' inputs -- the plain sequential recurrence.
+    m, n, H, d = 3, 4, 2, 8
+    long = W.gdn_case([W.chain(m + n)], H=H, dk=d, dv=d, io="f32", state="f32", seed=4)
+    li = long.oracle_inputs()
+    first = {k: (v[:, :m] if k in ("q", "k", "v", "alpha", "beta") else v) for k, v in li.items()}
+    first["parents"] = np.array([W.chain(m)])
+    second = {k: (v[:, m:] if k in ("q", "k", "v", "alpha", "beta") else v) for k, v in li.items()}
+    second["parents"] = np.array([W.chain(n)])
+    path = np.array([list(range(m))])
+    S0, o = G.verify_after_commit(first, path, np.array([m]), second)
+    # the sequential recurrence over all m + n tokens, written out
+    S = li["S0"][0].copy()
+    outs = []
+    for t in range(m + n):
+        for h in range(H):
+            kk, vv, a_, b_ = li["k"][0, t, h], li["v"][0, t, h], li["alpha"][0, t, h], li["beta"][0, t, h]
+            S[h] = a_ * S[h] @ (np.eye(d) - b_ * np.outer(kk, kk)) + b_ * np.outer(vv, kk)
+        outs.append(np.einsum("hvk,hk->hv", S, li["q"][0, t]))
+        if t == m - 1:
+            assert np.allclose(S0[0], S, atol=1e-12)
+    assert np.allclose(o[0], np.stack(outs[m:]), atol=1e-12)

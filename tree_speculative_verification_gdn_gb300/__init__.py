@@ -41,7 +41,8 @@ TV_STATIC_SCRATCH_BYTES = 64 << 20
 EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_prepare",
             "tv_gdn_tree_verify_fork", "tv_gdn_tree_verify_wy", "tv_gdn_commit",
             "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact",
-            "tv_accept_walk", "tv_gdn_tree_verify_fork_selective", "tv_gdn_commit_selective")
+            "tv_accept_walk", "tv_gdn_tree_verify_fork_selective", "tv_gdn_commit_selective",
+            "tv_gdn_tree_verify_wy_lazy")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -65,6 +66,8 @@ _SIGNATURES = {
                                               _F, _P, _P, _P, _P, _P]),
     "tv_gdn_commit_selective": (_I, [_P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                     _P, _P]),
+    "tv_gdn_tree_verify_wy_lazy": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                       _I, _I, _I, _F, _P, _P, _P, _P, _P]),
     "tv_accept_walk": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
 }
@@ -159,6 +162,20 @@ def tv_gdn_commit_selective(accepted_path, accepted_len, parents, node_states, s
         _ptr(accepted_path), _ptr(accepted_len), accepted_path.shape[1], _ptr(parents), _ptr(node_states),
         _ptr(slot), node_states.shape[1], _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), B, N, H, dk, dv,
         _DTYPES[k.dtype], _DTYPES[S0.dtype], _ptr(err), _stream(stream)), "tv_gdn_commit_selective")
+
+
+def tv_gdn_tree_verify_wy_lazy(prev_path, prev_len, prev_parents, prev_pseudo_v, prev_log_gamma, prev_k,
+                               q, k, v, alpha, beta, S0, parents, out, pseudo_v, log_gamma, err,
+                               q_scale: float = 1.0, stream=None) -> None:
+    """The previous round's TreeWY commit applied to S0 (in place) inside this round's verify."""
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(lib.tv_gdn_tree_verify_wy_lazy(
+        _ptr(prev_path), _ptr(prev_len), prev_path.shape[1], _ptr(prev_parents), prev_parents.shape[1],
+        _ptr(prev_pseudo_v), _ptr(prev_log_gamma), _ptr(prev_k), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+        _ptr(beta), _ptr(S0), _ptr(parents), B, N, H, dk, dv, _DTYPES[q.dtype], _DTYPES[S0.dtype],
+        float(q_scale), _ptr(out), _ptr(pseudo_v), _ptr(log_gamma), _ptr(err), _stream(stream)),
+        "tv_gdn_tree_verify_wy_lazy")
 
 
 def tv_gdn_tree_verify_wy(q, k, v, alpha, beta, S0, parents, out, pseudo_v, log_gamma, err,

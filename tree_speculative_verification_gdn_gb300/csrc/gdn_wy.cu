@@ -184,7 +184,7 @@ cudaError_t launch_wy_t(const GdnArgs& a, float* pseudo_v, float* log_gamma, cud
 }  // namespace
 
 cudaError_t launch_gdn_wy(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s) {
-  if (gdn_wy_tc_supported(a)) return launch_gdn_wy_tc(a, pseudo_v, log_gamma, s);
+  if (gdn_wy_tc_supported(a)) return launch_gdn_wy_tc(a, pseudo_v, log_gamma, WyLazy{}, s);
   return launch_gdn_wy_simt(a, pseudo_v, log_gamma, s);
 }
 

@@ -40,9 +40,14 @@ struct TcHead {
   int lvl_cnt[TV_MAX_NODES + 1];   // nodes per depth, then start of each depth level
   int lvl_fill[TV_MAX_NODES];
   int lvl_nodes[TV_MAX_NODES];     // nodes grouped by depth
+  // lazy commit: the previous round's accepted path, gamma ratios, log(gamma) of its last node
+  int lz_nodes[kLazyMaxLen];
+  float lz_g[kLazyMaxLen];
+  float lz_lga;
+  int lz_L, lz_status, lz_pad;
 };
 
-static_assert(sizeof(TcHead) % 8 == 0, "the path-entry table after the head is 8-byte aligned");
+static_assert(sizeof(TcHead) % 16 == 0, "the path-entry table after the head is 16-byte aligned");
 
 __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* __restrict__ pseudo_v,
                                                              float* __restrict__ log_gamma, int cap, int Npad,
@@ -50,7 +55,8 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
                                                              const __grid_constant__ CUtensorMap mS0,
                                                              const __grid_constant__ CUtensorMap mK,
                                                              const __grid_constant__ CUtensorMap mQ,
-                                                             const __grid_constant__ CUtensorMap mV) {
+                                                             const __grid_constant__ CUtensorMap mV,
+                                                             const __grid_constant__ WyLazy lz) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // 1024-byte aligned tiles
@@ -94,6 +100,45 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
 
   // Topology, log(gamma), gamma, beta, depth levels and path lists while the tiles are in flight.
   int status = load_and_check_tree(a.parents + (size_t)b * N, N, hd.par, &hd.flag);
+
+  // Lazy commit (TreeWY abstract: rebuild only the accepted state): the previous round's
+  // accepted path, its log(gamma), w rows and keys, staged while the tiles are in flight.
+  // Thread 0 checks the path's own links in the previous tree.
+  int* lz_nodes = hd.lz_nodes;
+  float* lz_g = hd.lz_g;
+  float& lz_lga = hd.lz_lga;
+  int& lz_L = hd.lz_L;
+  int& lz_status = hd.lz_status;
+  float* lz_w = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(pent + cap) + 15) & ~uintptr_t(15));  // [L][128]
+  bf16* lz_k = reinterpret_cast<bf16*>(lz_w + kLazyMaxLen * kD);      // [L][128]
+  const bool lazy = lz.path != nullptr;
+  if (lazy) {
+    if (tid == 0) {
+      const int L = lz.len[b];
+      int ok = L >= 1 && L <= lz.Lmax && L <= lz.Np && L <= kLazyMaxLen, prev = -1;
+      for (int r = 0; ok && r < L; ++r) {
+        const int node = lz.path[(size_t)b * lz.Lmax + r];
+        ok = node >= 0 && node < lz.Np && lz.parents[(size_t)b * lz.Np + node] == prev;
+        if (ok) lz_nodes[r] = node;
+        prev = node;
+      }
+      lz_L = ok ? L : 0;
+      lz_status = ok ? 0 : TV_ERR_BAD_PATH;
+      if (ok) lz_lga = lz.log_gamma[((size_t)b * lz.Np + prev) * H + h];
+    }
+    __syncthreads();
+    if (!status) status = lz_status;
+    if (!status) {
+      const int L = lz_L;
+      for (int x = tid; x < L * kD; x += kThreads) {
+        const size_t nh = ((size_t)b * lz.Np + lz_nodes[x / kD]) * H + h;
+        lz_w[x] = lz.pseudo_v[nh * kD + x % kD];
+        lz_k[x] = static_cast<const bf16*>(lz.k)[nh * kD + x % kD];
+      }
+      for (int t = tid; t < L; t += kThreads)
+        lz_g[t] = expf(lz_lga - lz.log_gamma[((size_t)b * lz.Np + lz_nodes[t]) * H + h]);
+    }
+  }
   if (!status) {
     for (int i = tid; i <= N; i += kThreads) hd.lvl_cnt[i] = 0;
     for (int i = tid; i < N; i += kThreads) {  // log(alpha) and beta, one load each
@@ -159,6 +204,36 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   if (!mbar_wait(&hd.tma_bar, 0)) hd.fail = 1;
   __syncthreads();
   const bool run = !status && !hd.fail;
+
+  if (run && lazy) {
+    // S_0 <- gamma_a S_0 + sum_t (gamma_a / gamma_t) w_t k_t^T on the swizzled tile, in the
+    // operation order of the commit kernel; the committed state also goes back to HBM.
+    // Thread (row, half) takes the 64 columns of one k-block of one row.
+    const int row = tid >> 1, kb = tid & 1, L = lz_L;
+    const float gam = expf(lz_lga);
+    unsigned char* rowp = sA + kb * (kTileA / 2) + row * 128;
+    uint4* g = reinterpret_cast<uint4*>(static_cast<bf16*>(const_cast<void*>(a.S0)) +
+                                        (((size_t)b * H + h) * kD + row) * kD + kb * 64);
+    for (int ch = 0; ch < 8; ++ch) {
+      uint4* sp = reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4));
+      float x[8];
+      unpack8(*sp, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= gam;
+      for (int t = 0; t < L; ++t) {
+        const float c = lz_g[t] * lz_w[t * kD + row];
+        float kf[8];
+        unpack8(*reinterpret_cast<const uint4*>(lz_k + t * kD + kb * 64 + ch * 8), kf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = fmaf(c, kf[e], x[e]);
+      }
+      const uint4 pk = pack8(x);
+      *sp = pk;
+      g[ch] = pk;
+    }
+    fence_proxy_async();  // the MMA reads the tile through the async proxy
+  }
+  __syncthreads();
 
   if (run && tid == 0) {
     tc_fence_after();
@@ -310,13 +385,23 @@ bool gdn_wy_tc_supported(const GdnArgs& a) {
   return a.io == TV_BF16 && a.state == TV_BF16 && a.dk == kD && a.dv == kD;
 }
 
-cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s) {
+bool gdn_wy_lazy_fits(int N) {
+  const int Npad = (N + 15) / 16 * 16;
+  int cap = N * (N + 1) / 2;
+  if (cap > kPathCap) cap = kPathCap;
+  return 1024 + kTileA + (size_t)4 * Npad * 128 + sizeof(TcHead) + (size_t)cap * 12 + 16 +
+             (size_t)kLazyMaxLen * kD * 6 <= 227 * 1024;
+}
+
+cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma, const WyLazy& lz,
+                             cudaStream_t s) {
   const int Npad = (a.N + 15) / 16 * 16;
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * Npad)) cols <<= 1;
   int cap = a.N * (a.N + 1) / 2;
   if (cap > kPathCap) cap = kPathCap;
-  const size_t base = 1024 + kTileA + (size_t)4 * Npad * 128 + sizeof(TcHead) + (size_t)cap * 12;
+  const size_t lazy_bytes = lz.path != nullptr ? 16 + (size_t)kLazyMaxLen * kD * (4 + 2) : 0;
+  const size_t base = 1024 + kTileA + (size_t)4 * Npad * 128 + sizeof(TcHead) + (size_t)cap * 12 + lazy_bytes;
   const int v_in_smem = base + (size_t)2 * Npad * 128 <= 227 * 1024;
   size_t smem = base + (v_in_smem ? (size_t)2 * Npad * 128 : 0);
   auto kern = gdn_wy_tc_kernel;
@@ -346,7 +431,7 @@ cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma
     if (!make_map_bf16_sw128(&mQ, a.q, 4, dims, strides, box)) return cudaErrorInvalidValue;
     if (!make_map_bf16_sw128(&mV, a.v, 4, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  kern<<<a.B * a.H, kThreads, smem, s>>>(a, pseudo_v, log_gamma, cap, Npad, cols, v_in_smem, mS0, mK, mQ, mV);
+  kern<<<a.B * a.H, kThreads, smem, s>>>(a, pseudo_v, log_gamma, cap, Npad, cols, v_in_smem, mS0, mK, mQ, mV, lz);
   return cudaGetLastError();
 }
 

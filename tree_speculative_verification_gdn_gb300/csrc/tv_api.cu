@@ -134,6 +134,26 @@ int tv_gdn_tree_verify_wy(const void* q, const void* k, const void* v, const flo
   return cuda_status(tv::launch_gdn_wy(a, pseudo_v, log_gamma, stream));
 }
 
+int tv_gdn_tree_verify_wy_lazy(const int32_t* prev_path, const int32_t* prev_len, int Lmax,
+                               const int32_t* prev_parents, int prev_N, const float* prev_pseudo_v,
+                               const float* prev_log_gamma, const void* prev_k, const void* q, const void* k,
+                               const void* v, const float* alpha, const float* beta, void* S0,
+                               const int32_t* parents, int B, int N, int H, int dk, int dv, int io_dtype,
+                               int state_dtype, float q_scale, void* out, float* pseudo_v, float* log_gamma,
+                               int32_t* err, tv_stream_t stream) {
+  int st = gdn_common(q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale,
+                      out, err);
+  if (st != TV_OK) return st;
+  if (!a4(pseudo_v) || !a4(log_gamma) || !a4(prev_path) || !a4(prev_len) || !a4(prev_parents) ||
+      !a4(prev_pseudo_v) || !a4(prev_log_gamma) || !a16(prev_k) || Lmax < 1 || prev_N < 1)
+    return TV_ERR_INVALID_ARG;
+  if (prev_N > TV_MAX_NODES) return TV_ERR_UNSUPPORTED;
+  tv::GdnArgs a{q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale, out, err};
+  if (!tv::gdn_wy_tc_supported(a) || !tv::gdn_wy_lazy_fits(N)) return TV_ERR_UNSUPPORTED;
+  const tv::WyLazy lz{prev_path, prev_len, Lmax, prev_N, prev_parents, prev_pseudo_v, prev_log_gamma, prev_k};
+  return cuda_status(tv::launch_gdn_wy_tc(a, pseudo_v, log_gamma, lz, stream));
+}
+
 int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,
                   const int32_t* parents, const void* node_states, const float* pseudo_v,
                   const float* log_gamma, const void* k, void* S0, int B, int N, int H, int dk, int dv,

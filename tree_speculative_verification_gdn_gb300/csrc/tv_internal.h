@@ -47,7 +47,22 @@ cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, const ForkSelec
 // for every other supported shape.
 cudaError_t launch_gdn_wy(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s);
 bool gdn_wy_tc_supported(const GdnArgs& a);
-cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s);
+// Lazy commit: the previous round's TreeWY commit applied to S_0 inside this round's verify.
+// path == nullptr: no pending commit.
+constexpr int kLazyMaxLen = 16;  // longest previous accepted path the fused commit takes
+struct WyLazy {
+  const int32_t* path;      // [B, Lmax] previous round's accepted paths
+  const int32_t* len;       // [B]
+  int Lmax;
+  int Np;                   // previous round's nodes per tree
+  const int32_t* parents;   // [B, Np] previous round's trees
+  const float* pseudo_v;    // [B, Np, H, dv] previous round's W
+  const float* log_gamma;   // [B, Np, H]
+  const void* k;            // [B, Np, H, dk] previous round's keys
+};
+cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma, const WyLazy& lz,
+                             cudaStream_t s);
+bool gdn_wy_lazy_fits(int N);  // shared memory of the fused-commit kernel fits for N nodes
 cudaError_t launch_gdn_wy_simt(const GdnArgs& a, float* pseudo_v, float* log_gamma, cudaStream_t s);
 
 struct CommitArgs {
