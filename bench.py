@@ -249,10 +249,11 @@ class Round:
         ws = tv.tv_tree_attn_workspace_size(self.aB, self.aN, self.Hq, self.Hkv, self.hd, a.block_table.shape[1])
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.slot_map = torch.empty(a.path.shape, dtype=i32, device=dev)
+        self.fork_ws = torch.empty(tv.tv_gdn_fork_workspace_size(B, N, H, dv), dtype=torch.uint8, device=dev)
         self.new_len = torch.empty((self.aB,), dtype=i32, device=dev)
         self.rows = ["tree_prepare", "fork_verify", "accept_walk", "fork_commit", "wy_verify", "wy_commit",
                      "tree_attn", "kv_compact"]
-        self.launches_per_step = 1 + layers * 4 + 4 + 1 + 2
+        self.launches_per_step = 1 + layers * 5 + 4 + 1 + 2   # the fork verify is two launches
 
     def step(self, ev=None):
         """One verify round.  ``ev``: optional dict row -> list of (start, end) event pairs."""
@@ -273,9 +274,10 @@ class Round:
         mark("tree_prepare", lambda: tv.tv_tree_prepare(self.parents, self.depth, self.mask, err[0, :B]))
         for l in range(self.layers):
             x = self.in_gdn[l]
-            mark("fork_verify", lambda: tv.tv_gdn_tree_verify_fork(
+            # fork mode in two passes: TreeWY outputs and w, then every snapshot from its parent's
+            mark("fork_verify", lambda: tv.tv_gdn_tree_verify_fork_ws(
                 x["q"], x["k"], x["v"], x["alpha"], x["beta"], self.S0_fork[l], self.parents, self.o_fork[l],
-                self.states[l], err[1, :B]))
+                self.states[l], self.fork_ws, err[1, :B]))
         # the target's tokens pick the accepted path on the device (one walk feeds both modes' commits)
         mark("accept_walk", lambda: tv.tv_accept_walk(
             self.parents, self.tokens["draft"], self.tokens["target"], self.path, self.path_len, self.next_tok,
@@ -454,6 +456,32 @@ def selective_fork_report(rnd, torch, tv, iters: int = 3) -> dict:
             "verify_ms_per_layer": round(v_ms, 5), "commit_ms_per_layer": round(c_ms, 5)}
 
 
+def one_pass_fork_report(rnd, torch, tv, iters: int = 3) -> dict:
+    """The one-pass fork verify (each row's dot products computed along the walk) on the same
+    24-layer stack, timed apart from the step, which uses the two-pass form."""
+    err = torch.zeros((rnd.B,), dtype=torch.int32, device=rnd.dev)
+    S0 = [s.clone() for s in rnd.S0_fork]
+
+    def once(ev=None):
+        for l in range(rnd.layers):
+            x = rnd.in_gdn[l]
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            tv.tv_gdn_tree_verify_fork(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S0[l], rnd.parents,
+                                       rnd.o_fork[l], rnd.states[l], err)
+            e.record()
+            if ev is not None:
+                ev.append((s, e))
+    once()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(iters):
+        once(ev)
+    torch.cuda.synchronize()
+    assert int(err.abs().sum()) == 0, err
+    return {"ms_per_layer": round(sum(s.elapsed_time(e) for s, e in ev) / len(ev), 5)}
+
+
 def lazy_commit_report(rnd, torch, tv, iters: int = 3) -> dict:
     """TreeWY with the previous round's commit fused into this round's verify, on the same
     24-layer stack, timed apart from the step: each layer's last W, log(gamma), keys and the
@@ -566,6 +594,7 @@ def run_ours(args) -> None:
 
     selective = selective_fork_report(rnd, torch, tv)
     lazy = lazy_commit_report(rnd, torch, tv)
+    one_pass = one_pass_fork_report(rnd, torch, tv)
     peaks = load_peaks()
     B, N, H, dk, dv = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv
     L_sum = int(rnd.gdn_host[0].path_len.sum())
@@ -611,7 +640,8 @@ def run_ours(args) -> None:
                        "l2": "working set >> 129 MB L2 (fork checkpoints 1.3 GB per layer)",
                        "parallelism": f"replicas x{world}"},
             "gpu_launches": rnd.launches_per_step * args.steps, "clocks": clk, "roofline": roof,
-            "rows": rows, "state_memory": mem, "selective_fork": selective, "lazy_commit": lazy, "e2e": e2e,
+            "rows": rows, "state_memory": mem, "selective_fork": selective, "lazy_commit": lazy,
+            "one_pass_fork": one_pass, "e2e": e2e,
             "cpu_baseline": cpu_base}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -219,6 +219,29 @@ TV_API int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* 
                   int dv, int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * tv_gdn_tree_verify_fork_ws -- fork mode in two passes, with a workspace.
+ *
+ * Same results and layouts as tv_gdn_tree_verify_fork (outputs and every node's snapshot),
+ * computed differently: a TreeWY pass (TreeWY abstract: one triangular solve gives every
+ * node's output and pseudo-value w_i = beta_i (v_i - alpha_i S_parent k_i)) writes the outputs
+ * and w into the workspace; then every snapshot is materialized from its parent's along the
+ * depth-first walk, S_i = alpha_i S_parent + w_i k_i^T -- the gated delta update
+ * (qwen35-tree-spec §四) with its S_parent k_i term taken from the solve.
+ *
+ *   workspace   device scratch of at least tv_gdn_fork_workspace_size(B, N, H, dv) bytes,
+ *               16-byte aligned, owned by the caller; contents on entry are ignored.  Calls
+ *               that share a workspace must not overlap in time.
+ *   err [B]     0, TV_ERR_BAD_TREE, or TV_ERR_UNSUPPORTED (also when the sum over nodes of
+ *               (depth + 1) exceeds 4096, the TreeWY limit)
+ * ---------------------------------------------------------------------------------------- */
+TV_API size_t tv_gdn_fork_workspace_size(int B, int N, int H, int dv);
+TV_API int tv_gdn_tree_verify_fork_ws(const void* q, const void* k, const void* v, const float* alpha,
+                                      const float* beta, const void* S0, const int32_t* parents, int B, int N,
+                                      int H, int dk, int dv, int io_dtype, int state_dtype, float q_scale,
+                                      void* out, void* node_states, void* workspace, size_t workspace_bytes,
+                                      int32_t* err, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * tv_gdn_tree_verify_fork_selective / tv_gdn_commit_selective -- fork mode with selective
  * snapshots.
  *

@@ -42,7 +42,7 @@ EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_pre
             "tv_gdn_tree_verify_fork", "tv_gdn_tree_verify_wy", "tv_gdn_commit",
             "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact",
             "tv_accept_walk", "tv_gdn_tree_verify_fork_selective", "tv_gdn_commit_selective",
-            "tv_gdn_tree_verify_wy_lazy")
+            "tv_gdn_tree_verify_wy_lazy", "tv_gdn_fork_workspace_size", "tv_gdn_tree_verify_fork_ws")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -68,6 +68,9 @@ _SIGNATURES = {
                                     _P, _P]),
     "tv_gdn_tree_verify_wy_lazy": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                        _I, _I, _I, _F, _P, _P, _P, _P, _P]),
+    "tv_gdn_fork_workspace_size": (_Z, [_I, _I, _I, _I]),
+    "tv_gdn_tree_verify_fork_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _Z,
+                                       _P, _P]),
     "tv_accept_walk": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
 }
@@ -138,6 +141,21 @@ def tv_gdn_tree_verify_fork(q, k, v, alpha, beta, S0, parents, out, node_states,
         _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(parents), B, N, H, dk, dv,
         _DTYPES[q.dtype], _DTYPES[S0.dtype], float(q_scale), _ptr(out), _ptr(node_states), _ptr(err),
         _stream(stream)), "tv_gdn_tree_verify_fork")
+
+
+def tv_gdn_fork_workspace_size(B, N, H, dv) -> int:
+    return int(lib.tv_gdn_fork_workspace_size(B, N, H, dv))
+
+
+def tv_gdn_tree_verify_fork_ws(q, k, v, alpha, beta, S0, parents, out, node_states, workspace, err,
+                               q_scale: float = 1.0, stream=None) -> None:
+    """Fork mode in two passes (TreeWY outputs and w, then the snapshots) with a workspace."""
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    _check(lib.tv_gdn_tree_verify_fork_ws(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(parents), B, N, H, dk, dv,
+        _DTYPES[q.dtype], _DTYPES[S0.dtype], float(q_scale), _ptr(out), _ptr(node_states), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)), "tv_gdn_tree_verify_fork_ws")
 
 
 def tv_gdn_tree_verify_fork_selective(q, k, v, alpha, beta, S0, parents, confidence, threshold: float, out,

@@ -156,6 +156,14 @@ struct Raw<bf16, CPL> {
     }
     v = to_f32(__ldg(vp));
   }
+  __device__ __forceinline__ void load_kw(const bf16* kp, const float* wp) {  // keys and a given w
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(kp + j * kStride));
+      k[4 * j] = a.x; k[4 * j + 1] = a.y; k[4 * j + 2] = a.z; k[4 * j + 3] = a.w;
+    }
+    v = __ldg(wp);
+  }
   __device__ __forceinline__ float kf(int e) const { return (e & 1) ? bf16hi(k[e >> 1]) : bf16lo(k[e >> 1]); }
   __device__ __forceinline__ float qf(int e) const { return (e & 1) ? bf16hi(q[e >> 1]) : bf16lo(q[e >> 1]); }
 };
@@ -172,13 +180,22 @@ struct Raw<float, CPL> {
     }
     v = __ldg(vp);
   }
+  __device__ __forceinline__ void load_kw(const float* kp, const float* wp) {
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) load_vec<8>(kp + j * kStride, k + 8 * j);
+    v = __ldg(wp);
+  }
   __device__ __forceinline__ float kf(int e) const { return k[e]; }
   __device__ __forceinline__ float qf(int e) const { return q[e]; }
 };
 
-template <typename TIO, typename TS, int DK>
+// FROM_W: the second pass of the two-pass fork -- w_i (and every output) already came from the
+// TreeWY pass in wsrc [B, N, H, dv]; this pass only materializes the snapshots,
+// S_i = alpha_i S_p + w_i k_i^T, along the same walk.
+template <typename TIO, typename TS, int DK, bool FROM_W>
 __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __restrict__ states,
-                                                            int ctas_per_seq, int nslots, ForkSelect sel) {
+                                                            int ctas_per_seq, int nslots, ForkSelect sel,
+                                                            const float* __restrict__ wsrc) {
   constexpr int CPL = DK / kLPR;  // columns per lane
   constexpr int Q4 = CPL / 4;     // float4 per lane per slot
   extern __shared__ __align__(128) unsigned char smem[];
@@ -189,6 +206,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
   const int b = blockIdx.x / ctas_per_seq, g = blockIdx.x % ctas_per_seq;
   const int N = a.N, H = a.H, dv = a.dv;
   const int tid = threadIdx.x;
+  if (FROM_W && a.err[b] != 0) return;  // the TreeWY pass rejected this sequence
   int status = build_schedule(a.parents + (size_t)b * N, N, sc, scratch);
   if (!status && sc.maxslot > nslots) status = TV_ERR_UNSUPPORTED;
   // Snapshot slots (selective fork): nodes at or below the confidence threshold, numbered in
@@ -214,7 +232,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     for (int i = tid; i < N; i += kThreads) scratch.slot[i] = i;
     __syncthreads();
   }
-  if (g == 0 && tid == 0) a.err[b] = status;
+  if (g == 0 && tid == 0 && (status || !FROM_W)) a.err[b] = status;
   if (status) return;
 
   const TIO* __restrict__ q = static_cast<const TIO*>(a.q);
@@ -244,6 +262,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
       const int t = x / per_node, c = x % per_node;
       const size_t nh = n0 + (size_t)t * H;
       const void* p = c < kq_lines ? (const void*)(k + nh * DK + c * (128 / sizeof(TIO)))
+                    : FROM_W           ? (const void*)(wsrc + nh * dv + r0)
                     : c < 2 * kq_lines ? (const void*)(q + nh * DK + (c - kq_lines) * (128 / sizeof(TIO)))
                                        : (const void*)(v + nh * dv + r0);
       asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
@@ -269,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     }
     // k_i . q_i is the same for every row of the head: 8 threads per node compute it once.
     // The loop bound is warp-uniform, so every lane takes part in the shuffles.
-    for (int t0 = 0; t0 < N; t0 += kThreads / kLPR) {
+    for (int t0 = 0; !FROM_W && t0 < N; t0 += kThreads / kLPR) {
       const int t = t0 + tid / kLPR;
       float dot = 0.f;
       if (t < N) {
@@ -291,11 +310,16 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     TIO* out_r = out + nh0 * dv + r;
     // snapshots of this sequence: [capacity][H][dv][dk]
     TS* st_r = states + ((((size_t)b * sel.capacity) * H + h) * dv + r) * DK + lane * 8;
+    const float* wb = FROM_W ? wsrc + nh0 * dv + r : nullptr;
     auto fetch = [&](int t, Raw<TIO, CPL>& x) {
       x.e = sc.ent[t < N ? t : N - 1];
-      x.kq = sc.kq[t < N ? t : N - 1];
       const int node = x.e.x;
-      x.load(kb + node * kq_stride, qb + node * kq_stride, vb + node * node_stride);
+      if constexpr (FROM_W) {
+        x.load_kw(kb + node * kq_stride, wb + node * node_stride);
+      } else {
+        x.kq = sc.kq[t < N ? t : N - 1];
+        x.load(kb + node * kq_stride, qb + node * kq_stride, vb + node * node_stride);
+      }
     };
     float2 cur[CPL / 2];  // the row's state, column pairs (2e, 2e + 1)
     // One node: parent state -> output and S_i (kept in cur), checkpoint, optional push.  The
@@ -321,28 +345,33 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
           cur[2 * j + 1] = make_float2(f.z, f.w);
         }
       }
-      float2 kf[CPL / 2], qf[CPL / 2];
+      float2 kf[CPL / 2];
 #pragma unroll
-      for (int e = 0; e < CPL / 2; ++e) {
-        kf[e] = make_float2(x.kf(2 * e), x.kf(2 * e + 1));
-        qf[e] = make_float2(x.qf(2 * e), x.qf(2 * e + 1));
-      }
-      float2 pk0 = make_float2(0.f, 0.f), pk1 = pk0, pq0 = pk0, pq1 = pk0;
+      for (int e = 0; e < CPL / 2; ++e) kf[e] = make_float2(x.kf(2 * e), x.kf(2 * e + 1));
+      float w;                                              // pseudo-value w_i[r]
+      if constexpr (FROM_W) {
+        w = x.v;
+      } else {
+        float2 qf[CPL / 2];
 #pragma unroll
-      for (int e = 0; e < CPL / 2; e += 2) {
-        pk0 = __ffma2_rn(cur[e], kf[e], pk0);
-        pq0 = __ffma2_rn(cur[e], qf[e], pq0);
-        pk1 = __ffma2_rn(cur[e + 1], kf[e + 1], pk1);
-        pq1 = __ffma2_rn(cur[e + 1], qf[e + 1], pq1);
-      }
-      float pk = (pk0.x + pk1.x) + (pk0.y + pk1.y), pq = (pq0.x + pq1.x) + (pq0.y + pq1.y);
+        for (int e = 0; e < CPL / 2; ++e) qf[e] = make_float2(x.qf(2 * e), x.qf(2 * e + 1));
+        float2 pk0 = make_float2(0.f, 0.f), pk1 = pk0, pq0 = pk0, pq1 = pk0;
 #pragma unroll
-      for (int o = kLPR / 2; o > 0; o >>= 1) {
-        pk += __shfl_xor_sync(0xffffffffu, pk, o);
-        pq += __shfl_xor_sync(0xffffffffu, pq, o);
+        for (int e = 0; e < CPL / 2; e += 2) {
+          pk0 = __ffma2_rn(cur[e], kf[e], pk0);
+          pq0 = __ffma2_rn(cur[e], qf[e], pq0);
+          pk1 = __ffma2_rn(cur[e + 1], kf[e + 1], pk1);
+          pq1 = __ffma2_rn(cur[e + 1], qf[e + 1], pq1);
+        }
+        float pk = (pk0.x + pk1.x) + (pk0.y + pk1.y), pq = (pq0.x + pq1.x) + (pq0.y + pq1.y);
+#pragma unroll
+        for (int o = kLPR / 2; o > 0; o >>= 1) {
+          pk += __shfl_xor_sync(0xffffffffu, pk, o);
+          pq += __shfl_xor_sync(0xffffffffu, pq, o);
+        }
+        w = be * (x.v - al * pk);
+        if (lane == 0) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * pq + w * x.kq) * q_scale);
       }
-      const float w = be * (x.v - al * pk);                 // pseudo-value w_i[r]
-      if (lane == 0) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * pq + w * x.kq) * q_scale);
       const float2 al2 = make_float2(al, al), w2 = make_float2(w, w);
 #pragma unroll
       for (int e = 0; e < CPL / 2; ++e) cur[e] = __ffma2_rn(w2, kf[e], __fmul2_rn(al2, cur[e]));
@@ -376,9 +405,10 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
   }
 }
 
-template <typename TIO, typename TS, int DK>
-cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel, cudaStream_t s) {
-  auto kern = gdn_fork_kernel<TIO, TS, DK>;
+template <typename TIO, typename TS, int DK, bool FROM_W = false>
+cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel, cudaStream_t s,
+                          const float* wsrc = nullptr) {
+  auto kern = gdn_fork_kernel<TIO, TS, DK, FROM_W>;
   const int nslots = slots_for(a.N);
   size_t stack = (size_t)nslots * (DK / kLPR / 4) * kThreads * sizeof(float4);
   if (stack < sizeof(BuildScratch)) stack = sizeof(BuildScratch);
@@ -393,7 +423,7 @@ cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel,
   int per_seq = slots / a.B;
   if (per_seq < 1) per_seq = 1;
   if (per_seq > items) per_seq = items;
-  kern<<<a.B * per_seq, kThreads, smem, s>>>(a, static_cast<TS*>(states), per_seq, nslots, sel);
+  kern<<<a.B * per_seq, kThreads, smem, s>>>(a, static_cast<TS*>(states), per_seq, nslots, sel, wsrc);
   return cudaGetLastError();
 }
 
@@ -409,6 +439,21 @@ cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, const ForkSelec
                       : launch_fork_t<bf16, bf16, 128>(a, node_states, sel, s);
   return a.dk == 64 ? launch_fork_t<bf16, float, 64>(a, node_states, sel, s)
                     : launch_fork_t<bf16, float, 128>(a, node_states, sel, s);
+}
+
+cudaError_t launch_gdn_fork_two_pass(const GdnArgs& a, void* node_states, float* pseudo_v, float* log_gamma,
+                                     cudaStream_t s) {
+  cudaError_t e = launch_gdn_wy(a, pseudo_v, log_gamma, s);  // every output, and w
+  if (e != cudaSuccess) return e;
+  const ForkSelect all{nullptr, 0.f, a.N, nullptr};
+  if (a.io == TV_F32 && a.state == TV_F32)
+    return a.dk == 64 ? launch_fork_t<float, float, 64, true>(a, node_states, all, s, pseudo_v)
+                      : launch_fork_t<float, float, 128, true>(a, node_states, all, s, pseudo_v);
+  if (a.io == TV_BF16 && a.state == TV_BF16)
+    return a.dk == 64 ? launch_fork_t<bf16, bf16, 64, true>(a, node_states, all, s, pseudo_v)
+                      : launch_fork_t<bf16, bf16, 128, true>(a, node_states, all, s, pseudo_v);
+  return a.dk == 64 ? launch_fork_t<bf16, float, 64, true>(a, node_states, all, s, pseudo_v)
+                    : launch_fork_t<bf16, float, 128, true>(a, node_states, all, s, pseudo_v);
 }
 
 }  // namespace tv

@@ -105,6 +105,29 @@ int tv_gdn_tree_verify_fork(const void* q, const void* k, const void* v, const f
   return cuda_status(tv::launch_gdn_fork(a, node_states, all, stream));
 }
 
+size_t tv_gdn_fork_workspace_size(int B, int N, int H, int dv) {
+  if (B < 1 || N < 1 || H < 1 || dv < 1) return 0;
+  const size_t pv = ((size_t)B * N * H * dv * 4 + 255) & ~(size_t)255;
+  const size_t lg = ((size_t)B * N * H * 4 + 255) & ~(size_t)255;
+  return pv + lg;
+}
+
+int tv_gdn_tree_verify_fork_ws(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
+                               const void* S0, const int32_t* parents, int B, int N, int H, int dk, int dv,
+                               int io_dtype, int state_dtype, float q_scale, void* out, void* node_states,
+                               void* workspace, size_t workspace_bytes, int32_t* err, tv_stream_t stream) {
+  int st = gdn_common(q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale,
+                      out, err);
+  if (st != TV_OK) return st;
+  if (!a16(node_states) || !a16(workspace)) return TV_ERR_INVALID_ARG;
+  if (workspace_bytes < tv_gdn_fork_workspace_size(B, N, H, dv)) return TV_ERR_INVALID_ARG;
+  float* pv = static_cast<float*>(workspace);
+  float* lg = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       (((size_t)B * N * H * dv * 4 + 255) & ~(size_t)255));
+  tv::GdnArgs a{q, k, v, alpha, beta, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, q_scale, out, err};
+  return cuda_status(tv::launch_gdn_fork_two_pass(a, node_states, pv, lg, stream));
+}
+
 int tv_gdn_tree_verify_fork_selective(const void* q, const void* k, const void* v, const float* alpha,
                                       const float* beta, const void* S0, const int32_t* parents,
                                       const float* confidence, float threshold, int capacity, int B, int N,

@@ -42,6 +42,10 @@ struct ForkSelect {
   int32_t* slot;            // [B, N] out (slot or -1), or nullptr
 };
 cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, const ForkSelect& sel, cudaStream_t s);
+// Two-pass fork: the TreeWY pass writes every output and w (pseudo_v, log_gamma: caller scratch),
+// then the walk materializes every snapshot from its parent's, S_i = alpha_i S_p + w_i k_i^T.
+cudaError_t launch_gdn_fork_two_pass(const GdnArgs& a, void* node_states, float* pseudo_v, float* log_gamma,
+                                     cudaStream_t s);
 
 // TreeWY verify: tcgen05 kernel for bf16 I/O and state with dk = dv = 128, CUDA-core kernel
 // for every other supported shape.
