@@ -26,6 +26,16 @@ constexpr int kPathCap = 4096;  // max sum over nodes of (depth + 1)
 constexpr int kBatch = 8;       // nodes per warp in flight during the solve
 constexpr uint32_t kTileA = kD * kD * 2;  // S_0 tile bytes
 
+// tcgen05.wait::ld with the 16 destination registers of the loads it waits for as operands:
+// every later use of them depends on the wait.
+__device__ __forceinline__ void tmem_wait_ld8x2(uint32_t* a, uint32_t* c) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                 "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3]), "+r"(c[4]), "+r"(c[5]), "+r"(c[6]), "+r"(c[7])
+               :
+               : "memory");
+}
+
 struct TcHead {
   uint64_t tma_bar;
   uint64_t mma_bar;
@@ -48,6 +58,7 @@ struct TcHead {
 };
 
 static_assert(sizeof(TcHead) % 16 == 0, "the path-entry table after the head is 16-byte aligned");
+static_assert(TV_MAX_NODES <= kThreads, "one node per thread in the prologue");
 
 __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* __restrict__ pseudo_v,
                                                              float* __restrict__ log_gamma, int cap, int Npad,
@@ -75,10 +86,19 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   const int b = blockIdx.x / H, h = blockIdx.x % H;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
+  // One node per thread (N <= kThreads): its parent, alpha and beta are requested before any
+  // barrier, so the three loads overlap each other and the set-up below.
+  const bool own = tid < N;
+  const size_t nh_own = ((size_t)b * N + tid) * H + h;
+  const int par_own = own ? __ldg(a.parents + (size_t)b * N + tid) : -1;
+  const float alpha_own = own ? __ldg(a.alpha + nh_own) : 1.f;
+  const float beta_own = own ? __ldg(a.beta + nh_own) : 0.f;
+
   if (tid == 0) {
     mbar_init(&hd.tma_bar, 1);
     mbar_init(&hd.mma_bar, 1);
     hd.fail = 0;
+    hd.flag = 0;
     hd.maxdepth = 0;
     mbar_fence_init();
   }
@@ -99,7 +119,16 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   }
 
   // Topology, log(gamma), gamma, beta, depth levels and path lists while the tiles are in flight.
-  int status = load_and_check_tree(a.parents + (size_t)b * N, N, hd.par, &hd.flag);
+  // A parent must be -1 or an earlier node.
+  if (own) {
+    hd.par[tid] = par_own;
+    if (par_own < -1 || par_own >= tid) hd.flag = 1;
+    hd.gam[tid] = logf(alpha_own);
+    hd.beta[tid] = beta_own;
+  }
+  for (int i = tid; i <= N; i += kThreads) hd.lvl_cnt[i] = 0;
+  __syncthreads();
+  int status = hd.flag ? TV_ERR_BAD_TREE : 0;
 
   // Lazy commit (TreeWY abstract: rebuild only the accepted state): the previous round's
   // accepted path, its log(gamma), w rows and keys, staged while the tiles are in flight.
@@ -140,12 +169,6 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
     }
   }
   if (!status) {
-    for (int i = tid; i <= N; i += kThreads) hd.lvl_cnt[i] = 0;
-    for (int i = tid; i < N; i += kThreads) {  // log(alpha) and beta, one load each
-      hd.gam[i] = logf(__ldg(a.alpha + ((size_t)b * N + i) * H + h));
-      hd.beta[i] = __ldg(a.beta + ((size_t)b * N + i) * H + h);
-    }
-    __syncthreads();
     for (int i = tid; i < N; i += kThreads) {
       int d = 0;
       float lg = hd.gam[i];
@@ -308,19 +331,48 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
     const int r = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float q_scale = a.q_scale;
-    for (int d = 0; d <= hd.maxdepth; ++d) {
+    const int maxd = hd.maxdepth;
+    // The (S_0 k, S_0 q) columns are MMA results that the solve never changes, so each warp
+    // requests the next batch's columns before it computes the current one: the TMEM load
+    // latency hides behind a batch of work.  (ld_d, ld_base) is the next batch to request, in
+    // the order the loop below consumes them.
+    uint32_t nk[kBatch], nq[kBatch];
+    int ld_d = 0, ld_base = wg * kBatch;
+    auto request_next = [&]() {
+      while (ld_d <= maxd && ld_base >= hd.lvl_cnt[ld_d]) {
+        ++ld_d;
+        if (ld_d <= maxd) ld_base = hd.lvl_cnt[ld_d - 1] + wg * kBatch;
+      }
+      if (ld_d > maxd) return;
+      const int s1 = hd.lvl_cnt[ld_d];
+#pragma unroll
+      for (int x = 0; x < kBatch; ++x) {
+        const int pos = ld_base + x;
+        const int col = pos < s1 ? hd.lvl_nodes[pos] : 0;
+        nk[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)col);
+        nq[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)(Npad + col));
+      }
+      ld_base += 2 * kBatch;
+    };
+    request_next();
+    for (int d = 0; d <= maxd; ++d) {
       const int s0 = d ? hd.lvl_cnt[d - 1] : 0, s1 = hd.lvl_cnt[d];
       for (int base = s0 + wg * kBatch; base < s1; base += 2 * kBatch) {
         uint32_t dk[kBatch], dq[kBatch];
         float vv[kBatch];
         int nodes[kBatch];
+        tmem_wait_ld8x2(nk, nq);  // the wait names the registers, so no use moves above it
+#pragma unroll
+        for (int x = 0; x < kBatch; ++x) {
+          dk[x] = nk[x];
+          dq[x] = nq[x];
+        }
+        request_next();
 #pragma unroll
         for (int x = 0; x < kBatch; ++x) {
           const int pos = base + x;
           nodes[x] = pos < s1 ? hd.lvl_nodes[pos] : -1;
           const int col = nodes[x] < 0 ? 0 : nodes[x];
-          dk[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)col);
-          dq[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)(Npad + col));
           if (v_in_smem) {  // v[node][r] from the swizzled V tile
             const int n = col, c = r % 64;
             const bf16* p = reinterpret_cast<const bf16*>(sV + (r / 64) * kq_bytes + n * 128 +
@@ -330,7 +382,6 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
             vv[x] = nodes[x] < 0 ? 0.f : to_f32(v[(((size_t)b * N + col) * H + h) * kD + r]);
           }
         }
-        tmem_wait_ld();
         // Every node of the level has depth d: walk the d ancestors of all kBatch nodes together
         // (independent chains), accumulating both the solve and the ancestors' share of the output
         // from one read of each ancestor's w.
