@@ -242,6 +242,34 @@ TV_API int tv_gdn_tree_verify_fork_ws(const void* q, const void* k, const void* 
                                       int32_t* err, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * tv_gdn_fork_materialize -- the snapshot pass of tv_gdn_tree_verify_fork_ws as a call of its
+ * own, so that it can run on a second stream.
+ *
+ * Source: the gated delta update of qwen35-tree-spec §四, S_i = alpha_i S_parent + w_i k_i^T,
+ * with w_i from a TreeWY verify (TreeWY abstract).  Every output of fork mode, and w, come from
+ * tv_gdn_tree_verify_wy on the same q, k, v, alpha, beta, S0 and parents; this call writes
+ * node_states exactly as tv_gdn_tree_verify_fork_ws does.  Nothing downstream of the outputs
+ * needs the snapshots until the commit, so a caller may run this pass on its own stream (after
+ * an event recorded behind the verify) while the next layer's verify runs on the first.
+ *
+ *   k, alpha, S0, parents   as tv_gdn_tree_verify_fork (read)
+ *   pseudo_v     [B, N, H, dv] fp32, the w written by tv_gdn_tree_verify_wy (read)
+ *   node_states  [B, N, H, dv, dk] state_dtype, 16-byte aligned (written)
+ *   err [B]      in: the verify's per-sequence status -- a sequence with err != 0 is skipped
+ *                and its snapshots are left untouched; out: unchanged for the others unless
+ *                the depth-first schedule fails (TV_ERR_UNSUPPORTED)
+ *   max_ctas_per_sm  0: as many resident CTAs per SM as fit; > 0: at most that many, which
+ *                leaves registers and shared memory for kernels of other streams
+ * Returns TV_ERR_INVALID_ARG for null or misaligned pointers, B, N or H < 1, or a negative
+ * max_ctas_per_sm; TV_ERR_UNSUPPORTED for sizes or dtypes without a kernel.
+ * The paper has no counterpart of the split: it is a scheduling choice of this library.
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_gdn_fork_materialize(const void* k, const float* alpha, const void* S0, const int32_t* parents,
+                                   const float* pseudo_v, int B, int N, int H, int dk, int dv, int io_dtype,
+                                   int state_dtype, int max_ctas_per_sm, void* node_states, int32_t* err,
+                                   tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * tv_gdn_tree_verify_fork_selective / tv_gdn_commit_selective -- fork mode with selective
  * snapshots.
  *

@@ -42,7 +42,8 @@ EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_pre
             "tv_gdn_tree_verify_fork", "tv_gdn_tree_verify_wy", "tv_gdn_commit",
             "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact",
             "tv_accept_walk", "tv_gdn_tree_verify_fork_selective", "tv_gdn_commit_selective",
-            "tv_gdn_tree_verify_wy_lazy", "tv_gdn_fork_workspace_size", "tv_gdn_tree_verify_fork_ws")
+            "tv_gdn_tree_verify_wy_lazy", "tv_gdn_fork_workspace_size", "tv_gdn_tree_verify_fork_ws",
+            "tv_gdn_fork_materialize")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -71,6 +72,7 @@ _SIGNATURES = {
     "tv_gdn_fork_workspace_size": (_Z, [_I, _I, _I, _I]),
     "tv_gdn_tree_verify_fork_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _Z,
                                        _P, _P]),
+    "tv_gdn_fork_materialize": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "tv_accept_walk": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
 }
@@ -156,6 +158,17 @@ def tv_gdn_tree_verify_fork_ws(q, k, v, alpha, beta, S0, parents, out, node_stat
         _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(S0), _ptr(parents), B, N, H, dk, dv,
         _DTYPES[q.dtype], _DTYPES[S0.dtype], float(q_scale), _ptr(out), _ptr(node_states), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream)), "tv_gdn_tree_verify_fork_ws")
+
+
+def tv_gdn_fork_materialize(k, alpha, S0, parents, pseudo_v, node_states, err, max_ctas_per_sm: int = 0,
+                            stream=None) -> None:
+    """Every fork-mode snapshot from the w of a preceding tv_gdn_tree_verify_wy (same inputs)."""
+    B, N, H, dk = k.shape
+    dv = pseudo_v.shape[-1]
+    _check(lib.tv_gdn_fork_materialize(
+        _ptr(k), _ptr(alpha), _ptr(S0), _ptr(parents), _ptr(pseudo_v), B, N, H, dk, dv, _DTYPES[k.dtype],
+        _DTYPES[S0.dtype], int(max_ctas_per_sm), _ptr(node_states), _ptr(err), _stream(stream)),
+        "tv_gdn_fork_materialize")
 
 
 def tv_gdn_tree_verify_fork_selective(q, k, v, alpha, beta, S0, parents, confidence, threshold: float, out,

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
       asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(S0 + (((size_t)b * H + hh) * dv + r0) * DK) + x * 128));
     for (int x = tid; x < (N * H + 31) / 32; x += kThreads) {  // alpha and beta of the sequence
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a.alpha + (size_t)b * N * H + x * 32));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beta + (size_t)b * N * H + x * 32));
+      if (!FROM_W) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beta + (size_t)b * N * H + x * 32));
     }
   };
   if (g < items) prefetch_item(g);
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     for (int t = tid; t < N; t += kThreads) {
       const size_t nh = nh0 + (size_t)sc.ent[t].x * H;
       sc.ent[t].z = __float_as_int(__ldg(a.alpha + nh));
-      sc.ent[t].w = __float_as_int(__ldg(a.beta + nh));
+      sc.ent[t].w = FROM_W ? 0 : __float_as_int(__ldg(a.beta + nh));  // w already holds beta
     }
     // k_i . q_i is the same for every row of the head: 8 threads per node compute it once.
     // The loop bound is warp-uniform, so every lane takes part in the shuffles.
@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
 
 template <typename TIO, typename TS, int DK, bool FROM_W = false>
 cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel, cudaStream_t s,
-                          const float* wsrc = nullptr) {
+                          const float* wsrc = nullptr, int max_ctas_per_sm = 0) {
   auto kern = gdn_fork_kernel<TIO, TS, DK, FROM_W>;
   const int nslots = slots_for(a.N);
   size_t stack = (size_t)nslots * (DK / kLPR / 4) * kThreads * sizeof(float4);
@@ -418,6 +418,7 @@ cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel,
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
   if (e != cudaSuccess) return e;
+  if (max_ctas_per_sm > 0 && occ > max_ctas_per_sm) occ = max_ctas_per_sm;
   const int items = a.H * (a.dv / kRows);
   const int slots = device_sm_count() * (occ > 0 ? occ : 1);
   int per_seq = slots / a.B;
@@ -441,19 +442,25 @@ cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, const ForkSelec
                     : launch_fork_t<bf16, float, 128>(a, node_states, sel, s);
 }
 
+cudaError_t launch_gdn_fork_materialize(const GdnArgs& a, void* node_states, const float* pseudo_v,
+                                        int max_ctas_per_sm, cudaStream_t s) {
+  const ForkSelect all{nullptr, 0.f, a.N, nullptr};
+  const int m = max_ctas_per_sm;
+  if (a.io == TV_F32 && a.state == TV_F32)
+    return a.dk == 64 ? launch_fork_t<float, float, 64, true>(a, node_states, all, s, pseudo_v, m)
+                      : launch_fork_t<float, float, 128, true>(a, node_states, all, s, pseudo_v, m);
+  if (a.io == TV_BF16 && a.state == TV_BF16)
+    return a.dk == 64 ? launch_fork_t<bf16, bf16, 64, true>(a, node_states, all, s, pseudo_v, m)
+                      : launch_fork_t<bf16, bf16, 128, true>(a, node_states, all, s, pseudo_v, m);
+  return a.dk == 64 ? launch_fork_t<bf16, float, 64, true>(a, node_states, all, s, pseudo_v, m)
+                    : launch_fork_t<bf16, float, 128, true>(a, node_states, all, s, pseudo_v, m);
+}
+
 cudaError_t launch_gdn_fork_two_pass(const GdnArgs& a, void* node_states, float* pseudo_v, float* log_gamma,
                                      cudaStream_t s) {
   cudaError_t e = launch_gdn_wy(a, pseudo_v, log_gamma, s);  // every output, and w
   if (e != cudaSuccess) return e;
-  const ForkSelect all{nullptr, 0.f, a.N, nullptr};
-  if (a.io == TV_F32 && a.state == TV_F32)
-    return a.dk == 64 ? launch_fork_t<float, float, 64, true>(a, node_states, all, s, pseudo_v)
-                      : launch_fork_t<float, float, 128, true>(a, node_states, all, s, pseudo_v);
-  if (a.io == TV_BF16 && a.state == TV_BF16)
-    return a.dk == 64 ? launch_fork_t<bf16, bf16, 64, true>(a, node_states, all, s, pseudo_v)
-                      : launch_fork_t<bf16, bf16, 128, true>(a, node_states, all, s, pseudo_v);
-  return a.dk == 64 ? launch_fork_t<bf16, float, 64, true>(a, node_states, all, s, pseudo_v)
-                    : launch_fork_t<bf16, float, 128, true>(a, node_states, all, s, pseudo_v);
+  return launch_gdn_fork_materialize(a, node_states, pseudo_v, 0, s);
 }
 
 }  // namespace tv
