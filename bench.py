@@ -624,9 +624,11 @@ def run_ours(args) -> None:
         e2e = {"value": whole_job_rate(rnd.B * rnd.N * rnd.layers * 2, world, e2e_ms), "unit": "nodes/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
-    selective = selective_fork_report(rnd, torch, tv)
-    lazy = lazy_commit_report(rnd, torch, tv)
-    one_pass = one_pass_fork_report(rnd, torch, tv)
+    selective = lazy = one_pass = None
+    if not args.no_reports:
+        selective = selective_fork_report(rnd, torch, tv)
+        lazy = lazy_commit_report(rnd, torch, tv)
+        one_pass = one_pass_fork_report(rnd, torch, tv)
     peaks = load_peaks()
     B, N, H, dk, dv = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv
     L_sum = int(rnd.gdn_host[0].path_len.sum())
@@ -720,6 +722,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-reports", action="store_true",
+                    help="skip the selective-fork, lazy-commit and one-pass-fork reports after the timed steps")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

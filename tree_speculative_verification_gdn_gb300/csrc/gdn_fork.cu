@@ -17,13 +17,16 @@
 // v prefetched into registers; the CTA's warps share one (sequence, head), so k and q come
 // from L1 after the first warp's read.
 //
-// Depth-first order visits a node's light children first and its heaviest child (largest
-// subtree) last.  A branching node pushes its state to a shared-memory slot that its later
-// children read back; the first child takes the state straight from registers.  With
-// heavy-last order a slot is at most 1 + (number of light edges above the node) and each
-// light edge halves the subtree, so slots 1..7 cover every tree of <= 256 nodes (a branching
-// node has >= 3 nodes in its subtree, so it sits below at most 6 light edges); the launch
-// sizes the stack for the bound of its N (slots_for).
+// Depth-first order visits a node's leaf children first, then its light children, and its
+// heaviest child (largest subtree) last.  A leaf's state only goes to its snapshot, so a leaf
+// is computed from the parent state in registers without replacing it; the first non-leaf
+// child then takes that state over.  A node with two or more non-leaf children pushes its
+// state to a shared-memory slot that the later ones read back.  With heavy-last order a slot
+// is at most 1 + (number of light edges above the node) and each light edge halves the
+// subtree, so slots 1..7 cover every tree of <= 256 nodes (a branching node has >= 3 nodes in
+// its subtree, so it sits below at most 6 light edges); the launch sizes the stack for the
+// bound of its N (slots_for).  On the k = 3, d = 3 tree an item makes 4 pushes and 8 pops
+// instead of one push per branching node and one pop per later child (13 and 26).
 #include "tv_common.cuh"
 #include "tv_internal.h"
 
@@ -44,6 +47,7 @@ struct Sched {
   int order[TV_MAX_NODES];   // node at each depth-first position
   int src[TV_MAX_NODES];     // where the parent state comes from: -1 registers, 0 S_0, else a slot
   int push[TV_MAX_NODES];    // slot the node's own state goes to (-1: not needed later)
+  int leaf[TV_MAX_NODES];    // 1: no children -- its state is stored, never kept in registers
   // per depth-first position t: {node, (src + 1) | (push + 1) << 8 | (snapshot slot + 1) << 16,
   // alpha bits, beta bits}
   int4 ent[TV_MAX_NODES];
@@ -57,7 +61,9 @@ struct BuildScratch {
   int size[TV_MAX_NODES];
   int nchild[TV_MAX_NODES];
   int hkey[TV_MAX_NODES];    // (size << 9) | (511 - child): heaviest child, lowest index on ties
-  int acc[TV_MAX_NODES];     // running offset of light children
+  int acc[TV_MAX_NODES];     // running offset of light non-leaf children
+  int nleaf[TV_MAX_NODES];   // leaf children
+  int acc_leaf[TV_MAX_NODES];  // running offset of leaf children
   int before[TV_MAX_NODES];  // nodes of earlier siblings' subtrees
   int pre[TV_MAX_NODES];     // depth-first position
   int slot[TV_MAX_NODES];    // snapshot slot of each node (selective fork), -1: none
@@ -72,7 +78,8 @@ __device__ int build_schedule(const int32_t* __restrict__ parents, int N, Sched&
   if (st) return st;
   if (tid == 0) { x.maxdepth = 0; x.root_acc = 0; s.maxslot = 0; }
   for (int i = tid; i < N; i += nt) {
-    x.size[i] = 1; x.nchild[i] = 0; x.hkey[i] = 0; x.acc[i] = 0; s.order[i] = -1;
+    x.size[i] = 1; x.nchild[i] = 0; x.hkey[i] = 0; x.acc[i] = 0; x.nleaf[i] = 0; x.acc_leaf[i] = 0;
+    s.order[i] = -1;
   }
   __syncthreads();
   for (int i = tid; i < N; i += nt) {
@@ -90,18 +97,24 @@ __device__ int build_schedule(const int32_t* __restrict__ parents, int N, Sched&
   }
   for (int i = tid; i < N; i += nt) {
     const int p = x.par[i];
-    if (p >= 0) atomicMax(&x.hkey[p], (x.size[i] << 9) | (511 - i));
+    if (p >= 0) {
+      atomicMax(&x.hkey[p], (x.size[i] << 9) | (511 - i));
+      if (x.nchild[i] == 0) atomicAdd(&x.nleaf[p], 1);
+    }
   }
   __syncthreads();
-  // Offset of each node among its siblings: light children in arbitrary (atomic) order,
-  // the heavy child after all of them; roots one after another.
+  // Offset of each node among its siblings: leaves first, then the light non-leaf children, in
+  // arbitrary (atomic) order, and the heavy child after all of them (a leaf heavy child, when
+  // every child is a leaf, counts as a leaf); roots one after another.
   for (int i = tid; i < N; i += nt) {
     const int p = x.par[i];
     if (p < 0) {
       x.before[i] = atomicAdd(&x.root_acc, x.size[i]);
+    } else if (x.nchild[i] == 0) {
+      x.before[i] = atomicAdd(&x.acc_leaf[p], 1);
     } else {
       const int heavy = 511 - (x.hkey[p] & 511);
-      x.before[i] = (i == heavy) ? x.size[p] - 1 - x.size[i] : atomicAdd(&x.acc[p], x.size[i]);
+      x.before[i] = (i == heavy) ? x.size[p] - 1 - x.size[i] : x.nleaf[p] + atomicAdd(&x.acc[p], x.size[i]);
     }
   }
   __syncthreads();
@@ -116,15 +129,22 @@ __device__ int build_schedule(const int32_t* __restrict__ parents, int N, Sched&
     x.pre[i] = pre;
     if (pre >= 0 && pre < N) s.order[pre] = i;
     else s.flag = 1;
-    const int slot = x.nchild[i] >= 2 ? 1 + light : -1;
+    // Leaves never disturb the parent state in registers, so a node saves its state only when
+    // a second non-leaf child will need it after the first one's subtree.
+    const int slot = x.nchild[i] - x.nleaf[i] >= 2 ? 1 + light : -1;
     s.push[i] = slot;
     if (slot > 0) atomicMax(&s.maxslot, slot);
   }
   __syncthreads();
   for (int i = tid; i < N; i += nt) {
     const int p = x.par[i];
-    s.src[i] = (p < 0) ? 0 : (x.pre[i] == x.pre[p] + 1 ? -1 : s.push[p]);
-    if (s.order[i] < 0 || s.src[i] > kSlots) s.flag = 1;  // never expected: guards every index
+    // A leaf, and the first non-leaf child (right after the leaves), find the parent state in
+    // registers; a later non-leaf child pops it.
+    const bool pops = p >= 0 && x.nchild[i] != 0 && x.pre[i] != x.pre[p] + 1 + x.nleaf[p];
+    s.src[i] = (p < 0) ? 0 : (pops ? s.push[p] : -1);
+    s.leaf[i] = x.nchild[i] == 0;
+    // never expected: guards every index
+    if (s.order[i] < 0 || s.src[i] > kSlots || (pops && s.push[p] <= 0)) s.flag = 1;
   }
   __syncthreads();
   return (s.maxslot <= kSlots && !s.flag) ? 0 : TV_ERR_UNSUPPORTED;
@@ -249,7 +269,8 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
 
   for (int t = tid; t < N; t += kThreads) {
     const int i = sc.order[t];
-    sc.ent[t] = make_int4(i, (sc.src[i] + 1) | ((sc.push[i] + 1) << 8) | ((scratch.slot[i] + 1) << 16), 0, 0);
+    sc.ent[t] = make_int4(i, (sc.src[i] + 1) | ((sc.push[i] + 1) << 8) | ((scratch.slot[i] + 1) << 16) |
+                                 (sc.leaf[i] << 28), 0, 0);
   }
   // Pulls one item's inputs into L2 ahead of use: alpha, beta, k and q of every node, the
   // slab's v rows and S_0 rows.  The node loop's register prefetch then waits on L2, not HBM.
@@ -329,7 +350,8 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     // with k.q from the per-item table.  Column pairs go through the paired fp32 FMA.
     auto body = [&](const Raw<TIO, CPL>& x) {
       const int i = x.e.x;
-      const int src = (x.e.y & 255) - 1, push = ((x.e.y >> 8) & 255) - 1, slot = (x.e.y >> 16) - 1;
+      const int src = (x.e.y & 255) - 1, push = ((x.e.y >> 8) & 255) - 1, slot = ((x.e.y >> 16) & 1023) - 1;
+      const bool leaf = (x.e.y >> 28) & 1;
       const float al = __int_as_float(x.e.z), be = __int_as_float(x.e.w);
       if (src == 0) {
         float f[CPL];
@@ -373,6 +395,21 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
         if (lane == 0) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * pq + w * x.kq) * q_scale);
       }
       const float2 al2 = make_float2(al, al), w2 = make_float2(w, w);
+      if (leaf) {
+        // A leaf's state only goes to its snapshot: cur keeps the parent state for the siblings.
+        if (slot >= 0) {
+          float f[CPL];
+#pragma unroll
+          for (int e = 0; e < CPL / 2; ++e) {
+            const float2 s2 = __ffma2_rn(w2, kf[e], __fmul2_rn(al2, cur[e]));
+            f[2 * e] = s2.x;
+            f[2 * e + 1] = s2.y;
+          }
+#pragma unroll
+          for (int j = 0; j < CPL / 8; ++j) store_vec_cs<8>(st_r + (size_t)slot * state_stride + j * kStride, f + 8 * j);
+        }
+        return;
+      }
 #pragma unroll
       for (int e = 0; e < CPL / 2; ++e) cur[e] = __ffma2_rn(w2, kf[e], __fmul2_rn(al2, cur[e]));
       {
