@@ -21,11 +21,12 @@
 // heaviest child (largest subtree) last.  A leaf's state only goes to its snapshot, so a leaf
 // is computed from the parent state in registers without replacing it; the first non-leaf
 // child then takes that state over.  A node with two or more non-leaf children pushes its
-// state to a shared-memory slot that the later ones read back.  With heavy-last order a slot
-// is at most 1 + (number of light edges above the node) and each light edge halves the
-// subtree, so slots 1..7 cover every tree of <= 256 nodes (a branching node has >= 3 nodes in
-// its subtree, so it sits below at most 6 light edges); the launch sizes the stack for the
-// bound of its N (slots_for).  On the k = 3, d = 3 tree an item makes 4 pushes and 8 pops
+// state to a shared-memory slot that the later ones read back.  With heavy-last order a node
+// pushes to slot 1 + (number of light edges above it); a pushing node has >= 5 nodes in its
+// subtree (two non-leaf children) and each light edge above it at least doubles that plus
+// one, so slot L + 1 needs a tree of >= g(L) nodes, g(0) = 5, g(L) = 2 g(L-1) + 1: slots
+// 1..6 cover every tree of <= 256 nodes and the launch sizes the stack for the bound of its N
+// (slots_for; 3 slots at N = 40).  On the k = 3, d = 3 tree an item makes 4 pushes and 8 pops
 // instead of one push per branching node and one pop per later child (13 and 26).
 #include "tv_common.cuh"
 #include "tv_internal.h"
@@ -36,7 +37,7 @@ namespace {
 constexpr int kLPR = 8;                 // lanes per state row
 constexpr int kRows = 16;               // state rows per CTA
 constexpr int kThreads = kLPR * kRows;  // 128
-constexpr int kSlots = 7;               // on-chip state slots 1..7 (S_0 is re-read for a root)
+constexpr int kSlots = 6;               // on-chip state slots 1..6 (S_0 is re-read for a root)
 // Column ownership: lane l of a row holds the chunks of 8 columns starting at l * 8 + j * kStride
 // (j = 0 .. CPL / 8 - 1), so one chunk-wide access by the 8 lanes of a row covers kStride
 // contiguous columns: full 32-byte sectors for every load and store of k, q, S_0 and states.
@@ -150,13 +151,14 @@ __device__ int build_schedule(const int32_t* __restrict__ parents, int N, Sched&
   return (s.maxslot <= kSlots && !s.flag) ? 0 : TV_ERR_UNSUPPORTED;
 }
 
-// Stack slots a tree of n nodes can need: a branching node below L light edges has at least
-// 2^(L+2) - 1 nodes in the tree, and it pushes to slot L + 1.
+// Stack slots a tree of n nodes can need: a pushing node below L light edges has at least
+// g(L) nodes in the tree (g(0) = 5, g(L) = 2 g(L-1) + 1), and it pushes to slot L + 1.
 __host__ __device__ constexpr int slots_for(int n) {
-  int L = 0;
-  while ((1 << (L + 3)) - 1 <= n) ++L;
+  int L = 0, g = 5;
+  while (2 * g + 1 <= n) { g = 2 * g + 1; ++L; }
   return L + 1;
 }
+static_assert(slots_for(TV_MAX_NODES) <= kSlots, "the stack bound covers every tree");
 
 // A node's inputs for one lane, as stored (bf16 pairs or fp32), prefetched into registers.
 template <typename TIO, int CPL>
