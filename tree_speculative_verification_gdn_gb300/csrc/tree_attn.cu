@@ -35,7 +35,10 @@ AttnPlan plan_attn(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int bs
   AttnPlan p;
   const long long slots = (long long)max_blocks * bs;
   const long long work = (long long)B * Hkv * slots;
-  long long chunk = (work + 2047) / 2048;        // ~2048 (sequence, KV head, chunk) items
+  // ~768 (sequence, KV head, chunk) items, about five per SM of a 152-SM GPU: longer chunks
+  // mean fewer CTA set-ups and partial rows to combine, shorter ones a smaller tail.  A fixed
+  // count keeps the workspace size a function of the sizes alone.
+  long long chunk = (work + 767) / 768;
   chunk = (chunk + 127) / 128 * 128;
   if (chunk < 128) chunk = 128;
   if (chunk > 8192) chunk = 8192;

@@ -102,6 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hi = min(total, lo + chunk);
   const int T = (hi - lo + KT - 1) / KT;
   const int G = a.Hq / a.Hkv, R = G * N;
+  // Softmax warps with at least one query row of this tile (rows r < active_rows); the others
+  // have nothing to compute and sit the tile loop out.
+  const int active_rows = G * max(0, min(npt, N - mt * npt));
+  const int active_warps = (active_rows + 31) / 32;
 
   if (tid == 0) {
     mbar_init(&bar.q_full, 1);
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar.s_full[s], 1);
-      mbar_init(&bar.p_full[s], kRows);
+      mbar_init(&bar.p_full[s], 32 * active_warps);
       mbar_init(&bar.pv_done[s], 1);
     }
     mbar_init(&bar.drain, 1);
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = tid;
     const int node = mt * npt + r / G, g = r % G;
     const bool active = (r < G * npt) && node < N;
+    const bool warp_idle = warp >= active_warps;
     uint32_t mb[TV_MAX_NODES / 32];
 #pragma unroll
     for (int w = 0; w < TV_MAX_NODES / 32; ++w) mb[w] = 0;
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float scale = a.sm_scale * kLog2e;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
+    for (int j = 0; j < T && !warp_idle; ++j) {
       const int st = j & 1;
       if (!__all_sync(0xffffffffu, wait_or_abort(&bar.s_full[st], (j >> 1) & 1, abort))) { ok = false; break; }
       tc_fence_after();
@@ -331,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int first = hi - base;
         unsigned char* v0 = sm + L::V0 + (j % kVStages) * L::KVB;
-        for (int idx = r; idx < (KT - first) * (HD / 8); idx += kRows) {
+        for (int idx = r; idx < (KT - first) * (HD / 8); idx += 32 * active_warps) {
           const int kr = first + idx / (HD / 8), rem = idx % (HD / 8);
           *reinterpret_cast<uint4*>(v0 + (rem / 8) * L::KVCHUNK + kr * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
         }
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bar.p_full[st]);
     }
-    if (ok && __all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort))) {
+    if (ok && !warp_idle && __all_sync(0xffffffffu, wait_or_abort(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort))) {
       tc_fence_after();
       const size_t row = (((size_t)b * a.Hkv + kvh) * nsplit + split) * R + (size_t)node * G + g;
 #pragma unroll 1
