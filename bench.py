@@ -35,6 +35,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 LAYERS = 24
+# w scratch slots of the fork mode's two passes: the TreeWY passes run up to this many layers
+# ahead of the snapshot passes (6 hides as much as 24 did in a sweep; 2 hid 15 us less per layer)
+FORK_SLOTS = 6
 METRIC = "tree-verified draft nodes/s per GDN layer; HBM GB/s & tensor util vs roofline"
 WORKLOAD = ("GDN stack: 24 GDN layers, B=64, N=40 (k=3 d=3), H=16, dk=dv=128, bf16, fork+commit and "
             "TreeWY+commit; paged attention: tree attention B=32, 16q/4kv, hd=256, paged P~U[2048,32768], N=40, "
@@ -256,13 +259,13 @@ class Round:
         ws = tv.tv_tree_attn_workspace_size(self.aB, self.aN, self.Hq, self.Hkv, self.hd, a.block_table.shape[1])
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.slot_map = torch.empty(a.path.shape, dtype=i32, device=dev)
-        # fork mode: the TreeWY pass of layer l writes w into slot l % 2, the snapshot pass of
-        # layer l reads it on the side stream while the next layer's TreeWY pass runs
+        # fork mode: the TreeWY pass of layer l writes w into slot l % FORK_SLOTS, the snapshot
+        # pass of layer l reads it on the side stream while the next layers' TreeWY passes run
         self.side = torch.cuda.Stream()
-        self.fork_pv = [torch.empty((B, N, H, dv), dtype=torch.float32, device=dev) for _ in range(2)]
-        self.fork_lg = [torch.empty((B, N, H), dtype=torch.float32, device=dev) for _ in range(2)]
+        self.fork_pv = [torch.empty((B, N, H, dv), dtype=torch.float32, device=dev) for _ in range(FORK_SLOTS)]
+        self.fork_lg = [torch.empty((B, N, H), dtype=torch.float32, device=dev) for _ in range(FORK_SLOTS)]
         self.w_ready = [torch.cuda.Event() for _ in range(layers)]
-        self.slot_free = [torch.cuda.Event() for _ in range(2)]
+        self.slot_free = [torch.cuda.Event() for _ in range(FORK_SLOTS)]
         self.new_len = torch.empty((self.aB,), dtype=i32, device=dev)
         self.rows = ["tree_prepare", "fork_verify", "fork_materialize", "accept_walk", "fork_commit", "wy_verify",
                      "wy_commit", "tree_attn", "kv_compact"]
@@ -296,9 +299,9 @@ class Round:
         f0 = timing_event(main)
         for l in range(self.layers):
             x = self.in_gdn[l]
-            slot = l % 2
-            if l >= 2:
-                main.wait_event(self.slot_free[slot])   # the snapshot pass of layer l - 2 has read it
+            slot = l % FORK_SLOTS
+            if l >= FORK_SLOTS:
+                main.wait_event(self.slot_free[slot])   # the snapshot pass that used it has read it
             tv.tv_gdn_tree_verify_wy(x["q"], x["k"], x["v"], x["alpha"], x["beta"], self.S0_fork[l], self.parents,
                                      self.o_fork[l], self.fork_pv[slot], self.fork_lg[slot], err[16 + l, :B])
             self.w_ready[l].record(main)
