@@ -26,14 +26,21 @@ constexpr int kPathCap = 4096;  // max sum over nodes of (depth + 1)
 constexpr int kBatch = 8;       // nodes per warp in flight during the solve
 constexpr uint32_t kTileA = kD * kD * 2;  // S_0 tile bytes
 
-// tcgen05.wait::ld with the 16 destination registers of the loads it waits for as operands:
+// tcgen05.wait::ld with the destination registers of the loads it waits for as operands:
 // every later use of them depends on the wait.
-__device__ __forceinline__ void tmem_wait_ld8x2(uint32_t* a, uint32_t* c) {
+__device__ __forceinline__ void tmem_wait_ld8(uint32_t* a) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
-                 "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3]), "+r"(c[4]), "+r"(c[5]), "+r"(c[6]), "+r"(c[7])
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7])
                :
                : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld16x2(uint32_t* a, uint32_t* c) {
+  tmem_wait_ld8(a);  // one wait covers every load issued so far; the others only tie registers
+  asm volatile("" : "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+               "+r"(a[15]));
+  asm volatile("" : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3]), "+r"(c[4]), "+r"(c[5]), "+r"(c[6]), "+r"(c[7]));
+  asm volatile("" : "+r"(c[8]), "+r"(c[9]), "+r"(c[10]), "+r"(c[11]), "+r"(c[12]), "+r"(c[13]), "+r"(c[14]),
+               "+r"(c[15]));
 }
 
 struct TcHead {
@@ -322,9 +329,15 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   __syncthreads();
 
   if (run && !hd.fail) {
-    // Forward substitution depth level by depth level: the nodes of one level depend only on
-    // shallower levels, so each warp takes kBatch of them at a time; the two warp groups split
-    // a level and meet at a barrier before the next.
+    // Thread (row r, warp group wg): r = TMEM lane.  First every node's MMA results leave TMEM
+    // 16 columns per load: a_i[r] = beta_i (v_i[r] - gamma_i (S_0 k_i)_r) into wsm, and, when it
+    // fits in the S_0 tile (free once the MMAs are done; N <= 64), b_i[r] = q_scale gamma_i
+    // (S_0 q_i)_r into bsm.  Then the forward substitution runs depth level by depth level:
+    // within a level every node is independent, so each warp takes kBatch of them at a time and
+    // walks their (equal-length) ancestor lists together, one read of each ancestor's w feeding
+    // both w_i = a_i - sum c_{i,t} w_t and o_i = b_i + sum e_{i,t} w_t; the two warp groups split
+    // a level and meet at a barrier before the next.  Without bsm, b_i comes from single-column
+    // TMEM loads requested one batch ahead.
     const bf16* __restrict__ v = static_cast<const bf16*>(a.v);
     bf16* __restrict__ out = static_cast<bf16*>(a.out);
     const int q = warp % 4, wg = warp / 4;
@@ -332,11 +345,35 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const float q_scale = a.q_scale;
     const int maxd = hd.maxdepth;
-    // The (S_0 k, S_0 q) columns are MMA results that the solve never changes, so each warp
-    // requests the next batch's columns before it computes the current one: the TMEM load
-    // latency hides behind a batch of work.  (ld_d, ld_base) is the next batch to request, in
-    // the order the loop below consumes them.
-    uint32_t nk[kBatch], nq[kBatch];
+    const bool use_bsm = (uint32_t)N * kD * 4 <= kTileA;
+    float* bsm = reinterpret_cast<float*>(sA);
+    for (int c = wg; c < Npad / 16; c += 2) {
+      uint32_t dk[16], dq[16];
+      tmem_ld16_nowait(tmem + lane_base + (uint32_t)(16 * c), dk);
+      if (use_bsm) tmem_ld16_nowait(tmem + lane_base + (uint32_t)(Npad + 16 * c), dq);
+      tmem_wait_ld16x2(dk, dq);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int i = 16 * c + u;
+        if (i < N) {
+          float vv;
+          if (v_in_smem) {  // v[i][r] from the swizzled V tile
+            const int cc = r % 64;
+            vv = to_f32(*(reinterpret_cast<const bf16*>(sV + (r / 64) * kq_bytes + i * 128 +
+                                                         (((cc / 8) ^ (i & 7)) << 4)) + (cc % 8)));
+          } else {
+            vv = to_f32(v[(((size_t)b * N + i) * H + h) * kD + r]);
+          }
+          const float gam = hd.gam[i];
+          wsm[i * kD + r] = hd.beta[i] * (vv - gam * __uint_as_float(dk[u]));
+          if (use_bsm) bsm[i * kD + r] = q_scale * gam * __uint_as_float(dq[u]);
+        }
+      }
+    }
+    __syncthreads();
+    // (ld_d, ld_base): the next batch whose (S_0 q) columns to request, in the order the loop
+    // below consumes them (only without bsm).
+    uint32_t nq[kBatch];
     int ld_d = 0, ld_base = wg * kBatch;
     auto request_next = [&]() {
       while (ld_d <= maxd && ld_base >= hd.lvl_cnt[ld_d]) {
@@ -349,51 +386,31 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
       for (int x = 0; x < kBatch; ++x) {
         const int pos = ld_base + x;
         const int col = pos < s1 ? hd.lvl_nodes[pos] : 0;
-        nk[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)col);
         nq[x] = tmem_ld1_nowait(tmem + lane_base + (uint32_t)(Npad + col));
       }
       ld_base += 2 * kBatch;
     };
-    request_next();
+    if (!use_bsm) request_next();
     for (int d = 0; d <= maxd; ++d) {
       const int s0 = d ? hd.lvl_cnt[d - 1] : 0, s1 = hd.lvl_cnt[d];
       for (int base = s0 + wg * kBatch; base < s1; base += 2 * kBatch) {
-        uint32_t dk[kBatch], dq[kBatch];
-        float vv[kBatch];
-        int nodes[kBatch];
-        tmem_wait_ld8x2(nk, nq);  // the wait names the registers, so no use moves above it
+        uint32_t dq[kBatch];
+        if (!use_bsm) {
+          tmem_wait_ld8(nq);  // the wait names the registers, so no use moves above it
 #pragma unroll
-        for (int x = 0; x < kBatch; ++x) {
-          dk[x] = nk[x];
-          dq[x] = nq[x];
+          for (int x = 0; x < kBatch; ++x) dq[x] = nq[x];
+          request_next();
         }
-        request_next();
+        float w[kBatch], ov[kBatch];
+        int nodes[kBatch], o[kBatch];
 #pragma unroll
         for (int x = 0; x < kBatch; ++x) {
           const int pos = base + x;
           nodes[x] = pos < s1 ? hd.lvl_nodes[pos] : -1;
-          const int col = nodes[x] < 0 ? 0 : nodes[x];
-          if (v_in_smem) {  // v[node][r] from the swizzled V tile
-            const int n = col, c = r % 64;
-            const bf16* p = reinterpret_cast<const bf16*>(sV + (r / 64) * kq_bytes + n * 128 +
-                                                          (((c / 8) ^ (n & 7)) << 4)) + (c % 8);
-            vv[x] = nodes[x] < 0 ? 0.f : to_f32(*p);
-          } else {
-            vv[x] = nodes[x] < 0 ? 0.f : to_f32(v[(((size_t)b * N + col) * H + h) * kD + r]);
-          }
-        }
-        // Every node of the level has depth d: walk the d ancestors of all kBatch nodes together
-        // (independent chains), accumulating both the solve and the ancestors' share of the output
-        // from one read of each ancestor's w.
-        float w[kBatch], ov[kBatch];
-        int o[kBatch];
-#pragma unroll
-        for (int x = 0; x < kBatch; ++x) {
           const int i = nodes[x] < 0 ? 0 : nodes[x];
-          const float gam = hd.gam[i];
           o[x] = hd.off[i];
-          w[x] = hd.beta[i] * (vv[x] - gam * __uint_as_float(dk[x]));
-          ov[x] = q_scale * gam * __uint_as_float(dq[x]);
+          w[x] = wsm[i * kD + r];
+          ov[x] = use_bsm ? bsm[i * kD + r] : q_scale * hd.gam[i] * __uint_as_float(dq[x]);
         }
         for (int t = 0; t < d; ++t) {
 #pragma unroll
