@@ -6,6 +6,7 @@
 // tv_gdn_tree_verify_wy: S_a = gamma_a S_0 + sum_{r<L} (gamma_a / gamma_{path[r]}) w_{path[r]}
 // k_{path[r]}^T, done in place on S_0 -- a rank-L update of a state that is read and written
 // once.
+#include "tv_async.cuh"
 #include "tv_common.cuh"
 #include "tv_internal.h"
 
@@ -50,37 +51,87 @@ __device__ int check_path(const CommitArgs& a, int b, PathCheck& pc) {
   return pc.status;
 }
 
-constexpr int kMaxVec = 16;  // 16-byte vectors per thread: a 128 x 128 fp32 tile over 256 threads
+constexpr int kForkThreads = 128;
 
-// One CTA per (sequence, head): copy the accepted checkpoint over S_0.  The tile is loaded into
-// registers from the node the (not yet checked) path names, clamped into [0, N), while the path
-// is being checked; it is stored only if the check passes, and then that node is the accepted
-// one.
-template <typename TS>
-__global__ void __launch_bounds__(kThreads) commit_fork_kernel(CommitArgs a) {
-  __shared__ PathCheck pc;
-  const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
-  const int L0 = a.path_len[b];
-  int guess = (L0 >= 1 && L0 <= a.Lmax) ? a.path[(size_t)b * a.Lmax + L0 - 1] : 0;
-  guess = guess < 0 ? 0 : (guess >= a.N ? a.N - 1 : guess);
-  const size_t tile = (size_t)a.dv * a.dk * sizeof(TS);  // bytes, a multiple of 16
-  const int nvec = (int)(tile / 16);                      // <= kMaxVec * kThreads
-  const uint4* src = reinterpret_cast<const uint4*>(
-      static_cast<const char*>(a.node_states) + ((((size_t)b * a.N + guess) * a.H + h) * tile));
-  uint4 buf[kMaxVec];
-#pragma unroll
-  for (int u = 0; u < kMaxVec; ++u) {
-    const int j = threadIdx.x + u * kThreads;
-    if (j < nvec) buf[u] = __ldg(src + j);
+// The first half of check_path: the path entries (clamped into [0, N)), its length (clamped
+// into [0, min(Lmax, N)]) and the parents land in shared memory; returns the clamped length.
+// The raw entries and length are kept for the check.
+__device__ int path_prefetch(const CommitArgs& a, int b, PathCheck& pc) {
+  const int cap = a.Lmax < a.N ? a.Lmax : a.N;
+  if (threadIdx.x == 0) pc.flag = 0;
+  for (int r = threadIdx.x; r < cap; r += blockDim.x) pc.path[r] = a.path[(size_t)b * a.Lmax + r];
+  for (int i = threadIdx.x; i < a.N; i += blockDim.x) pc.par[i] = a.parents[(size_t)b * a.N + i];
+  if (threadIdx.x == 0) pc.L = a.path_len[b];
+  __syncthreads();
+  const int L = pc.L;
+  return L < 0 ? 0 : (L > cap ? cap : L);
+}
+
+// The second half: the tree and the path in shared memory are checked as in check_path.  The
+// raw path entries are still there; the loads issued from them used clamped indices.
+__device__ int check_prefetched_path(const CommitArgs& a, int b, PathCheck& pc) {
+  const int cap = a.Lmax < a.N ? a.Lmax : a.N;
+  for (int i = threadIdx.x; i < a.N; i += blockDim.x) {
+    const int p = pc.par[i];
+    if (p < -1 || p >= i) pc.flag = 1;
   }
-  const int st = check_path(a, b, pc);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int st = pc.flag ? TV_ERR_BAD_TREE : 0;
+    if (!st) {
+      const int L = pc.L;
+      int ok = (L >= 1 && L <= cap);
+      int prev = -1;
+      for (int r = 0; ok && r < L; ++r) {
+        const int node = pc.path[r];
+        ok = (node >= 0 && node < a.N && pc.par[node] == prev);
+        prev = node;
+      }
+      st = ok ? 0 : TV_ERR_BAD_PATH;
+      pc.last = prev;
+    }
+    pc.status = st;
+  }
+  __syncthreads();
+  return pc.status;
+}
+
+// One CTA per (sequence, head): copy the accepted checkpoint over S_0.  Thread 0 starts a bulk
+// copy of the tile of the node the (not yet checked) path names, clamped into [0, N), into
+// shared memory while the CTA checks the path; the tile goes out to S_0 by a bulk store only if
+// the check passes, and then that node is the accepted one.
+template <typename TS>
+__global__ void __launch_bounds__(kForkThreads) commit_fork_kernel(CommitArgs a) {
+  __shared__ PathCheck pc;
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int guess_s;
+  extern __shared__ __align__(128) unsigned char tile_s[];
+  const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const uint32_t tile = (uint32_t)a.dv * a.dk * sizeof(TS);  // bytes, a multiple of 16
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    const int L0 = a.path_len[b];
+    int guess = (L0 >= 1 && L0 <= a.Lmax) ? a.path[(size_t)b * a.Lmax + L0 - 1] : 0;
+    guess = guess < 0 ? 0 : (guess >= a.N ? a.N - 1 : guess);
+    guess_s = guess;
+    mbar_arrive_expect_tx(&bar, tile);
+    bulk_g2s(tile_s, static_cast<const char*>(a.node_states) + (((size_t)b * a.N + guess) * a.H + h) * tile, tile,
+             &bar);
+  }
+  const int st = check_path(a, b, pc);  // its barriers also publish guess_s
   if (h == 0 && threadIdx.x == 0) a.err[b] = st;
-  if (st || pc.last != guess) return;  // pc.last == guess whenever the path is valid
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.S0) + ((size_t)b * a.H + h) * tile);
-#pragma unroll
-  for (int u = 0; u < kMaxVec; ++u) {
-    const int j = threadIdx.x + u * kThreads;
-    if (j < nvec) dst[j] = buf[u];
+  if (threadIdx.x == 0) {
+    // The copy must have landed before the tile is stored -- or before the CTA may exit.
+    const bool landed = mbar_wait(&bar, 0);
+    if (landed && !st && pc.last == guess_s) {  // pc.last == guess whenever the path is valid
+      bulk_s2g(static_cast<char*>(a.S0) + ((size_t)b * a.H + h) * tile, tile_s, tile);
+      bulk_commit();
+      bulk_wait_read<0>();
+    } else if (!landed) {
+      a.err[b] = TV_ERR_TIMEOUT;
+      mbar_wait(&bar, 0);
+    }
   }
 }
 
@@ -120,22 +171,30 @@ __global__ void __launch_bounds__(kThreads, 3) commit_wy_kernel(CommitArgs a) {
         for (int u = 0; u < VPC; ++u)
           raw[p][j][u] = reinterpret_cast<const uint4*>(s0 + (size_t)p * kRows * DK + j * kStride)[u];
 
-  const int st = check_path(a, b, pc);
+  // The path's log(gamma), w rows and keys are fetched from the unchecked path (its length and
+  // nodes clamped into range, so every read is in bounds) while the path is being checked; they
+  // are used only if the check passes, and then they are the path's.
+  const int Lu = path_prefetch(a, b, pc);
+  auto node_at = [&](int r) {  // the unchecked entry, clamped into [0, N)
+    const int n = pc.path[r];
+    return n < 0 ? 0 : (n >= N ? N - 1 : n);
+  };
+  for (int r = threadIdx.x; r < Lu; r += kThreads) coef[r] = a.log_gamma[((size_t)b * N + node_at(r)) * H + h];
+  for (int x = threadIdx.x; x < Lu * dv; x += kThreads) {
+    const int r = x / dv, rr = x % dv;
+    wsm[x] = a.pseudo_v[(((size_t)b * N + node_at(r)) * H + h) * dv + rr];
+  }
+  constexpr int KV = DK * (int)sizeof(TIO) / 16;  // 16-byte vectors per key
+  for (int x = threadIdx.x; x < Lu * KV; x += kThreads) {
+    const int r = x / KV, c = x % KV;
+    reinterpret_cast<uint4*>(ksm + (size_t)r * DK)[c] =
+        __ldg(reinterpret_cast<const uint4*>(static_cast<const TIO*>(a.k) + (((size_t)b * N + node_at(r)) * H + h) * DK) + c);
+  }
+  const int st = check_prefetched_path(a, b, pc);  // barriers inside
   if (h == 0 && threadIdx.x == 0) a.err[b] = st;
   if (st) return;
   const int L = pc.L;
-  if (threadIdx.x == 0) lga_s = a.log_gamma[((size_t)b * N + pc.last) * H + h];
-  for (int r = threadIdx.x; r < L; r += kThreads) coef[r] = a.log_gamma[((size_t)b * N + pc.path[r]) * H + h];
-  for (int x = threadIdx.x; x < L * dv; x += kThreads) {
-    const int r = x / dv, rr = x % dv;
-    wsm[x] = a.pseudo_v[(((size_t)b * N + pc.path[r]) * H + h) * dv + rr];
-  }
-  constexpr int KV = DK * (int)sizeof(TIO) / 16;  // 16-byte vectors per key
-  for (int x = threadIdx.x; x < L * KV; x += kThreads) {
-    const int r = x / KV, c = x % KV;
-    reinterpret_cast<uint4*>(ksm + (size_t)r * DK)[c] =
-        __ldg(reinterpret_cast<const uint4*>(static_cast<const TIO*>(a.k) + (((size_t)b * N + pc.path[r]) * H + h) * DK) + c);
-  }
+  if (threadIdx.x == 0) lga_s = coef[L - 1];
   __syncthreads();
   const float lga = lga_s;
   const float gam = expf(lga);
@@ -265,6 +324,16 @@ cudaError_t launch_replay_t(const CommitArgs& a, const ReplayArgs& r, cudaStream
   return cudaGetLastError();
 }
 
+template <typename TS>
+cudaError_t launch_fork_commit_t(const CommitArgs& a, cudaStream_t s) {
+  const size_t smem = (size_t)a.dv * a.dk * sizeof(TS);
+  auto kern = commit_fork_kernel<TS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<a.B * a.H, kForkThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename TIO, typename TS, int DK>
 cudaError_t launch_wy_t(const CommitArgs& a, cudaStream_t s) {
   const int cap = a.Lmax < a.N ? a.Lmax : a.N;  // a valid path has distinct nodes
@@ -289,11 +358,8 @@ cudaError_t launch_gdn_commit_replay(const CommitArgs& a, const ReplayArgs& r, c
 }
 
 cudaError_t launch_gdn_commit(const CommitArgs& a, cudaStream_t s) {
-  if (a.mode == TV_MODE_FORK) {
-    if (a.state == TV_F32) commit_fork_kernel<float><<<a.B * a.H, kThreads, 0, s>>>(a);
-    else commit_fork_kernel<bf16><<<a.B * a.H, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
-  }
+  if (a.mode == TV_MODE_FORK)
+    return a.state == TV_F32 ? launch_fork_commit_t<float>(a, s) : launch_fork_commit_t<bf16>(a, s);
   if (a.io == TV_F32 && a.state == TV_F32)
     return a.dk == 64 ? launch_wy_t<float, float, 64>(a, s) : launch_wy_t<float, float, 128>(a, s);
   if (a.io == TV_BF16 && a.state == TV_BF16)
