@@ -100,11 +100,19 @@ TV_API int tv_version(void);
  *   depth     [B, N] int32          out: depth of every node
  *   mask_bits [B, N, W] uint32      out: W = ceil(N / 32); bit (j % 32) of word j / 32 of row
  *                                   i is 1 iff node j is i or an ancestor of i
- *   err       [B] int32             out: 0 or TV_ERR_BAD_TREE
- * Outputs of a sequence whose tree is malformed are unspecified.
+ *   paths     [B, N, path_cap] int32  out, optional (NULL: not written): row i is the root-to-i
+ *                                   path (handbook §实现: the nodes a draft token's branch
+ *                                   passes through), root first, then -1 up to path_cap entries
+ *   path_cap  entries per path row, >= 1 when paths is given (depth + 1 entries are needed)
+ *   max_depth [B] int32             out, optional (NULL: not written): the deepest node's depth
+ *   err       [B] int32             out: 0, TV_ERR_BAD_TREE, or TV_ERR_UNSUPPORTED when a node's
+ *                                   depth + 1 exceeds path_cap (depth, mask_bits and max_depth
+ *                                   are still written; that sequence's paths are unspecified)
+ * Outputs of a sequence whose tree is malformed are unspecified.  Returns TV_ERR_INVALID_ARG for
+ * a null or misaligned required pointer, a misaligned optional one, or path_cap < 1 with paths.
  * ---------------------------------------------------------------------------------------- */
 TV_API int tv_tree_prepare(const int32_t* parents, int B, int N, int32_t* depth, uint32_t* mask_bits,
-                    int32_t* err, tv_stream_t stream);
+                           int32_t* paths, int path_cap, int32_t* max_depth, int32_t* err, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * tv_gdn_tree_verify_fork -- one GDN layer over B draft trees, fork/checkpoint mode.

@@ -72,15 +72,23 @@ def gdn_inputs(case: W.GDNCase) -> dict:
                 beta=to_dev(case.beta), S0=to_dev(case.S0), parents=to_dev(case.parents))
 
 
-def run_tree_prepare(parents: torch.Tensor) -> dict:
+def run_tree_prepare(parents: torch.Tensor, path_cap: int | None = None) -> dict:
+    """Depth and mask bits; with path_cap, also the root-to-node paths and the maximum depth."""
     B, N = parents.shape
     p = to_dev(parents)
     depth = torch.full((B, N), -7, dtype=torch.int32, device=DEV)
     bits = torch.zeros((B, N, (N + 31) // 32), dtype=torch.int32, device=DEV)
     err = _err(B)
-    tv.tv_tree_prepare(p, depth, bits, err)
+    paths = maxd = None
+    if path_cap is not None:
+        paths = torch.full((B, N, path_cap), 777, dtype=torch.int32, device=DEV)
+        maxd = torch.full((B,), 777, dtype=torch.int32, device=DEV)
+    tv.tv_tree_prepare(p, depth, bits, err, paths=paths, max_depth=maxd)
     torch.cuda.synchronize()
-    return dict(depth=depth.cpu(), mask_bits=bits.cpu().numpy().view(np.uint32), err=err.cpu())
+    r = dict(depth=depth.cpu(), mask_bits=bits.cpu().numpy().view(np.uint32), err=err.cpu())
+    if path_cap is not None:
+        r.update(paths=paths.cpu().numpy(), max_depth=maxd.cpu().numpy())
+    return r
 
 
 def run_fork(case: W.GDNCase, inputs: dict | None = None, keep_device: bool = False) -> dict:

@@ -56,7 +56,7 @@ def test_status_strings_and_version():
 
 def test_null_pointers_are_rejected_before_launch():
     L = tv.lib
-    assert L.tv_tree_prepare(None, 1, 4, None, None, None, None) == tv.TV_ERR_INVALID_ARG
+    assert L.tv_tree_prepare(None, 1, 4, None, None, None, 0, None, None, None) == tv.TV_ERR_INVALID_ARG
     args = [None] * 7 + [1, 7, 2, 64, 64, tv.TV_F32, tv.TV_F32, 1.0, None, None, None, None]
     assert L.tv_gdn_tree_verify_fork(*args) == tv.TV_ERR_INVALID_ARG
     args = [None] * 7 + [1, 7, 2, 64, 64, tv.TV_F32, tv.TV_F32, 1.0, None, None, None, None, None]

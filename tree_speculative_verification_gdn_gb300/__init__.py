@@ -54,7 +54,7 @@ _SIGNATURES = {
     "tv_status_string": (ctypes.c_char_p, [_I]),
     "tv_last_cuda_error": (_I, []),
     "tv_version": (_I, []),
-    "tv_tree_prepare": (_I, [_P, _I, _I, _P, _P, _P, _P]),
+    "tv_tree_prepare": (_I, [_P, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
     "tv_gdn_tree_verify_fork": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "tv_gdn_tree_verify_wy": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
     "tv_gdn_commit": (_I, [_I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
@@ -127,12 +127,14 @@ def status_string(status: int) -> str:
     return lib.tv_status_string(status).decode()
 
 
-def tv_tree_prepare(parents, depth, mask_bits, err, stream=None) -> None:
+def tv_tree_prepare(parents, depth, mask_bits, err, paths=None, max_depth=None, stream=None) -> None:
     """parents [B,N] int32 -> depth [B,N] int32, mask_bits [B,N,ceil(N/32)] int32 (bit pattern
-    of uint32 words), err [B] int32."""
+    of uint32 words), err [B] int32; optionally paths [B,N,cap] int32 (root-to-node, -1 padded)
+    and max_depth [B] int32."""
     B, N = parents.shape
-    _check(lib.tv_tree_prepare(_ptr(parents), B, N, _ptr(depth), _ptr(mask_bits), _ptr(err),
-                               _stream(stream)), "tv_tree_prepare")
+    cap = paths.shape[-1] if paths is not None else 0
+    _check(lib.tv_tree_prepare(_ptr(parents), B, N, _ptr(depth), _ptr(mask_bits), _ptr(paths), cap,
+                               _ptr(max_depth), _ptr(err), _stream(stream)), "tv_tree_prepare")
 
 
 def tv_gdn_tree_verify_fork(q, k, v, alpha, beta, S0, parents, out, node_states, err,

@@ -85,11 +85,14 @@ int tv_last_cuda_error(void) { return g_last_cuda; }
 
 int tv_version(void) { return 100; }
 
-int tv_tree_prepare(const int32_t* parents, int B, int N, int32_t* depth, uint32_t* mask_bits,
-                    int32_t* err, tv_stream_t stream) {
+int tv_tree_prepare(const int32_t* parents, int B, int N, int32_t* depth, uint32_t* mask_bits, int32_t* paths,
+                    int path_cap, int32_t* max_depth, int32_t* err, tv_stream_t stream) {
   if (!a4(parents) || !a4(depth) || !a4(mask_bits) || !a4(err) || B < 1 || N < 1) return TV_ERR_INVALID_ARG;
+  if ((paths != nullptr && (!a4(paths) || path_cap < 1)) || (max_depth != nullptr && !a4(max_depth)))
+    return TV_ERR_INVALID_ARG;
   if (N > TV_MAX_NODES) return TV_ERR_UNSUPPORTED;
-  return cuda_status(tv::launch_tree_prepare(parents, B, N, depth, mask_bits, err, stream));
+  return cuda_status(tv::launch_tree_prepare(parents, B, N, depth, mask_bits, paths, paths ? path_cap : 0, max_depth,
+                                             err, stream));
 }
 
 int tv_gdn_tree_verify_fork(const void* q, const void* k, const void* v, const float* alpha,

@@ -29,8 +29,8 @@ struct GdnArgs {
   int32_t* err;
 };
 
-cudaError_t launch_tree_prepare(const int32_t* parents, int B, int N, int32_t* depth,
-                                uint32_t* mask_bits, int32_t* err, cudaStream_t s);
+cudaError_t launch_tree_prepare(const int32_t* parents, int B, int N, int32_t* depth, uint32_t* mask_bits,
+                                int32_t* paths, int path_cap, int32_t* max_depth, int32_t* err, cudaStream_t s);
 
 // Selective fork: a node keeps its snapshot only if its confidence is at most the threshold;
 // kept snapshots take slots 0, 1, ... in node order.  confidence == nullptr: every node keeps
