@@ -749,6 +749,15 @@ def run_ours(args) -> None:
             "unit": "GB/s", "frac": rows[dom]["frac_hbm"], "traffic": kernel_traffic(dom),
             "peak_source": peaks["source"] + " (copy, burst)"}
     value = whole_job_rate(B * N * rnd.layers * 2, world, ms_per_step)
+    # accepted tokens per round (the device accept walk's path lengths) over the stack's verify
+    # and commit time, per mode
+    l_sum = int(rnd.path_len.sum())
+    stack_ms = {m: rnd.layers * (rows[f"{m}_verify"]["ms_per_call"] + rows[f"{m}_commit"]["ms_per_call"])
+                for m in ("fork", "wy")}
+    accepted = {"tokens_per_round": l_sum, "batch": B,
+                "fork_tokens_per_s": round(l_sum / (stack_ms["fork"] * 1e-3), 1),
+                "wy_tokens_per_s": round(l_sum / (stack_ms["wy"] * 1e-3), 1),
+                "stack_verify_commit_ms": {m: round(v, 4) for m, v in stack_ms.items()}}
     mem = {"fork_checkpoint_bytes": rnd.fork_state_bytes, "wy_pseudo_value_bytes": rnd.wy_state_bytes,
            "pages_bytes_per_checkpoint": checkpoint_bytes(24, 16, 128, 128, 2),
            "pages_accounting_fork_bytes": checkpoint_bytes(24, 16, 128, 128, 2) * B * N,
@@ -762,7 +771,8 @@ def run_ours(args) -> None:
                        "l2": "working set >> 129 MB L2 (fork checkpoints 1.3 GB per layer)",
                        "parallelism": f"replicas x{world}"},
             "gpu_launches": rnd.launches_per_step * args.steps, "clocks": clk, "roofline": roof,
-            "rows": rows, "state_memory": mem, "selective_fork": selective, "lazy_commit": lazy,
+            "rows": rows, "accepted_tokens": accepted, "state_memory": mem, "selective_fork": selective,
+            "lazy_commit": lazy,
             "one_pass_fork": one_pass, "e2e": e2e,
             "cpu_baseline": cpu_base}
     if rank == 0:

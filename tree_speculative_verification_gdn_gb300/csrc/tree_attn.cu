@@ -267,30 +267,63 @@ __global__ void __launch_bounds__(kPartialThreads) attn_partial_simt_kernel(Attn
   }
 }
 
-// One CTA per (sequence, node, query head); one thread per head dim.
-__global__ void attn_combine_kernel(AttnArgs a, const float* __restrict__ ml, const float* __restrict__ acc,
-                                    int chunk, int nsplit) {
-  const int h = blockIdx.x % a.Hq;
-  const int i = (blockIdx.x / a.Hq) % a.N;
-  const int b = blockIdx.x / (a.Hq * a.N);
+// One CTA per (sequence, node).  Thread h < Hq first forms query head h's running max M and
+// normaliser l over the key chunks; then the CTA merges the chunks' unnormalised outputs four
+// head dims (16 bytes) per thread at a time: o = sum_s 2^(m_s - M) acc_s / l.
+constexpr int kCombineThreads = 256;
+
+__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(AttnArgs a, const float* __restrict__ ml,
+                                                                       const float* __restrict__ acc, int chunk,
+                                                                       int nsplit) {
+  extern __shared__ float head_ml[];  // [Hq] max, then [Hq] normaliser
+  const int i = blockIdx.x % a.N;
+  const int b = blockIdx.x / a.N;
   if (a.err[b]) return;
-  const int G = a.Hq / a.Hkv, R = G * a.N, kvh = h / G, rr = i * G + h % G;
+  const int Hq = a.Hq, hd = a.hd;
+  const int G = Hq / a.Hkv, R = G * a.N;
   const int total = a.prefix_len[b] + a.N;
   const int nsp = (total + chunk - 1) / chunk;
-  const size_t base = ((size_t)b * a.Hkv + kvh) * nsplit;
-  float M = -INFINITY;
-  for (int s = 0; s < nsp; ++s) M = fmaxf(M, ml[((base + s) * R + rr) * 2]);
-  const int d = threadIdx.x;
-  float lsum = 0.f, o = 0.f;
-  for (int s = 0; s < nsp; ++s) {
-    const size_t row = (base + s) * R + rr;
-    const float ms = ml[row * 2];
-    if (ms == -INFINITY) continue;
-    const float wgt = exp2f(ms - M);
-    lsum = fmaf(ml[row * 2 + 1], wgt, lsum);
-    o = fmaf(acc[row * a.hd + d], wgt, o);
+  auto row_of = [&](int h, int s) {  // partial row of (sequence b, node i, query head h) in chunk s
+    return (((size_t)b * a.Hkv + h / G) * nsplit + s) * R + (size_t)i * G + h % G;
+  };
+  for (int h = threadIdx.x; h < Hq; h += blockDim.x) {
+    float M = -INFINITY;
+    for (int s = 0; s < nsp; ++s) M = fmaxf(M, ml[row_of(h, s) * 2]);
+    float lsum = 0.f;
+    for (int s = 0; s < nsp; ++s) {
+      const size_t row = row_of(h, s);
+      const float ms = ml[row * 2];
+      if (ms == -INFINITY) continue;
+      lsum = fmaf(ml[row * 2 + 1], exp2f(ms - M), lsum);
+    }
+    head_ml[h] = M;
+    head_ml[Hq + h] = lsum;
   }
-  static_cast<bf16*>(a.out)[(((size_t)b * a.N + i) * a.Hq + h) * a.hd + d] = from_f32<bf16>(o / lsum);
+  __syncthreads();
+  const int v4 = hd / 4;
+  bf16* out = static_cast<bf16*>(a.out) + ((size_t)b * a.N + i) * Hq * hd;
+  for (int x = threadIdx.x; x < Hq * v4; x += blockDim.x) {
+    const int h = x / v4, c = (x % v4) * 4;
+    const float M = head_ml[h];
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < nsp; ++s) {
+      const size_t row = row_of(h, s);
+      const float ms = ml[row * 2];
+      if (ms == -INFINITY) continue;
+      const float wgt = exp2f(ms - M);
+      const float4 p = *reinterpret_cast<const float4*>(acc + row * hd + c);
+      o.x = fmaf(p.x, wgt, o.x);
+      o.y = fmaf(p.y, wgt, o.y);
+      o.z = fmaf(p.z, wgt, o.z);
+      o.w = fmaf(p.w, wgt, o.w);
+    }
+    const float lsum = head_ml[Hq + h];
+    bf16* dst = out + (size_t)h * hd + c;
+    dst[0] = from_f32<bf16>(o.x / lsum);
+    dst[1] = from_f32<bf16>(o.y / lsum);
+    dst[2] = from_f32<bf16>(o.z / lsum);
+    dst[3] = from_f32<bf16>(o.w / lsum);
+  }
 }
 
 template <int HD>
@@ -329,9 +362,9 @@ cudaError_t launch_tree_attn(const AttnArgs& a, void* workspace, size_t workspac
   else if (a.hd == 128) e = launch_partial<128>(a, p, ws, s);
   else e = launch_partial<256>(a, p, ws, s);
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<a.B * a.N * a.Hq, a.hd, 0, s>>>(a, reinterpret_cast<const float*>(ws + p.off_ml),
-                                                        reinterpret_cast<const float*>(ws + p.off_acc),
-                                                        p.chunk, p.nsplit);
+  attn_combine_kernel<<<a.B * a.N, kCombineThreads, 2 * a.Hq * sizeof(float), s>>>(
+      a, reinterpret_cast<const float*>(ws + p.off_ml), reinterpret_cast<const float*>(ws + p.off_acc), p.chunk,
+      p.nsplit);
   return cudaGetLastError();
 }
 
