@@ -530,7 +530,9 @@ def selective_fork_report(rnd, torch, tv, iters: int = 3) -> dict:
     """Fork mode with selective snapshots (qwen35-tree-spec §六, 选择性 Fork) on the same 24-layer
     stack, timed apart from the step: nodes with draft confidence above 0.95 keep no snapshot
     (synthetic confidences, about half of the nodes above the threshold), and the commit
-    replays from the deepest kept snapshot of the accepted path."""
+    replays from the deepest kept snapshot of the accepted path.  Verify runs in the step's
+    two-pass schedule (TreeWY passes on this stream, selective snapshot passes on the side
+    stream, six w slots); the one-pass selective kernel is timed too."""
     import numpy as np
     B, N, H, dk, dv, L = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv, rnd.layers
     rng = np.random.default_rng(99)
@@ -538,38 +540,63 @@ def selective_fork_report(rnd, torch, tv, iters: int = 3) -> dict:
     conf_np = np.where(high, rng.uniform(0.951, 1.0, (B, N)), rng.uniform(0.0, 0.95, (B, N))).astype(np.float32)
     kept = int((conf_np <= 0.95).sum(axis=1).max())
     conf = torch.from_numpy(conf_np).to(rnd.dev)
-    states = torch.empty((B, kept, H, dv, dk), dtype=torch.bfloat16, device=rnd.dev)
-    slot = torch.empty((B, N), dtype=torch.int32, device=rnd.dev)
+    states = [torch.empty((B, kept, H, dv, dk), dtype=torch.bfloat16, device=rnd.dev) for _ in range(L)]
+    slot = [torch.empty((B, N), dtype=torch.int32, device=rnd.dev) for _ in range(L)]
     S0 = [s.clone() for s in rnd.S0_fork]
     out = torch.empty_like(rnd.o_fork[0])
-    err = torch.zeros((2, B), dtype=torch.int32, device=rnd.dev)
+    err = torch.zeros((L + 2, B), dtype=torch.int32, device=rnd.dev)
+    main, side = torch.cuda.current_stream(), rnd.side
+    ev = torch.cuda.Event
 
-    def once(ev=None):
+    def two_pass():
         for l in range(L):
             x = rnd.in_gdn[l]
-            s, m, e = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            s.record()
+            k = l % FORK_SLOTS
+            if l >= FORK_SLOTS:
+                main.wait_event(rnd.slot_free[k])
+            tv.tv_gdn_tree_verify_wy(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S0[l], rnd.parents, out,
+                                     rnd.fork_pv[k], rnd.fork_lg[k], err[l])
+            rnd.w_ready[l].record(main)
+            side.wait_event(rnd.w_ready[l])
+            tv.tv_gdn_fork_materialize_selective(x["k"], x["alpha"], S0[l], rnd.parents, rnd.fork_pv[k], conf, 0.95,
+                                                 states[l], slot[l], err[l], stream=side)
+            rnd.slot_free[k].record(side)
+        main.wait_stream(side)
+
+    def commits():
+        for l in range(L):
+            x = rnd.in_gdn[l]
+            tv.tv_gdn_commit_selective(rnd.path, rnd.path_len, rnd.parents, states[l], slot[l], x["k"], x["v"],
+                                       x["alpha"], x["beta"], S0[l], err[L])
+
+    def one_pass():
+        for l in range(L):
+            x = rnd.in_gdn[l]
             tv.tv_gdn_tree_verify_fork_selective(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S0[l], rnd.parents,
-                                                 conf, 0.95, out, states, slot, err[0])
-            m.record()
-            tv.tv_gdn_commit_selective(rnd.path, rnd.path_len, rnd.parents, states, slot, x["k"], x["v"], x["alpha"],
-                                       x["beta"], S0[l], err[1])
-            e.record()
-            if ev is not None:
-                ev.append((s, m, e))
-    once()
-    torch.cuda.synchronize()
-    ev = []
-    for _ in range(iters):
-        once(ev)
-    torch.cuda.synchronize()
+                                                 conf, 0.95, out, states[l], slot[l], err[L + 1])
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(iters):
+            s_, e_ = ev(enable_timing=True), ev(enable_timing=True)
+            s_.record(main)
+            fn()
+            e_.record(main)
+            torch.cuda.synchronize()
+            t.append(s_.elapsed_time(e_) / L)
+        return sum(t) / len(t)
+
+    v_ms = timed(two_pass)
+    c_ms = timed(commits)       # after a verify: its snapshots and slots are in place
+    p_ms = timed(one_pass)
     assert int(err.abs().sum()) == 0, err
-    v_ms = sum(s.elapsed_time(m) for s, m, _ in ev) / len(ev)
-    c_ms = sum(m.elapsed_time(e) for _, m, e in ev) / len(ev)
     full = B * N * H * dv * dk * 2
     return {"threshold": 0.95, "kept_fraction": round(float((conf_np <= 0.95).mean()), 4),
             "snapshot_bytes_per_layer": B * kept * H * dv * dk * 2, "full_checkpoint_bytes_per_layer": full,
-            "verify_ms_per_layer": round(v_ms, 5), "commit_ms_per_layer": round(c_ms, 5)}
+            "verify_ms_per_layer": round(v_ms, 5), "commit_ms_per_layer": round(c_ms, 5),
+            "one_pass_verify_ms_per_layer": round(p_ms, 5)}
 
 
 def one_pass_fork_report(rnd, torch, tv, iters: int = 3) -> dict:

@@ -277,6 +277,22 @@ TV_API int tv_gdn_fork_materialize(const void* k, const float* alpha, const void
                                    int state_dtype, int max_ctas_per_sm, void* node_states, int32_t* err,
                                    tv_stream_t stream);
 
+/* tv_gdn_fork_materialize_selective -- the same pass keeping only the selected snapshots
+ * (qwen35-tree-spec §六, 选择性 Fork): node i keeps its snapshot iff confidence[b][i] <=
+ * threshold, at slot s of node_states [B, capacity, H, dv, dk], slots numbered in node order,
+ * exactly as tv_gdn_tree_verify_fork_selective; its outputs come from the preceding
+ * tv_gdn_tree_verify_wy.  slot [B, N] int32 out (-1: no snapshot).  A sequence that keeps
+ * more than capacity snapshots reports TV_ERR_CAPACITY in err and keeps none; a sequence the
+ * verify rejected (err != 0 on entry) keeps none either (all its slots -1).  The commit is
+ * tv_gdn_commit_selective.  Argument errors as tv_gdn_fork_materialize, plus a null
+ * confidence or slot, a non-finite threshold, or capacity outside [1, N]. */
+TV_API int tv_gdn_fork_materialize_selective(const void* k, const float* alpha, const void* S0,
+                                             const int32_t* parents, const float* pseudo_v,
+                                             const float* confidence, float threshold, int capacity, int B,
+                                             int N, int H, int dk, int dv, int io_dtype, int state_dtype,
+                                             int max_ctas_per_sm, void* node_states, int32_t* slot, int32_t* err,
+                                             tv_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------
  * tv_gdn_tree_verify_fork_selective / tv_gdn_commit_selective -- fork mode with selective
  * snapshots.

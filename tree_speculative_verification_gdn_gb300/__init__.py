@@ -43,7 +43,7 @@ EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_pre
             "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact",
             "tv_accept_walk", "tv_gdn_tree_verify_fork_selective", "tv_gdn_commit_selective",
             "tv_gdn_tree_verify_wy_lazy", "tv_gdn_fork_workspace_size", "tv_gdn_tree_verify_fork_ws",
-            "tv_gdn_fork_materialize")
+            "tv_gdn_fork_materialize", "tv_gdn_fork_materialize_selective")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -73,6 +73,8 @@ _SIGNATURES = {
     "tv_gdn_tree_verify_fork_ws": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _Z,
                                        _P, _P]),
     "tv_gdn_fork_materialize": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "tv_gdn_fork_materialize_selective": (_I, [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                               _P, _P, _P, _P]),
     "tv_accept_walk": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
 }
@@ -171,6 +173,18 @@ def tv_gdn_fork_materialize(k, alpha, S0, parents, pseudo_v, node_states, err, m
         _ptr(k), _ptr(alpha), _ptr(S0), _ptr(parents), _ptr(pseudo_v), B, N, H, dk, dv, _DTYPES[k.dtype],
         _DTYPES[S0.dtype], int(max_ctas_per_sm), _ptr(node_states), _ptr(err), _stream(stream)),
         "tv_gdn_fork_materialize")
+
+
+def tv_gdn_fork_materialize_selective(k, alpha, S0, parents, pseudo_v, confidence, threshold: float, node_states,
+                                      slot, err, max_ctas_per_sm: int = 0, stream=None) -> None:
+    """The selected fork-mode snapshots (confidence <= threshold) from the w of a preceding
+    tv_gdn_tree_verify_wy: node_states [B, capacity, H, dv, dk], slot [B, N] int32."""
+    B, N, H, dk = k.shape
+    dv = pseudo_v.shape[-1]
+    _check(lib.tv_gdn_fork_materialize_selective(
+        _ptr(k), _ptr(alpha), _ptr(S0), _ptr(parents), _ptr(pseudo_v), _ptr(confidence), float(threshold),
+        node_states.shape[1], B, N, H, dk, dv, _DTYPES[k.dtype], _DTYPES[S0.dtype], int(max_ctas_per_sm),
+        _ptr(node_states), _ptr(slot), _ptr(err), _stream(stream)), "tv_gdn_fork_materialize_selective")
 
 
 def tv_gdn_tree_verify_fork_selective(q, k, v, alpha, beta, S0, parents, confidence, threshold: float, out,

@@ -228,7 +228,11 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
   const int b = blockIdx.x / ctas_per_seq, g = blockIdx.x % ctas_per_seq;
   const int N = a.N, H = a.H, dv = a.dv;
   const int tid = threadIdx.x;
-  if (FROM_W && a.err[b] != 0) return;  // the TreeWY pass rejected this sequence
+  if (FROM_W && a.err[b] != 0) {  // the TreeWY pass rejected this sequence: it keeps no snapshot
+    if (g == 0 && sel.slot != nullptr)
+      for (int i = tid; i < N; i += kThreads) sel.slot[(size_t)b * N + i] = -1;
+    return;
+  }
   int status = build_schedule(a.parents + (size_t)b * N, N, sc, scratch);
   if (!status && sc.maxslot > nslots) status = TV_ERR_UNSUPPORTED;
   // Snapshot slots (selective fork): nodes at or below the confidence threshold, numbered in
@@ -482,8 +486,7 @@ cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, const ForkSelec
 }
 
 cudaError_t launch_gdn_fork_materialize(const GdnArgs& a, void* node_states, const float* pseudo_v,
-                                        int max_ctas_per_sm, cudaStream_t s) {
-  const ForkSelect all{nullptr, 0.f, a.N, nullptr};
+                                        const ForkSelect& all, int max_ctas_per_sm, cudaStream_t s) {
   const int m = max_ctas_per_sm;
   if (a.io == TV_F32 && a.state == TV_F32)
     return a.dk == 64 ? launch_fork_t<float, float, 64, true>(a, node_states, all, s, pseudo_v, m)
@@ -499,7 +502,8 @@ cudaError_t launch_gdn_fork_two_pass(const GdnArgs& a, void* node_states, float*
                                      cudaStream_t s) {
   cudaError_t e = launch_gdn_wy(a, pseudo_v, log_gamma, s);  // every output, and w
   if (e != cudaSuccess) return e;
-  return launch_gdn_fork_materialize(a, node_states, pseudo_v, 0, s);
+  const ForkSelect all{nullptr, 0.f, a.N, nullptr};
+  return launch_gdn_fork_materialize(a, node_states, pseudo_v, all, 0, s);
 }
 
 }  // namespace tv

@@ -144,7 +144,27 @@ int tv_gdn_fork_materialize(const void* k, const float* alpha, const void* S0, c
   // q, v, beta and out are not read by this pass.
   tv::GdnArgs a{nullptr, k, nullptr, alpha, nullptr, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, 1.f,
                 nullptr, err};
-  return cuda_status(tv::launch_gdn_fork_materialize(a, node_states, pseudo_v, max_ctas_per_sm, stream));
+  const tv::ForkSelect all{nullptr, 0.f, N, nullptr};
+  return cuda_status(tv::launch_gdn_fork_materialize(a, node_states, pseudo_v, all, max_ctas_per_sm, stream));
+}
+
+int tv_gdn_fork_materialize_selective(const void* k, const float* alpha, const void* S0, const int32_t* parents,
+                                      const float* pseudo_v, const float* confidence, float threshold, int capacity,
+                                      int B, int N, int H, int dk, int dv, int io_dtype, int state_dtype,
+                                      int max_ctas_per_sm, void* node_states, int32_t* slot, int32_t* err,
+                                      tv_stream_t stream) {
+  if (!a16(k) || !a4(alpha) || !a16(S0) || !a4(parents) || !a16(pseudo_v) || !a16(node_states) || !a4(err) ||
+      !a4(confidence) || !a4(slot))
+    return TV_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || H < 1 || max_ctas_per_sm < 0 || !isfinite(threshold) || capacity < 1 || capacity > N)
+    return TV_ERR_INVALID_ARG;
+  if (N > TV_MAX_NODES || !dim_ok(dk) || !dim_ok(dv)) return TV_ERR_UNSUPPORTED;
+  const int st = gdn_dtypes(io_dtype, state_dtype);
+  if (st != TV_OK) return st;
+  tv::GdnArgs a{nullptr, k, nullptr, alpha, nullptr, S0, parents, B, N, H, dk, dv, io_dtype, state_dtype, 1.f,
+                nullptr, err};
+  const tv::ForkSelect sel{confidence, threshold, capacity, slot};
+  return cuda_status(tv::launch_gdn_fork_materialize(a, node_states, pseudo_v, sel, max_ctas_per_sm, stream));
 }
 
 int tv_gdn_tree_verify_fork_selective(const void* q, const void* k, const void* v, const float* alpha,

@@ -46,10 +46,11 @@ cudaError_t launch_gdn_fork(const GdnArgs& a, void* node_states, const ForkSelec
 // then the walk materializes every snapshot from its parent's, S_i = alpha_i S_p + w_i k_i^T.
 cudaError_t launch_gdn_fork_two_pass(const GdnArgs& a, void* node_states, float* pseudo_v, float* log_gamma,
                                      cudaStream_t s);
-// The second pass alone (after a TreeWY verify of the same inputs wrote pseudo_v and err); at
-// most max_ctas_per_sm resident CTAs per SM when > 0.
+// The second pass alone (after a TreeWY verify of the same inputs wrote pseudo_v and err), every
+// snapshot or (sel.confidence set) the selected ones; at most max_ctas_per_sm resident CTAs per
+// SM when > 0.
 cudaError_t launch_gdn_fork_materialize(const GdnArgs& a, void* node_states, const float* pseudo_v,
-                                        int max_ctas_per_sm, cudaStream_t s);
+                                        const ForkSelect& sel, int max_ctas_per_sm, cudaStream_t s);
 
 // TreeWY verify: tcgen05 kernel for bf16 I/O and state with dk = dv = 128, CUDA-core kernel
 // for every other supported shape.
