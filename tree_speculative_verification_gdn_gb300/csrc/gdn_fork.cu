@@ -228,12 +228,10 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
   const int b = blockIdx.x / ctas_per_seq, g = blockIdx.x % ctas_per_seq;
   const int N = a.N, H = a.H, dv = a.dv;
   const int tid = threadIdx.x;
-  if (FROM_W && a.err[b] != 0) {  // the TreeWY pass rejected this sequence: it keeps no snapshot
-    if (g == 0 && sel.slot != nullptr)
-      for (int i = tid; i < N; i += kThreads) sel.slot[(size_t)b * N + i] = -1;
-    return;
-  }
-  int status = build_schedule(a.parents + (size_t)b * N, N, sc, scratch);
+  // A sequence the TreeWY pass rejected keeps its status and no snapshot (its slots go to -1
+  // below when selecting).
+  const int prior = FROM_W ? a.err[b] : 0;
+  int status = prior ? prior : build_schedule(a.parents + (size_t)b * N, N, sc, scratch);
   if (!status && sc.maxslot > nslots) status = TV_ERR_UNSUPPORTED;
   // Snapshot slots (selective fork): nodes at or below the confidence threshold, numbered in
   // node order by one warp's ballot scan; otherwise slot = node.

@@ -149,31 +149,49 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   bf16* lz_k = reinterpret_cast<bf16*>(lz_w + kLazyMaxLen * kD);      // [L][128]
   const bool lazy = lz.path != nullptr;
   if (lazy) {
-    if (tid == 0) {
-      const int L = lz.len[b];
-      int ok = L >= 1 && L <= lz.Lmax && L <= lz.Np && L <= kLazyMaxLen, prev = -1;
-      for (int r = 0; ok && r < L; ++r) {
-        const int node = lz.path[(size_t)b * lz.Lmax + r];
-        ok = node >= 0 && node < lz.Np && lz.parents[(size_t)b * lz.Np + node] == prev;
-        if (ok) lz_nodes[r] = node;
-        prev = node;
+    // Every thread stages its rows of the path's w and keys from the unchecked entries, clamped
+    // into range so every read is in bounds, while warp 0 checks the path, one entry per lane:
+    // node in range, its parent the previous entry (-1 for the first).  The rows are used only
+    // if the check passes, and then they are the path's.
+    const int Lraw = lz.len[b];
+    const int Lc = Lraw < 0 ? 0 : min(Lraw, min(kLazyMaxLen, min(lz.Lmax, lz.Np)));
+    for (int x = tid; x < Lc * kD; x += kThreads) {
+      const int e = lz.path[(size_t)b * lz.Lmax + x / kD];
+      const int node = e < 0 ? 0 : (e >= lz.Np ? lz.Np - 1 : e);
+      const size_t nh = ((size_t)b * lz.Np + node) * H + h;
+      lz_w[x] = lz.pseudo_v[nh * kD + x % kD];
+      lz_k[x] = static_cast<const bf16*>(lz.k)[nh * kD + x % kD];
+    }
+    if (warp == 0) {
+      const bool len_ok = Lraw >= 1 && Lraw <= lz.Lmax && Lraw <= lz.Np && Lraw <= kLazyMaxLen;
+      int node = -1, pn = -1;
+      float lgt = 0.f;
+      if (len_ok && lane < Lraw) {
+        node = lz.path[(size_t)b * lz.Lmax + lane];
+        if (node >= 0 && node < lz.Np) {
+          pn = lz.parents[(size_t)b * lz.Np + node];
+          lgt = lz.log_gamma[((size_t)b * lz.Np + node) * H + h];
+        }
       }
-      lz_L = ok ? L : 0;
-      lz_status = ok ? 0 : TV_ERR_BAD_PATH;
-      if (ok) lz_lga = lz.log_gamma[((size_t)b * lz.Np + prev) * H + h];
+      int prev = __shfl_up_sync(0xffffffffu, node, 1);
+      if (lane == 0) prev = -1;
+      const bool mine = lane >= Lraw || (node >= 0 && node < lz.Np && pn == prev);
+      const bool ok = len_ok && __all_sync(0xffffffffu, mine);
+      const float lga = __shfl_sync(0xffffffffu, lgt, ok ? Lraw - 1 : 0);
+      if (ok && lane < Lraw) {
+        lz_nodes[lane] = node;
+        lz_g[lane] = lgt;  // log(gamma) of the entry for now; the ratio below
+      }
+      if (lane == 0) {
+        lz_L = ok ? Lraw : 0;
+        lz_status = ok ? 0 : TV_ERR_BAD_PATH;
+        lz_lga = lga;
+      }
     }
     __syncthreads();
     if (!status) status = lz_status;
-    if (!status) {
-      const int L = lz_L;
-      for (int x = tid; x < L * kD; x += kThreads) {
-        const size_t nh = ((size_t)b * lz.Np + lz_nodes[x / kD]) * H + h;
-        lz_w[x] = lz.pseudo_v[nh * kD + x % kD];
-        lz_k[x] = static_cast<const bf16*>(lz.k)[nh * kD + x % kD];
-      }
-      for (int t = tid; t < L; t += kThreads)
-        lz_g[t] = expf(lz_lga - lz.log_gamma[((size_t)b * lz.Np + lz_nodes[t]) * H + h]);
-    }
+    if (!status)
+      for (int t = tid; t < lz_L; t += kThreads) lz_g[t] = expf(lz_lga - lz_g[t]);
   }
   if (!status) {
     for (int i = tid; i < N; i += kThreads) {
