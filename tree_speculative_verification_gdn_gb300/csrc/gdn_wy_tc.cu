@@ -67,6 +67,9 @@ struct TcHead {
 static_assert(sizeof(TcHead) % 16 == 0, "the path-entry table after the head is 16-byte aligned");
 static_assert(TV_MAX_NODES <= kThreads, "one node per thread in the prologue");
 
+// LAZY: the previous round's commit is applied to S_0 first (lz); a separate instantiation, so
+// the plain kernel keeps its own register allocation.
+template <bool LAZY>
 __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* __restrict__ pseudo_v,
                                                              float* __restrict__ log_gamma, int cap, int Npad,
                                                              uint32_t tmem_cols, int v_in_smem,
@@ -147,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   int& lz_status = hd.lz_status;
   float* lz_w = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(pent + cap) + 15) & ~uintptr_t(15));  // [L][128]
   bf16* lz_k = reinterpret_cast<bf16*>(lz_w + kLazyMaxLen * kD);      // [L][128]
-  const bool lazy = lz.path != nullptr;
+  constexpr bool lazy = LAZY;
   if (lazy) {
     // Every thread stages its rows of the path's w and keys from the unchecked entries, clamped
     // into range so every read is in bounds, while warp 0 checks the path, one entry per lane:
@@ -257,26 +260,35 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
     // S_0 <- gamma_a S_0 + sum_t (gamma_a / gamma_t) w_t k_t^T on the swizzled tile, in the
     // operation order of the commit kernel; the committed state also goes back to HBM.
     // Thread (row, half) takes the 64 columns of one k-block of one row.
+    // All 64 columns stay in registers while the path entries stream past, each entry's
+    // coefficient formed once; every element still sees gamma_a first, then the entries in order.
     const int row = tid >> 1, kb = tid & 1, L = lz_L;
     const float gam = expf(lz_lga);
     unsigned char* rowp = sA + kb * (kTileA / 2) + row * 128;
     uint4* g = reinterpret_cast<uint4*>(static_cast<bf16*>(const_cast<void*>(a.S0)) +
                                         (((size_t)b * H + h) * kD + row) * kD + kb * 64);
+    float x[8][8];
+#pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
-      uint4* sp = reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4));
-      float x[8];
-      unpack8(*sp, x);
+      unpack8(*reinterpret_cast<const uint4*>(rowp + ((ch ^ (row & 7)) << 4)), x[ch]);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] *= gam;
-      for (int t = 0; t < L; ++t) {
-        const float c = lz_g[t] * lz_w[t * kD + row];
+      for (int e = 0; e < 8; ++e) x[ch][e] *= gam;
+    }
+    for (int t = 0; t < L; ++t) {
+      const float c = lz_g[t] * lz_w[t * kD + row];
+      const uint4* kr = reinterpret_cast<const uint4*>(lz_k + t * kD + kb * 64);
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
         float kf[8];
-        unpack8(*reinterpret_cast<const uint4*>(lz_k + t * kD + kb * 64 + ch * 8), kf);
+        unpack8(kr[ch], kf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = fmaf(c, kf[e], x[e]);
+        for (int e = 0; e < 8; ++e) x[ch][e] = fmaf(c, kf[e], x[ch][e]);
       }
-      const uint4 pk = pack8(x);
-      *sp = pk;
+    }
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      const uint4 pk = pack8(x[ch]);
+      *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4)) = pk;
       g[ch] = pk;
     }
     fence_proxy_async();  // the MMA reads the tile through the async proxy
@@ -490,7 +502,7 @@ cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma
   const size_t base = 1024 + kTileA + (size_t)4 * Npad * 128 + sizeof(TcHead) + (size_t)cap * 12 + lazy_bytes;
   const int v_in_smem = base + (size_t)2 * Npad * 128 <= 227 * 1024;
   size_t smem = base + (v_in_smem ? (size_t)2 * Npad * 128 : 0);
-  auto kern = gdn_wy_tc_kernel;
+  auto kern = lz.path != nullptr ? gdn_wy_tc_kernel<true> : gdn_wy_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   if (e != cudaSuccess) return e;
   // TMEM: the CTAs resident on one SM must fit in its 512 columns; pad shared memory if needed.
