@@ -217,8 +217,11 @@ class Round:
         def d(t):
             return t.contiguous().to(dev)
 
-        # per-round inputs (copied from host in the end-to-end measurement)
-        self.in_gdn = [dict(q=d(c.q), k=d(c.k), v=d(c.v), alpha=d(c.alpha), beta=d(c.beta)) for c in self.gdn_host]
+        # per-round inputs (copied from host in the end-to-end measurement); every layer's keys lie
+        # in one [layers, B, N, H, dk] tensor, which the stack's TreeWY commit reads in one launch
+        self.k_all = torch.stack([c.k for c in self.gdn_host]).contiguous().to(dev)
+        self.in_gdn = [dict(q=d(c.q), k=self.k_all[l], v=d(c.v), alpha=d(c.alpha), beta=d(c.beta))
+                       for l, c in enumerate(self.gdn_host)]
         self.parents = d(c0.parents)
         # draft and target tokens under which the on-device accept walk takes the sampled paths
         draft, target = W.walk_tokens(c0.trees, c0.path.numpy(), c0.path_len.numpy(), seed=seed + 1)
@@ -227,20 +230,26 @@ class Round:
                             prefix_len=d(a.prefix_len), parents=d(a.parents))
         draft, target = W.walk_tokens(a.trees, a.path.numpy(), a.path_len.numpy(), seed=seed + 2)
         self.a_tokens = dict(draft=d(draft), target=d(target))
-        # resident state
-        self.S0_fork = [d(c.S0) for c in self.gdn_host]
-        self.S0_wy = [d(c.S0) for c in self.gdn_host]
+        # resident state, each mode's layers back to back ([layers, B, H, dv, dk]) so that one launch
+        # commits the stack; S0_fork[l] / S0_wy[l] are views of layer l
+        self.S0_fork_all = torch.stack([c.S0 for c in self.gdn_host]).contiguous().to(dev)
+        self.S0_wy_all = self.S0_fork_all.clone()
+        self.S0_fork = [self.S0_fork_all[l] for l in range(layers)]
+        self.S0_wy = [self.S0_wy_all[l] for l in range(layers)]
         self.k_cache, self.v_cache = d(a.k_cache), d(a.v_cache)
         # outputs
         bf = torch.bfloat16
         self.o_fork = [torch.empty((B, N, H, dv), dtype=bf, device=dev) for _ in range(layers)]
         self.o_wy = [torch.empty((B, N, H, dv), dtype=bf, device=dev) for _ in range(layers)]
         mem0 = torch.cuda.memory_allocated()
-        self.states = [torch.empty((B, N, H, dv, dk), dtype=bf, device=dev) for _ in range(layers)]
+        self.states_all = torch.empty((layers, B, N, H, dv, dk), dtype=bf, device=dev)
+        self.states = [self.states_all[l] for l in range(layers)]
         self.fork_state_bytes = torch.cuda.memory_allocated() - mem0
         mem0 = torch.cuda.memory_allocated()
-        self.pv = [torch.empty((B, N, H, dv), dtype=torch.float32, device=dev) for _ in range(layers)]
-        self.lg = [torch.empty((B, N, H), dtype=torch.float32, device=dev) for _ in range(layers)]
+        self.pv_all = torch.empty((layers, B, N, H, dv), dtype=torch.float32, device=dev)
+        self.lg_all = torch.empty((layers, B, N, H), dtype=torch.float32, device=dev)
+        self.pv = [self.pv_all[l] for l in range(layers)]
+        self.lg = [self.lg_all[l] for l in range(layers)]
         self.wy_state_bytes = torch.cuda.memory_allocated() - mem0
         i32 = torch.int32
         # accepted paths: written by the accept walk each round, read by the commits / compaction
@@ -269,7 +278,9 @@ class Round:
         self.new_len = torch.empty((self.aB,), dtype=i32, device=dev)
         self.rows = ["tree_prepare", "fork_verify", "fork_materialize", "accept_walk", "fork_commit", "wy_verify",
                      "wy_commit", "tree_attn", "kv_compact"]
-        self.launches_per_step = 1 + layers * 5 + 4 + 1 + 2   # the fork verify is two launches
+        # tree prepare; per layer the fork's two passes and the TreeWY verify; one commit launch per
+        # mode for the whole stack; two accept walks; four attention kernels; the compaction
+        self.launches_per_step = 1 + layers * 3 + 2 + 2 + 4 + 1
 
     def step(self, ev=None, io=None):
         """One verify round.  ``ev``: optional dict row -> list of (start, end, calls) entries.
@@ -288,12 +299,12 @@ class Round:
             e.record(stream)
             return e
 
-        def mark(row, fn, stream=None):
+        def mark(row, fn, stream=None, calls=1):
             st = main if stream is None else stream
             s = timing_event(st)
             fn()
             if ev is not None:
-                ev[row].append((s, timing_event(st), 1))
+                ev[row].append((s, timing_event(st), calls))
 
         mark("tree_prepare", lambda: tv.tv_tree_prepare(self.parents, self.depth, self.mask, err[0, :B]))
         # Fork mode in two passes: the TreeWY pass (every output, and w) on this stream, then the
@@ -324,10 +335,10 @@ class Round:
         mark("accept_walk", lambda: tv.tv_accept_walk(
             self.parents, self.tokens["draft"], self.tokens["target"], self.path, self.path_len, self.next_tok,
             err[7, :B]))
-        for l in range(self.layers):
-            mark("fork_commit", lambda: tv.tv_gdn_commit(
-                tv.TV_MODE_FORK, self.path, self.path_len, self.parents, self.S0_fork[l], err[2, :B],
-                node_states=self.states[l]))
+        # every layer commits the accepted paths at once: one launch for the stack
+        mark("fork_commit", lambda: tv.tv_gdn_commit_layers(
+            tv.TV_MODE_FORK, self.path, self.path_len, self.parents, self.S0_fork_all, err[2, :B],
+            node_states=self.states_all), calls=self.layers)
         for l in range(self.layers):
             x = self.in_gdn[l]
             mark("wy_verify", lambda: tv.tv_gdn_tree_verify_wy(
@@ -335,13 +346,12 @@ class Round:
                 self.pv[l], self.lg[l], err[3, :B]))
             if io is not None:
                 io.output(main, "wy", l)
-        for l in range(self.layers):
-            x = self.in_gdn[l]
-            mark("wy_commit", lambda: tv.tv_gdn_commit(
-                tv.TV_MODE_WY, self.path, self.path_len, self.parents, self.S0_wy[l], err[4, :B],
-                pseudo_v=self.pv[l], log_gamma=self.lg[l], k=x["k"]))
-            if io is not None:
-                io.layer_done(main, l)   # the last reader of this layer's inputs has been issued
+        mark("wy_commit", lambda: tv.tv_gdn_commit_layers(
+            tv.TV_MODE_WY, self.path, self.path_len, self.parents, self.S0_wy_all, err[4, :B],
+            pseudo_v=self.pv_all, log_gamma=self.lg_all, k=self.k_all), calls=self.layers)
+        if io is not None:
+            for l in range(self.layers):
+                io.layer_done(main, l)   # the last reader of the layers' inputs has been issued
         a = self.in_attn
         aB = self.aB
         if io is not None:

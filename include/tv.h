@@ -226,6 +226,19 @@ TV_API int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* 
                   const float* log_gamma, const void* k, void* S0, int B, int N, int H, int dk,
                   int dv, int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream);
 
+/* tv_gdn_commit_layers -- the commit of a whole stack of independent layers in one launch.
+ * Every layer commits the same accepted paths (the path, its length and the parents are shared),
+ * once the target has accepted them; the per-layer tensors lie back to back, layer first:
+ *   S0 [layers, B, H, dv, dk]; fork: node_states [layers, B, N, H, dv, dk]; TreeWY:
+ *   pseudo_v [layers, B, N, H, dv], log_gamma [layers, B, N, H], k [layers, B, N, H, dk].
+ * The result for each layer equals tv_gdn_commit on that layer's slices.  err [B] reports the
+ * shared path check.  layers >= 1; layers * B * H must fit in an int.  The pages have no
+ * counterpart: layers are independent at commit time, so one launch serves them all. */
+TV_API int tv_gdn_commit_layers(int mode, const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,
+                                const int32_t* parents, const void* node_states, const float* pseudo_v,
+                                const float* log_gamma, const void* k, void* S0, int layers, int B, int N, int H,
+                                int dk, int dv, int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------
  * tv_gdn_tree_verify_fork_ws -- fork mode in two passes, with a workspace.
  *

@@ -236,3 +236,29 @@ def test_host_side_argument_errors():
         tv.tv_gdn_tree_verify_fork(q96, q96, x["v"], x["alpha"], x["beta"], x["S0"], x["parents"], out, st,
                                    err)
     assert e.value.status == tv.TV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("mode", ["fork", "wy"])
+def test_commit_of_a_layer_stack_in_one_launch_equals_per_layer_commits(mode):
+    # Three independent layers sharing the trees and the accepted paths: tv_gdn_commit_layers on
+    # the stacked tensors gives each layer's tv_gdn_commit result, bit for bit.
+    cases = [W.stack_b64_layer(layer=l, B=8) for l in range(3)]
+    c0 = cases[0]
+    runs = [(_gpu.run_fork(c, keep_device=True) if mode == "fork" else _gpu.run_wy(c)) for c in cases]
+    want = [_gpu.run_commit(c, mode, r, path=c0.path, path_len=c0.path_len) for c, r in zip(cases, runs)]
+    S0 = torch.stack([r["inputs"]["S0"] for r in runs]).contiguous()
+    err = torch.full((c0.shape[0],), 777, dtype=torch.int32, device="cuda:0")
+    path, plen = _gpu.to_dev(c0.path), _gpu.to_dev(c0.path_len)
+    parents = runs[0]["inputs"]["parents"]
+    if mode == "fork":
+        states = torch.stack([r["states"] for r in runs]).contiguous()
+        tv.tv_gdn_commit_layers(tv.TV_MODE_FORK, path, plen, parents, S0, err, node_states=states)
+    else:
+        pv = torch.stack([r["pv_dev"] for r in runs]).contiguous()
+        lg = torch.stack([r["lg_dev"] for r in runs]).contiguous()
+        k = torch.stack([r["inputs"]["k"] for r in runs]).contiguous()
+        tv.tv_gdn_commit_layers(tv.TV_MODE_WY, path, plen, parents, S0, err, pseudo_v=pv, log_gamma=lg, k=k)
+    torch.cuda.synchronize()
+    assert (err.cpu() == 0).all()
+    for l in range(3):
+        assert torch.equal(S0[l].cpu(), want[l])

@@ -43,7 +43,7 @@ EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_pre
             "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact",
             "tv_accept_walk", "tv_gdn_tree_verify_fork_selective", "tv_gdn_commit_selective",
             "tv_gdn_tree_verify_wy_lazy", "tv_gdn_fork_workspace_size", "tv_gdn_tree_verify_fork_ws",
-            "tv_gdn_fork_materialize", "tv_gdn_fork_materialize_selective")
+            "tv_gdn_fork_materialize", "tv_gdn_fork_materialize_selective", "tv_gdn_commit_layers")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -58,6 +58,7 @@ _SIGNATURES = {
     "tv_gdn_tree_verify_fork": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "tv_gdn_tree_verify_wy": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P]),
     "tv_gdn_commit": (_I, [_I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "tv_gdn_commit_layers": (_I, [_I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P]),
     "tv_tree_attn_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "tv_tree_attn": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _P, _P, _Z,
                           _P, _P]),
@@ -247,6 +248,21 @@ def tv_gdn_commit(mode: int, accepted_path, accepted_len, parents, S0, err, *, n
         int(mode), _ptr(accepted_path), _ptr(accepted_len), Lmax, _ptr(parents), _ptr(node_states),
         _ptr(pseudo_v), _ptr(log_gamma), _ptr(k), _ptr(S0), B, N, H, dk, dv, io, _DTYPES[S0.dtype],
         _ptr(err), _stream(stream)), "tv_gdn_commit")
+
+
+def tv_gdn_commit_layers(mode: int, accepted_path, accepted_len, parents, S0, err, *, node_states=None,
+                         pseudo_v=None, log_gamma=None, k=None, io_dtype=None, N=None, stream=None) -> None:
+    """One launch commits every layer: S0 [layers, B, H, dv, dk] and the mode's per-layer tensors
+    with a leading layer dimension; path, lengths, parents and err are shared by the layers."""
+    layers, B, H, dv, dk = S0.shape
+    Lmax = accepted_path.shape[1]
+    N = parents.shape[1] if N is None else N
+    io = _DTYPES[k.dtype] if k is not None else (_DTYPES[io_dtype] if io_dtype is not None else
+                                                  _DTYPES[S0.dtype])
+    _check(lib.tv_gdn_commit_layers(
+        int(mode), _ptr(accepted_path), _ptr(accepted_len), Lmax, _ptr(parents), _ptr(node_states),
+        _ptr(pseudo_v), _ptr(log_gamma), _ptr(k), _ptr(S0), layers, B, N, H, dk, dv, io, _DTYPES[S0.dtype],
+        _ptr(err), _stream(stream)), "tv_gdn_commit_layers")
 
 
 def tv_tree_attn_workspace_size(B, N, Hq, Hkv, hd, max_blocks, block_size=TV_BLOCK_SIZE) -> int:

@@ -51,6 +51,20 @@ __device__ int check_path(const CommitArgs& a, int b, PathCheck& pc) {
   return pc.status;
 }
 
+// The per-layer view of a multi-layer commit: CTA blockIdx.x takes layer blockIdx.x / (B H) of
+// (sequence, head) blockIdx.x % (B H).
+__device__ __forceinline__ CommitArgs layer_view(const CommitArgs& a, int layer) {
+  CommitArgs v = a;
+  const size_t es = a.state == TV_F32 ? 4 : 2, eio = a.io == TV_F32 ? 4 : 2;
+  const size_t bnh = (size_t)a.B * a.N * a.H;
+  v.S0 = static_cast<char*>(a.S0) + layer * (size_t)a.B * a.H * a.dv * a.dk * es;
+  if (a.node_states) v.node_states = static_cast<const char*>(a.node_states) + layer * bnh * a.dv * a.dk * es;
+  if (a.pseudo_v) v.pseudo_v = a.pseudo_v + layer * bnh * a.dv;
+  if (a.log_gamma) v.log_gamma = a.log_gamma + layer * bnh;
+  if (a.k) v.k = static_cast<const char*>(a.k) + layer * bnh * a.dk * eio;
+  return v;
+}
+
 constexpr int kForkThreads = 128;
 
 // The first half of check_path: the path entries (clamped into [0, N)), its length (clamped
@@ -101,12 +115,14 @@ __device__ int check_prefetched_path(const CommitArgs& a, int b, PathCheck& pc) 
 // shared memory while the CTA checks the path; the tile goes out to S_0 by a bulk store only if
 // the check passes, and then that node is the accepted one.
 template <typename TS>
-__global__ void __launch_bounds__(kForkThreads) commit_fork_kernel(CommitArgs a) {
+__global__ void __launch_bounds__(kForkThreads) commit_fork_kernel(CommitArgs a0) {
   __shared__ PathCheck pc;
   __shared__ __align__(8) uint64_t bar;
   __shared__ int guess_s;
   extern __shared__ __align__(128) unsigned char tile_s[];
-  const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int layer = blockIdx.x / (a0.B * a0.H), bh = blockIdx.x % (a0.B * a0.H);
+  const CommitArgs a = layer_view(a0, layer);
+  const int b = bh / a.H, h = bh % a.H;
   const uint32_t tile = (uint32_t)a.dv * a.dk * sizeof(TS);  // bytes, a multiple of 16
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -120,7 +136,7 @@ __global__ void __launch_bounds__(kForkThreads) commit_fork_kernel(CommitArgs a)
              &bar);
   }
   const int st = check_path(a, b, pc);  // its barriers also publish guess_s
-  if (h == 0 && threadIdx.x == 0) a.err[b] = st;
+  if (layer == 0 && h == 0 && threadIdx.x == 0) a.err[b] = st;
   if (threadIdx.x == 0) {
     // The copy must have landed before the tile is stored -- or before the CTA may exit.
     const bool landed = mbar_wait(&bar, 0);
@@ -143,15 +159,17 @@ constexpr int kStride = 8 * kLPR;  // lane l holds columns l * 8 + j * kStride .
 // owns rows rl, rl + 32, ... of the head.  All of them are loaded before the path check; the
 // path's log(gamma), w rows and keys are then fetched in one phase into shared memory.
 template <typename TIO, typename TS, int DK>
-__global__ void __launch_bounds__(kThreads, 3) commit_wy_kernel(CommitArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) commit_wy_kernel(CommitArgs a0) {
   constexpr int CPL = DK / kLPR;
   __shared__ PathCheck pc;
   __shared__ float coef[TV_MAX_NODES];
   __shared__ float lga_s;
   extern __shared__ __align__(16) unsigned char dyn[];  // w [cap][dv] fp32, then k [cap][DK]
   constexpr int P = 4;                 // passes of 32 rows: dv <= 128
+  const int layer = blockIdx.x / (a0.B * a0.H), bh = blockIdx.x % (a0.B * a0.H);
+  const CommitArgs a = layer_view(a0, layer);
   const int passes = a.dv / kRows;
-  const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int b = bh / a.H, h = bh % a.H;
   const int N = a.N, H = a.H, dv = a.dv;
   const int cap = a.Lmax < N ? a.Lmax : N;
   float* wsm = reinterpret_cast<float*>(dyn);
@@ -191,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 3) commit_wy_kernel(CommitArgs a) {
         __ldg(reinterpret_cast<const uint4*>(static_cast<const TIO*>(a.k) + (((size_t)b * N + node_at(r)) * H + h) * DK) + c);
   }
   const int st = check_prefetched_path(a, b, pc);  // barriers inside
-  if (h == 0 && threadIdx.x == 0) a.err[b] = st;
+  if (layer == 0 && h == 0 && threadIdx.x == 0) a.err[b] = st;
   if (st) return;
   const int L = pc.L;
   if (threadIdx.x == 0) lga_s = coef[L - 1];
@@ -330,7 +348,7 @@ cudaError_t launch_fork_commit_t(const CommitArgs& a, cudaStream_t s) {
   auto kern = commit_fork_kernel<TS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<a.B * a.H, kForkThreads, smem, s>>>(a);
+  kern<<<a.layers * a.B * a.H, kForkThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -343,7 +361,7 @@ cudaError_t launch_wy_t(const CommitArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<a.B * a.H, kThreads, smem, s>>>(a);
+  kern<<<a.layers * a.B * a.H, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -216,12 +216,13 @@ int tv_gdn_tree_verify_wy_lazy(const int32_t* prev_path, const int32_t* prev_len
   return cuda_status(tv::launch_gdn_wy_tc(a, pseudo_v, log_gamma, lz, stream));
 }
 
-int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,
-                  const int32_t* parents, const void* node_states, const float* pseudo_v,
-                  const float* log_gamma, const void* k, void* S0, int B, int N, int H, int dk, int dv,
-                  int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream) {
+int tv_gdn_commit_layers(int mode, const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,
+                         const int32_t* parents, const void* node_states, const float* pseudo_v,
+                         const float* log_gamma, const void* k, void* S0, int layers, int B, int N, int H, int dk,
+                         int dv, int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream) {
   if (!a4(accepted_path) || !a4(accepted_len) || !a4(parents) || !a16(S0) || !a4(err)) return TV_ERR_INVALID_ARG;
-  if (B < 1 || N < 1 || H < 1 || Lmax < 1) return TV_ERR_INVALID_ARG;
+  if (layers < 1 || B < 1 || N < 1 || H < 1 || Lmax < 1) return TV_ERR_INVALID_ARG;
+  if ((long long)layers * B * H > 0x7fffffffLL) return TV_ERR_UNSUPPORTED;
   if (mode == TV_MODE_FORK) {
     if (!a16(node_states)) return TV_ERR_INVALID_ARG;
   } else if (mode == TV_MODE_WY) {
@@ -234,7 +235,18 @@ int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* accepte
   if (st != TV_OK) return st;
   tv::CommitArgs a{mode, accepted_path, accepted_len, Lmax, parents, node_states, pseudo_v, log_gamma, k,
                    S0, B, N, H, dk, dv, io_dtype, state_dtype, err};
+  a.layers = layers;
+  if (mode == TV_MODE_FORK) a.pseudo_v = nullptr, a.log_gamma = nullptr, a.k = nullptr;
+  else a.node_states = nullptr;
   return cuda_status(tv::launch_gdn_commit(a, stream));
+}
+
+int tv_gdn_commit(int mode, const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,
+                  const int32_t* parents, const void* node_states, const float* pseudo_v,
+                  const float* log_gamma, const void* k, void* S0, int B, int N, int H, int dk, int dv,
+                  int io_dtype, int state_dtype, int32_t* err, tv_stream_t stream) {
+  return tv_gdn_commit_layers(mode, accepted_path, accepted_len, Lmax, parents, node_states, pseudo_v, log_gamma, k,
+                              S0, 1, B, N, H, dk, dv, io_dtype, state_dtype, err, stream);
 }
 
 int tv_gdn_commit_selective(const int32_t* accepted_path, const int32_t* accepted_len, int Lmax,

@@ -87,6 +87,8 @@ struct CommitArgs {
   void* S0;
   int B, N, H, dk, dv, io, state;
   int32_t* err;
+  int layers = 1;  // S0, node_states, pseudo_v, log_gamma, k: [layers, B, ...] back to back; the
+                   // path, its length, parents and err are shared by the layers
 };
 cudaError_t launch_gdn_commit(const CommitArgs& a, cudaStream_t s);
 // Commit after a selective fork: resume from the deepest accepted node that kept a snapshot
