@@ -420,8 +420,61 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
       }
       ld_base += 2 * kBatch;
     };
+    if (use_bsm) {
+      // Thread (row pair, group): rows r0 and r0 + 64 (the walk reads shared memory only, so a
+      // thread's rows need not be its TMEM lane), node group g of 4 splitting each level; each
+      // per-node load serves both rows.
+      const int r0 = tid & 63, g = tid >> 6;
+      bf16* __restrict__ outb = out + ((size_t)b * N * H + h) * kD;
+      float* __restrict__ pvb = pseudo_v + ((size_t)b * N * H + h) * kD;
+      for (int d = 0; d <= maxd; ++d) {
+        const int s0 = d ? hd.lvl_cnt[d - 1] : 0, s1 = hd.lvl_cnt[d];
+        for (int base = s0 + g * kBatch; base < s1; base += 4 * kBatch) {
+          float w0[kBatch], w1[kBatch], ov0[kBatch], ov1[kBatch];
+          int nodes[kBatch], o[kBatch];
+#pragma unroll
+          for (int x = 0; x < kBatch; ++x) {
+            const int pos = base + x;
+            nodes[x] = pos < s1 ? hd.lvl_nodes[pos] : -1;
+            const int i = nodes[x] < 0 ? 0 : nodes[x];
+            o[x] = hd.off[i];
+            w0[x] = wsm[i * kD + r0];
+            w1[x] = wsm[i * kD + r0 + 64];
+            ov0[x] = bsm[i * kD + r0];
+            ov1[x] = bsm[i * kD + r0 + 64];
+          }
+          for (int t = 0; t < d; ++t) {
+#pragma unroll
+            for (int x = 0; x < kBatch; ++x) {
+              if (nodes[x] < 0) continue;
+              const float2 c = coef[o[x] + t];
+              const float* wj = wsm + (pent[o[x] + t] & 255) * kD + r0;
+              const float a0 = wj[0], a1 = wj[64];
+              w0[x] = fmaf(-c.x, a0, w0[x]);
+              ov0[x] = fmaf(c.y, a0, ov0[x]);
+              w1[x] = fmaf(-c.x, a1, w1[x]);
+              ov1[x] = fmaf(c.y, a1, ov1[x]);
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < kBatch; ++x) {
+            const int i = nodes[x];
+            if (i < 0) continue;
+            wsm[i * kD + r0] = w0[x];
+            wsm[i * kD + r0 + 64] = w1[x];
+            const float e = coef[o[x] + d].y;
+            const size_t ni = (size_t)i * H * kD;
+            outb[ni + r0] = from_f32<bf16>(fmaf(e, w0[x], ov0[x]));
+            outb[ni + r0 + 64] = from_f32<bf16>(fmaf(e, w1[x], ov1[x]));
+            pvb[ni + r0] = w0[x];
+            pvb[ni + r0 + 64] = w1[x];
+          }
+        }
+        __syncthreads();
+      }
+    }
     if (!use_bsm) request_next();
-    for (int d = 0; d <= maxd; ++d) {
+    for (int d = 0; d <= (use_bsm ? -1 : maxd); ++d) {
       const int s0 = d ? hd.lvl_cnt[d - 1] : 0, s1 = hd.lvl_cnt[d];
       for (int base = s0 + wg * kBatch; base < s1; base += 2 * kBatch) {
         uint32_t dq[kBatch];
