@@ -113,3 +113,35 @@ def test_workspace_size_is_host_only_and_monotone():
     s2 = tv.tv_tree_attn_workspace_size(32, 40, 16, 4, 256, 2053)
     assert 0 < s1 < s2
     assert tv.tv_tree_attn_workspace_size(1, 15, 16, 3, 128, 258) == 0   # Hq % Hkv != 0
+
+
+@cpu_only
+def test_stack_commit_and_selective_snapshot_argument_checks():
+    keep, p = _fake()
+    L = tv.lib
+    # tv_gdn_commit_layers: the layer count and the mode are checked on the host
+    base = [tv.TV_MODE_FORK, p, p, 4, p, p, None, None, None, p]
+    assert L.tv_gdn_commit_layers(*base, 0, 2, 7, 2, 64, 64, 0, 0, p, None) == tv.TV_ERR_INVALID_ARG
+    assert L.tv_gdn_commit_layers(*base, 3, 2, 300, 2, 64, 64, 0, 0, p, None) == tv.TV_ERR_UNSUPPORTED
+    assert L.tv_gdn_commit_layers(*base, 1 << 20, 1 << 10, 7, 1 << 10, 64, 64, 0, 0, p, None) == \
+        tv.TV_ERR_UNSUPPORTED                                        # layers * B * H overflows an int
+    wy = [tv.TV_MODE_WY, p, p, 4, p, None, p, p, p, p]
+    assert L.tv_gdn_commit_layers(*wy, 2, 2, 7, 2, 96, 64, 0, 0, p, None) == tv.TV_ERR_UNSUPPORTED
+    assert L.tv_gdn_commit_layers(7, p, p, 4, p, p, p, p, p, p, 2, 2, 7, 2, 64, 64, 0, 0, p, None) == \
+        tv.TV_ERR_INVALID_ARG                                        # no such mode
+    # tv_gdn_fork_materialize_selective: capacity, threshold and pointers
+    sel = [p, p, p, p, p, p]
+    assert L.tv_gdn_fork_materialize_selective(*sel, 0.95, 0, 2, 7, 2, 64, 64, 0, 0, 0, p, p, p, None) == \
+        tv.TV_ERR_INVALID_ARG                                        # capacity 0
+    assert L.tv_gdn_fork_materialize_selective(*sel, 0.95, 8, 2, 7, 2, 64, 64, 0, 0, 0, p, p, p, None) == \
+        tv.TV_ERR_INVALID_ARG                                        # capacity > N
+    assert L.tv_gdn_fork_materialize_selective(*sel, float("nan"), 3, 2, 7, 2, 64, 64, 0, 0, 0, p, p, p, None) == \
+        tv.TV_ERR_INVALID_ARG
+    assert L.tv_gdn_fork_materialize_selective(p, p, p, p, p, None, 0.95, 3, 2, 7, 2, 64, 64, 0, 0, 0, p, p, p,
+                                               None) == tv.TV_ERR_INVALID_ARG   # no confidence
+    assert L.tv_gdn_fork_materialize_selective(*sel, 0.95, 3, 2, 7, 2, 64, 64, 0, 0, -1, p, p, p, None) == \
+        tv.TV_ERR_INVALID_ARG                                        # negative CTA cap
+    assert L.tv_gdn_fork_materialize(p, p, p, p, p, 2, 300, 2, 64, 64, 0, 0, 0, p, p, None) == tv.TV_ERR_UNSUPPORTED
+    # tv_tree_prepare: paths need a positive row length
+    assert L.tv_tree_prepare(p, 2, 7, p, p, p, 0, None, p, None) == tv.TV_ERR_INVALID_ARG
+    del keep
