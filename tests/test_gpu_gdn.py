@@ -238,11 +238,22 @@ def test_host_side_argument_errors():
     assert e.value.status == tv.TV_ERR_UNSUPPORTED
 
 
+def _stack_cases(kind):
+    if kind == "bf16":
+        return [W.stack_b64_layer(layer=l, B=8) for l in range(3)]
+    rng = np.random.default_rng(31)
+    trees = [W.random_tree(21, rng) for _ in range(4)]
+    return [W.gdn_case(trees, H=3, dk=64, dv=64, io="f32", state="f32", seed=40 + l, path_max_len=6)
+            for l in range(2)]
+
+
+@pytest.mark.parametrize("kind", ["bf16", "f32"])
 @pytest.mark.parametrize("mode", ["fork", "wy"])
-def test_commit_of_a_layer_stack_in_one_launch_equals_per_layer_commits(mode):
-    # Three independent layers sharing the trees and the accepted paths: tv_gdn_commit_layers on
-    # the stacked tensors gives each layer's tv_gdn_commit result, bit for bit.
-    cases = [W.stack_b64_layer(layer=l, B=8) for l in range(3)]
+def test_commit_of_a_layer_stack_in_one_launch_equals_per_layer_commits(mode, kind):
+    # Independent layers sharing the trees and the accepted paths: tv_gdn_commit_layers on the
+    # stacked tensors gives each layer's tv_gdn_commit result, bit for bit (bf16 d=128 and
+    # fp32 d=64, so both element sizes enter the layer offsets).
+    cases = _stack_cases(kind)
     c0 = cases[0]
     runs = [(_gpu.run_fork(c, keep_device=True) if mode == "fork" else _gpu.run_wy(c)) for c in cases]
     want = [_gpu.run_commit(c, mode, r, path=c0.path, path_len=c0.path_len) for c, r in zip(cases, runs)]
@@ -260,5 +271,5 @@ def test_commit_of_a_layer_stack_in_one_launch_equals_per_layer_commits(mode):
         tv.tv_gdn_commit_layers(tv.TV_MODE_WY, path, plen, parents, S0, err, pseudo_v=pv, log_gamma=lg, k=k)
     torch.cuda.synchronize()
     assert (err.cpu() == 0).all()
-    for l in range(3):
+    for l in range(len(cases)):
         assert torch.equal(S0[l].cpu(), want[l])
