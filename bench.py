@@ -866,6 +866,60 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args) -> None:
+    """Per-layer GDN verify times across tree sizes: random dynamic trees (1..4 children per
+    node, depth <= 8), N in {15, 40, 64, 128, 256}, B in {8, 32}, H=16, d=128, bf16.  Fork mode
+    runs its two passes on one stream (tv_gdn_tree_verify_fork_ws), TreeWY one launch.  One
+    JSON line, apart from the benchmark's."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import tree_speculative_verification_gdn_gb300 as tv
+    import workloads as W
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    ev = torch.cuda.Event
+
+    def timed(fn, iters=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        s, e = ev(enable_timing=True), ev(enable_timing=True)
+        s.record()
+        for _ in range(iters):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / iters
+
+    rows = []
+    for B in (8, 32):
+        for N in (15, 40, 64, 128, 256):
+            c = W.sweep_gdn_layer(N, B)
+            x = {k: getattr(c, k).contiguous().to("cuda") for k in ("q", "k", "v", "alpha", "beta", "S0", "parents")}
+            _, _, H, dk, dv = c.shape
+            out = torch.empty((B, N, H, dv), dtype=torch.bfloat16, device="cuda")
+            pv = torch.empty((B, N, H, dv), dtype=torch.float32, device="cuda")
+            lg = torch.empty((B, N, H), dtype=torch.float32, device="cuda")
+            states = torch.empty((B, N, H, dv, dk), dtype=torch.bfloat16, device="cuda")
+            ws = torch.empty(tv.tv_gdn_fork_workspace_size(B, N, H, dv), dtype=torch.uint8, device="cuda")
+            err = torch.zeros((B,), dtype=torch.int32, device="cuda")
+            wy_ms = timed(lambda: tv.tv_gdn_tree_verify_wy(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"],
+                                                           x["parents"], out, pv, lg, err))
+            fork_ms = timed(lambda: tv.tv_gdn_tree_verify_fork_ws(x["q"], x["k"], x["v"], x["alpha"], x["beta"],
+                                                                  x["S0"], x["parents"], out, states, ws, err))
+            assert int(err.abs().sum()) == 0, (N, B, err.tolist())
+            fb, wb = gdn_bytes(B, N, H, dk, dv, 2, 2, "fork"), gdn_bytes(B, N, H, dk, dv, 2, 2, "wy")
+            rows.append({"B": B, "N": N, "max_depth": max(max(_depths(t)) for t in c.trees),
+                         "wy_ms": round(wy_ms, 4), "wy_nodes_per_s": round(B * N / (wy_ms * 1e-3)),
+                         "wy_frac_hbm": round(wb / (wy_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
+                         "fork_ms": round(fork_ms, 4), "fork_nodes_per_s": round(B * N / (fork_ms * 1e-3)),
+                         "fork_frac_hbm": round(fb / (fork_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)})
+            del states, ws
+    print(json.dumps({"sweep": "GDN verify per layer, random dynamic trees, H=16, d=128, bf16", "rows": rows}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -878,8 +932,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-reports", action="store_true",
                     help="skip the selective-fork, lazy-commit and one-pass-fork reports after the timed steps")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the benchmark: per-layer GDN verify times across tree sizes (one JSON line)")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
