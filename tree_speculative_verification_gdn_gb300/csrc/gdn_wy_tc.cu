@@ -7,10 +7,11 @@
 // node keys and queries (B operands, N x 128 each, zero rows past N) into shared memory in the
 // 128-byte swizzle layout, one thread issues 16 MMAs (M = 128, N = Npad, K = 16) that
 // accumulate in fp32 in TMEM, and the epilogue reads row r of both products back with
-// tcgen05.ld -- row r belongs to TMEM lane r.  The (node, path entry) coefficients come from
-// the same shared-memory tiles, 8 lanes per entry.  The forward substitution then runs depth
-// level by depth level: within a level every node is independent, so two warp groups split it
-// and each warp keeps 8 nodes' loads in flight.
+// tcgen05.ld, 16 columns per load -- row r belongs to TMEM lane r.  The (node, path entry)
+// coefficients come from the same shared-memory tiles, 8 lanes per entry, while the MMAs run.
+// The forward substitution then runs depth level by depth level: within a level every node is
+// independent, so groups of threads split it, 8 nodes at a time, and every per-node load
+// serves all of a thread's rows (two per thread while the products fit in shared memory).
 #include "tv_async.cuh"
 #include "tv_common.cuh"
 #include "tv_internal.h"
