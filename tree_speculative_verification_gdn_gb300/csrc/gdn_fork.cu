@@ -465,6 +465,9 @@ cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel,
   int per_seq = slots / a.B;
   if (per_seq < 1) per_seq = 1;
   if (per_seq > items) per_seq = items;
+  // The fewest CTAs per sequence with the same longest CTA: slots freed for other streams' work
+  // without lengthening this kernel.
+  per_seq = (items + (items + per_seq - 1) / per_seq - 1) / ((items + per_seq - 1) / per_seq);
   kern<<<a.B * per_seq, kThreads, smem, s>>>(a, static_cast<TS*>(states), per_seq, nslots, sel, wsrc);
   return cudaGetLastError();
 }
