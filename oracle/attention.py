@@ -19,6 +19,11 @@ Sources
   the listing; qwen35-tree-spec §七 Step 4).  Reading: node i's KV sits at logical slot
   prefix_len + i; after compaction slots prefix_len + r hold node path[r] for r < L and the
   new length is prefix_len + L.
+* Block-table compaction: the same note allows updating the block table instead of moving
+  the slots.  Reading: a logical block that lies wholly at or past the prefix and whose kept
+  entries all come from one other block, each at its own row, takes that block by an exchange
+  of the two table entries; every other kept entry is moved as above.  The logical contents
+  of slots [0, new length) are those of the moving compaction.
 """
 from __future__ import annotations
 
@@ -148,3 +153,69 @@ def kv_compact(k_cache: np.ndarray, v_cache: np.ndarray, block_table: np.ndarray
             slot_map[b, r] = src[r]
         new_len[b] = P + L
     return kc, vc, slot_map, new_len
+
+
+def remap_plan(P: int, path, L: int, block_size: int = 16):
+    """Destination blocks taken over by a table exchange, in ascending order: pairs (m, j) where
+    logical block m lies wholly at or past P (m * bs >= P), holds kept entries r (P + r in
+    block m, r < L), and every one of them comes from P + path[r] = P + r + j * bs with the
+    same j >= 1.  Such a block's kept entries are exactly block m + j's entries at the same
+    rows, so block m may take block m + j's physical block."""
+    bs = block_size
+    plan = []
+    first = -(-P // bs)
+    last = (P + L - 1) // bs
+    for m in range(first, last + 1):
+        rows = [r for r in range(L) if m * bs <= P + r < (m + 1) * bs]
+        shifts = {int(path[r]) - r for r in rows}
+        if len(shifts) == 1:
+            d = shifts.pop()
+            if d > 0 and d % bs == 0:
+                plan.append((m, d // bs))
+    return plan
+
+
+def kv_compact_remap(k_cache: np.ndarray, v_cache: np.ndarray, block_table: np.ndarray,
+                     prefix_len: np.ndarray, parents: np.ndarray, path: np.ndarray,
+                     path_len: np.ndarray, block_size: int = 16):
+    """Compaction that exchanges block-table entries where a whole destination block can be
+    taken from one source block (``remap_plan``), and moves the remaining kept entries.
+
+    For each valid sequence: the table row's entries m and m + j are exchanged for every
+    (m, j) of the plan, in ascending m; then for every kept entry r < L outside the planned
+    blocks, physical slot (new table, P + r) receives what physical slot (old table,
+    P + path[r]) held before the call.  Returns the new caches, the new block table, ``slot_map
+    [B, Lmax]`` (physical source slot under the old table, -1 past L), ``new_len [B]`` and
+    ``remapped [B]`` (the number of exchanges).  A sequence with an invalid tree or path keeps
+    its cache and table; its new length is P."""
+    kc = k_cache.copy()
+    vc = v_cache.copy()
+    table = np.asarray(block_table).copy()
+    B, Lmax = path.shape
+    slot_map = np.full((B, Lmax), -1, dtype=np.int64)
+    new_len = np.asarray(prefix_len, dtype=np.int64).copy()
+    remapped = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        P = int(prefix_len[b])
+        L = int(path_len[b])
+        if not (is_valid_tree(parents[b]) and is_valid_path(parents[b], path[b], L)):
+            continue
+        old_row = np.asarray(block_table[b])
+        new_row = table[b]
+        plan = remap_plan(P, path[b], L, block_size)
+        for m, j in plan:
+            new_row[m], new_row[m + j] = new_row[m + j], new_row[m]
+        taken = {m for m, _ in plan}
+        src = [physical_slot(old_row, P + int(path[b][r]), block_size) for r in range(L)]
+        saved_k = [k_cache[s // block_size, :, s % block_size, :].copy() for s in src]
+        saved_v = [v_cache[s // block_size, :, s % block_size, :].copy() for s in src]
+        for r in range(L):
+            slot_map[b, r] = src[r]
+            if (P + r) // block_size in taken:
+                continue
+            dst = physical_slot(new_row, P + r, block_size)
+            kc[dst // block_size, :, dst % block_size, :] = saved_k[r]
+            vc[dst // block_size, :, dst % block_size, :] = saved_v[r]
+        new_len[b] = P + L
+        remapped[b] = len(plan)
+    return kc, vc, table, slot_map, new_len, remapped

@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import test_oracle_attention as PA
+import test_oracle_compact_remap as PR
 import test_oracle_gdn as PG
 from oracle import attention as A
 from oracle import gdn as G
@@ -225,3 +226,74 @@ def _walk_ignores_lmax(parents, draft_tokens, target_tokens, lmax):
 def test_accept_walk_mutants_are_caught(monkeypatch, mutant):
     monkeypatch.setattr(T, "accept_walk", mutant)
     assert _run_pins(_WALK_PINS) >= 1
+
+
+_PLAN = A.remap_plan
+
+
+def _run_remap_pins():
+    """Every remap pin with each of its parameters; returns how many failed."""
+    calls = [lambda f=f: PR.test_golden_cases(f) for f in PR._golden_cases()]
+    calls += [lambda s=s: PR.test_logical_view_equals_moving_compaction(s) for s in (0, 1, 2)]
+    calls += [lambda s=s: PR.test_plan_matches_physical_statement(s) for s in (3, 4)]
+    calls += [PR.test_invalid_path_leaves_everything]
+    failed = 0
+    for call in calls:
+        try:
+            call()
+        except (AssertionError, IndexError):
+            failed += 1
+    return failed
+
+
+def _plan_floor(P, path, L, block_size=16):
+    """Also considers the block that holds the last prefix slots."""
+    bs = block_size
+    plan = []
+    for m in range(P // bs, (P + L - 1) // bs + 1):
+        rows = [r for r in range(L) if m * bs <= P + r < (m + 1) * bs]
+        shifts = {int(path[r]) - r for r in rows}
+        if len(shifts) == 1:
+            d = shifts.pop()
+            if d > 0 and d % bs == 0:
+                plan.append((m, d // bs))
+    return plan
+
+
+def _plan_any_shift(P, path, L, block_size=16):
+    """Takes over blocks whose shift is not a whole number of blocks."""
+    bs = block_size
+    plan = []
+    for m in range(-(-P // bs), (P + L - 1) // bs + 1):
+        rows = [r for r in range(L) if m * bs <= P + r < (m + 1) * bs]
+        shifts = {int(path[r]) - r for r in rows}
+        if len(shifts) == 1 and min(shifts) > 0:
+            plan.append((m, max(1, min(shifts) // bs)))
+    return plan
+
+
+def _plan_first_row_only(P, path, L, block_size=16):
+    """Decides each block from its first kept entry alone."""
+    bs = block_size
+    plan = []
+    for m in range(-(-P // bs), (P + L - 1) // bs + 1):
+        r = max(m * bs - P, 0)
+        d = int(path[r]) - r
+        if d > 0 and d % bs == 0:
+            plan.append((m, d // bs))
+    return plan
+
+
+def _plan_descending(P, path, L, block_size=16):
+    """Right blocks, exchanged from the last to the first."""
+    return _PLAN(P, path, L, block_size)[::-1]
+
+
+@pytest.mark.parametrize("mutant", [_plan_floor, _plan_any_shift, _plan_first_row_only, _plan_descending])
+def test_remap_plan_mutants_are_caught(monkeypatch, mutant):
+    monkeypatch.setattr(A, "remap_plan", mutant)
+    assert _run_remap_pins() >= 1
+
+
+def test_remap_pins_pass_on_the_oracle():
+    assert _run_remap_pins() == 0

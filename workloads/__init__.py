@@ -53,6 +53,17 @@ def branching_tree(branching: list[int]) -> list[int]:
     return parents
 
 
+def candidate_chains(lengths: list[int]) -> list[int]:
+    """A root with one draft chain per entry of ``lengths`` under it, each chain numbered
+    contiguously (depth-first order, so ``parents[i] < i`` still holds)."""
+    parents = [-1]
+    for length in lengths:
+        parents.append(0)
+        for _ in range(length - 1):
+            parents.append(len(parents) - 1)
+    return parents
+
+
 def full_tree(k: int, d: int) -> list[int]:
     """Full k-ary tree of depth ``d`` below the root, numbered breadth-first."""
     return branching_tree([k] * d)
