@@ -205,6 +205,7 @@ class Round:
         dev = torch.device("cuda", torch.cuda.current_device())
         self.dev = dev
         seed = 1000 * rank
+        self.seed = seed
         self.layers = layers
         self.gdn_host = [W.stack_b64_layer(layer=l, seed=seed) for l in range(layers)]
         c0 = self.gdn_host[0]
@@ -688,6 +689,56 @@ def lazy_commit_report(rnd, torch, tv, iters: int = 3) -> dict:
             "bytes_saved_per_layer": B * H * dv * dv * 2}
 
 
+def block_table_compaction_report(rnd, torch, tv, W, iters: int = 20) -> dict:
+    """Compaction of accepted paths that run down long draft chains, on the step's paged cache
+    (batch 32, 4 KV heads, hd 256): a root with chains of 16, 16 and 7 nodes (40 nodes, as the
+    step's trees), each path down one chain.  Moving every kept entry (``tv_kv_compact``)
+    against exchanging whole blocks of the table where it can (``tv_kv_compact_remap``)."""
+    import numpy as np
+    aB, aN = rnd.aB, rnd.aN
+    assert aN == 1 + sum(W.CHAIN_LENGTHS)
+    parents = torch.tensor([W.candidate_chains(W.CHAIN_LENGTHS)] * aB, dtype=torch.int32, device=rnd.dev)
+    paths = W.candidate_chain_paths(W.CHAIN_LENGTHS, aB, np.random.default_rng(rnd.seed + 21))
+    lens = [len(p) for p in paths]
+    Lmax = max(lens)
+    path = torch.tensor([p + [-1] * (Lmax - len(p)) for p in paths], dtype=torch.int32, device=rnd.dev)
+    path_len = torch.tensor(lens, dtype=torch.int32, device=rnd.dev)
+    table, plen = rnd.in_attn["block_table"], rnd.in_attn["prefix_len"]
+    table_out = torch.empty_like(table)
+    i32 = dict(dtype=torch.int32, device=rnd.dev)
+    slot_map, new_len = torch.empty((aB, Lmax), **i32), torch.empty((aB,), **i32)
+    remapped, err = torch.zeros((aB,), **i32), torch.zeros((2, aB), **i32)
+
+    def copy_form():
+        tv.tv_kv_compact(rnd.k_cache, rnd.v_cache, table, plen, parents, path, path_len, slot_map, new_len, err[0])
+
+    def remap_form():
+        tv.tv_kv_compact_remap(rnd.k_cache, rnd.v_cache, table, table_out, plen, parents, path, path_len,
+                               slot_map, new_len, remapped, err[1])
+
+    def timed(fn):
+        # a call takes microseconds on the device and longer to issue from Python: the calls are
+        # queued behind a device-side sleep so that the events bracket device time only
+        fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(4_000_000)
+        s.record()
+        for _ in range(iters):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / iters
+
+    ms_copy = timed(copy_form)
+    ms_remap = timed(remap_form)
+    assert int(err.abs().sum()) == 0, err
+    return {"tree": "root + chains of 16, 16, 7 nodes", "kept_entries": sum(lens),
+            "blocks_exchanged": int(remapped.sum()),
+            "copy_form_bytes": compact_bytes(lens, rnd.Hkv, rnd.hd),
+            "copy_form_ms": round(ms_copy, 5), "block_table_form_ms": round(ms_remap, 5)}
+
+
 def run_ours(args) -> None:
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -768,11 +819,12 @@ def run_ours(args) -> None:
                "copies": "pinned host memory, per layer on an upload and a download stream overlapping the kernels, "
                          "uploads into two alternating input sets; the step ends after the last download"}
 
-    selective = lazy = one_pass = None
+    selective = lazy = one_pass = remap = None
     if not args.no_reports:
         selective = selective_fork_report(rnd, torch, tv)
         lazy = lazy_commit_report(rnd, torch, tv)
         one_pass = one_pass_fork_report(rnd, torch, tv)
+        remap = block_table_compaction_report(rnd, torch, tv, W)
     peaks = load_peaks()
     B, N, H, dk, dv = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv
     L_sum = int(rnd.gdn_host[0].path_len.sum())
@@ -831,7 +883,7 @@ def run_ours(args) -> None:
             "gpu_launches": rnd.launches_per_step * args.steps, "clocks": clk, "roofline": roof,
             "rows": rows, "accepted_tokens": accepted, "state_memory": mem, "selective_fork": selective,
             "lazy_commit": lazy,
-            "one_pass_fork": one_pass, "e2e": e2e,
+            "one_pass_fork": one_pass, "block_table_compaction": remap, "e2e": e2e,
             "cpu_baseline": cpu_base}
     if rank == 0:
         print(json.dumps(line), flush=True)

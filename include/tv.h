@@ -432,6 +432,40 @@ TV_API int tv_kv_compact(void* k_cache, void* v_cache, int num_blocks, const int
                   int32_t* err, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * tv_kv_compact_remap -- keep the accepted path's KV, exchanging whole blocks of the block
+ * table where that replaces moving them.
+ *
+ * Source: handbook chapter 树形草稿与 EAGLE, note after the listing (the accepted nodes' slots
+ * are compacted to the sequence's positions, or only the block table is updated).  Reading,
+ * per sequence with P = prefix_len[b], L = accepted_len[b], block size 16:
+ *  - a logical block m with 16 m >= P that holds kept entries (P + r for r < L), all of which
+ *    come from logical slot P + r + 16 j for one j >= 1, takes block m + j's physical block:
+ *    entries m and m + j of the table row are exchanged, in ascending m;
+ *  - every other kept entry r is moved: physical slot (new row, P + r) receives what physical
+ *    slot (old row, P + path[r]) held before the call.  Every source is read before any
+ *    write; an entry already in place is not written.
+ * Read through block_table_out, logical slots [0, P + L) then hold what tv_kv_compact leaves
+ * in them read through block_table.  The new row is a permutation of the old one; entries of
+ * blocks holding prefix slots are unchanged.  Slots at or past the new length are void.
+ *
+ *   k_cache, v_cache [num_blocks, Hkv, block_size, hd] bf16     in/out
+ *   block_table     [B, max_blocks] int32   in   the rows before the call
+ *   block_table_out [B, max_blocks] int32   out  the rows after the exchanges (a copy of the
+ *                                                row for a sequence with an error); must not
+ *                                                overlap block_table (TV_ERR_INVALID_ARG)
+ *   prefix_len, parents, accepted_path, accepted_len, slot_map, new_len, err: as for
+ *                                                tv_kv_compact (slot_map under the old rows)
+ *   remapped        [B] int32               out  exchanges made (0 on error)
+ * Supported: hd in {64, 128, 256}; block_size = 16; N <= TV_MAX_NODES.
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_kv_compact_remap(void* k_cache, void* v_cache, int num_blocks, const int32_t* block_table,
+                        int32_t* block_table_out, int max_blocks, const int32_t* prefix_len,
+                        const int32_t* parents, int N, const int32_t* accepted_path,
+                        const int32_t* accepted_len, int Lmax, int B, int Hkv, int hd, int block_size,
+                        int32_t* slot_map, int32_t* new_len, int32_t* remapped, int32_t* err,
+                        tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * tv_accept_walk -- greedy acceptance of B draft trees, on the device.
  *
  * Source: handbook chapter 树形草稿与 EAGLE, §实现, tree_speculative_generate: from node 0,

@@ -183,3 +183,22 @@ def run_compact(case: W.AttnCase, k_cache: torch.Tensor, v_cache: torch.Tensor, 
     torch.cuda.synchronize()
     return dict(k_cache=kc.cpu(), v_cache=vc.cpu(), slot_map=slot_map.cpu().numpy(),
                 new_len=new_len.cpu().numpy(), err=err.cpu())
+
+
+def run_compact_remap(k_cache, v_cache, block_table, prefix_len, parents, path, path_len,
+                      table_out_fill: int = -7) -> dict:
+    """``tv_kv_compact_remap`` on copies of the given tensors; returns everything on the CPU."""
+    B = block_table.shape[0]
+    kc, vc = to_dev(k_cache), to_dev(v_cache)
+    table = to_dev(block_table)
+    table_out = torch.full_like(table, table_out_fill)
+    p = to_dev(path)
+    slot_map = torch.full(p.shape, 777, dtype=torch.int32, device=DEV)
+    new_len = torch.full((B,), 777, dtype=torch.int32, device=DEV)
+    remapped = torch.full((B,), 777, dtype=torch.int32, device=DEV)
+    err = _err(B)
+    tv.tv_kv_compact_remap(kc, vc, table, table_out, to_dev(prefix_len), to_dev(parents), p, to_dev(path_len),
+                           slot_map, new_len, remapped, err)
+    torch.cuda.synchronize()
+    return dict(k_cache=kc, v_cache=vc, table=table_out.cpu().numpy(), slot_map=slot_map.cpu().numpy(),
+                new_len=new_len.cpu().numpy(), remapped=remapped.cpu().numpy(), err=err.cpu())

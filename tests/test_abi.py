@@ -145,3 +145,26 @@ def test_stack_commit_and_selective_snapshot_argument_checks():
     # tv_tree_prepare: paths need a positive row length
     assert L.tv_tree_prepare(p, 2, 7, p, p, p, 0, None, p, None) == tv.TV_ERR_INVALID_ARG
     del keep
+
+
+@cpu_only
+def test_block_table_compaction_argument_checks():
+    keep, p = _fake()
+    out = ctypes.c_void_p(p.value + 4096)
+    base = [p, p, 8, p, out, 4, p, p, 40, p, p, 5, 2, 4, 128, 16, p, p, p, p, None]
+
+    def call(**changes):
+        a = list(base)
+        for i, v in changes.items():
+            a[int(i[1:])] = v
+        return tv.lib.tv_kv_compact_remap(*a)
+
+    assert call(a4=ctypes.c_void_p(p.value + 16)) == tv.TV_ERR_INVALID_ARG   # output overlaps the table
+    assert call(a4=p) == tv.TV_ERR_INVALID_ARG
+    assert call(a4=None) == tv.TV_ERR_INVALID_ARG
+    assert call(a18=None) == tv.TV_ERR_INVALID_ARG                           # no exchange counts
+    assert call(a12=0) == tv.TV_ERR_INVALID_ARG
+    assert call(a14=96) == tv.TV_ERR_UNSUPPORTED
+    assert call(a15=32) == tv.TV_ERR_UNSUPPORTED
+    assert call(a8=257) == tv.TV_ERR_UNSUPPORTED
+    del keep

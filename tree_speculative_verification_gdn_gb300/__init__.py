@@ -43,7 +43,8 @@ EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_pre
             "tv_tree_attn_workspace_size", "tv_tree_attn", "tv_tree_attn_static", "tv_kv_compact",
             "tv_accept_walk", "tv_gdn_tree_verify_fork_selective", "tv_gdn_commit_selective",
             "tv_gdn_tree_verify_wy_lazy", "tv_gdn_fork_workspace_size", "tv_gdn_tree_verify_fork_ws",
-            "tv_gdn_fork_materialize", "tv_gdn_fork_materialize_selective", "tv_gdn_commit_layers")
+            "tv_gdn_fork_materialize", "tv_gdn_fork_materialize_selective", "tv_gdn_commit_layers",
+            "tv_kv_compact_remap")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -78,6 +79,8 @@ _SIGNATURES = {
                                                _P, _P, _P, _P]),
     "tv_accept_walk": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "tv_kv_compact_remap": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                 _P]),
 }
 
 
@@ -308,6 +311,20 @@ def tv_kv_compact(k_cache, v_cache, block_table, prefix_len, parents, accepted_p
         _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table), max_blocks, _ptr(prefix_len),
         _ptr(parents), N, _ptr(accepted_path), _ptr(accepted_len), Lmax, B, Hkv, hd, bs, _ptr(slot_map),
         _ptr(new_len), _ptr(err), _stream(stream)), "tv_kv_compact")
+
+
+def tv_kv_compact_remap(k_cache, v_cache, block_table, block_table_out, prefix_len, parents, accepted_path,
+                        accepted_len, slot_map, new_len, remapped, err, stream=None) -> None:
+    """Compaction that exchanges whole blocks of ``block_table`` where it can (result rows in
+    ``block_table_out``) and moves the other kept entries; ``remapped [B]`` counts exchanges."""
+    num_blocks, Hkv, bs, hd = k_cache.shape
+    B, max_blocks = block_table.shape
+    N = parents.shape[1]
+    Lmax = accepted_path.shape[1]
+    _check(lib.tv_kv_compact_remap(
+        _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table), _ptr(block_table_out), max_blocks,
+        _ptr(prefix_len), _ptr(parents), N, _ptr(accepted_path), _ptr(accepted_len), Lmax, B, Hkv, hd, bs,
+        _ptr(slot_map), _ptr(new_len), _ptr(remapped), _ptr(err), _stream(stream)), "tv_kv_compact_remap")
 
 
 def tv_accept_walk(parents, draft_tokens, target_tokens, accepted_path, accepted_len, next_token, err,

@@ -308,6 +308,31 @@ int tv_kv_compact(void* k_cache, void* v_cache, int num_blocks, const int32_t* b
   return cuda_status(tv::launch_kv_compact(a, stream));
 }
 
+int tv_kv_compact_remap(void* k_cache, void* v_cache, int num_blocks, const int32_t* block_table,
+                        int32_t* block_table_out, int max_blocks, const int32_t* prefix_len,
+                        const int32_t* parents, int N, const int32_t* accepted_path,
+                        const int32_t* accepted_len, int Lmax, int B, int Hkv, int hd, int block_size,
+                        int32_t* slot_map, int32_t* new_len, int32_t* remapped, int32_t* err,
+                        tv_stream_t stream) {
+  if (!a16(k_cache) || !a16(v_cache) || !a4(block_table) || !a4(block_table_out) || !a4(prefix_len) ||
+      !a4(parents) || !a4(accepted_path) || !a4(accepted_len) || !a4(slot_map) || !a4(new_len) ||
+      !a4(remapped) || !a4(err))
+    return TV_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || Hkv < 1 || Lmax < 1 || num_blocks < 1 || max_blocks < 1) return TV_ERR_INVALID_ARG;
+  {
+    const uintptr_t in0 = reinterpret_cast<uintptr_t>(block_table);
+    const uintptr_t out0 = reinterpret_cast<uintptr_t>(block_table_out);
+    const uintptr_t bytes = (uintptr_t)B * (uintptr_t)max_blocks * sizeof(int32_t);
+    if (in0 < out0 + bytes && out0 < in0 + bytes) return TV_ERR_INVALID_ARG;
+  }
+  if (N > TV_MAX_NODES || (hd != 64 && hd != 128 && hd != 256) || block_size != TV_BLOCK_SIZE)
+    return TV_ERR_UNSUPPORTED;
+  tv::CompactArgs a{k_cache, v_cache, num_blocks, block_table, max_blocks, prefix_len, parents, N,
+                    accepted_path, accepted_len, Lmax, B, Hkv, hd, block_size, slot_map, new_len, err,
+                    block_table_out, remapped};
+  return cuda_status(tv::launch_kv_compact_remap(a, stream));
+}
+
 int tv_accept_walk(const int32_t* parents, const int32_t* draft_tokens, const int32_t* target_tokens, int B,
                    int N, int Lmax, int32_t* accepted_path, int32_t* accepted_len, int32_t* next_token,
                    int32_t* err, tv_stream_t stream) {

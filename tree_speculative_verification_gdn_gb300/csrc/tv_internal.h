@@ -142,8 +142,11 @@ struct CompactArgs {
   int32_t* slot_map;
   int32_t* new_len;
   int32_t* err;
+  int32_t* table_out;   // block-table form only: the row after the exchanges
+  int32_t* remapped;    // block-table form only: exchanges per sequence
 };
 cudaError_t launch_kv_compact(const CompactArgs& a, cudaStream_t s);
+cudaError_t launch_kv_compact_remap(const CompactArgs& a, cudaStream_t s);
 
 struct AcceptArgs {
   const int32_t* parents;

@@ -345,6 +345,34 @@ def paged_attn_b32_case(B: int = 32, seed: int = 0, pmin: int = 2048, pmax: int 
                      path_max_len=4)
 
 
+def paged_chains_case(B: int = 32, seed: int = 0, pmin: int = 2048, pmax: int = 32768) -> AttnCase:
+    """Compaction on candidate chains: the paged batch-32 shapes (16q/4kv, hd 256, bf16,
+    P ~ U{2048..32768}) with a root and chains of 16, 16 and 7 nodes (N = 40) in depth-first
+    order; each accepted path runs down one chain, chosen uniformly, for a uniform length
+    (1 .. chain length + 1)."""
+    rng = np.random.default_rng(seed + 11)
+    prefix = [int(x) for x in rng.integers(pmin, pmax + 1, size=B)]
+    lengths = CHAIN_LENGTHS
+    paths = candidate_chain_paths(lengths, B, rng)
+    return attn_case([candidate_chains(lengths)] * B, prefix, Hq=16, Hkv=4, hd=256, seed=seed,
+                     rope_theta=1e6, paths=paths)
+
+
+CHAIN_LENGTHS = [16, 16, 7]
+
+
+def candidate_chain_paths(lengths: list[int], B: int, rng: np.random.Generator) -> list[list[int]]:
+    """One accepted path per sequence of a ``candidate_chains(lengths)`` tree: down one chain,
+    chosen uniformly, for a uniform length 1 .. chain length + 1 (root included)."""
+    starts = [1 + sum(lengths[:c]) for c in range(len(lengths))]
+    paths = []
+    for _ in range(B):
+        c = int(rng.integers(0, len(lengths)))
+        L = int(rng.integers(1, lengths[c] + 2))
+        paths.append([0] + list(range(starts[c], starts[c] + L - 1)))
+    return paths
+
+
 def sweep_trees(N: int, B: int, seed: int = 0) -> list[list[int]]:
     """Wide-tree sweep: random dynamic trees (1..4 children per node, depth <= 8), one per sequence."""
     rng = np.random.default_rng(seed + 4000 + N)
