@@ -19,15 +19,18 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kVecPerThread = 8;
+constexpr int kMaxWin = TV_MAX_NODES / 16 + 2;   // logical blocks spanned by P .. P + N - 1
 
 struct CompactCheck {
   int par[TV_MAX_NODES];
   int path[TV_MAX_NODES];
-  int flag, L, P;
+  int win[kMaxWin];        // table entries of logical blocks first .. first + nwin - 1
+  int flag, L, P, first, nwin;
 };
 
 // Tree, path, capacity and block-table checks for sequence b (whole CTA; the result is the
-// same in every thread).  On success c.path[0 .. L) holds the path.
+// same in every thread).  On success c.path[0 .. L) holds the path and c.win the table entries
+// of the logical blocks the tree's slots span (every source and destination lies there).
 __device__ int check_compact(const CompactArgs& a, int b, CompactCheck& c) {
   if (threadIdx.x == 0) {
     c.L = a.path_len[b];
@@ -53,7 +56,12 @@ __device__ int check_compact(const CompactArgs& a, int b, CompactCheck& c) {
   bool bad_block = false;
   for (int lb = first + threadIdx.x; lb <= last; lb += kThreads) {
     const int blk = table[lb];
+    c.win[lb - first] = blk;
     bad_block |= blk < 0 || blk >= a.num_blocks;
+  }
+  if (threadIdx.x == 0) {
+    c.first = first;
+    c.nwin = last - first + 1;
   }
   if (__syncthreads_or(bad_path)) return TV_ERR_BAD_PATH;
   if (__syncthreads_or(bad_block)) return TV_ERR_BAD_BLOCK;
@@ -68,7 +76,6 @@ __device__ void move_entries(const CompactArgs& a, int b, int kvh, const Compact
   const int bs = a.block_size;
   const int vpr = a.hd / 8;                                  // 16-byte vectors per row
   const int rows_per_round = kThreads * kVecPerThread / (2 * vpr);
-  const int* table = a.block_table + (size_t)b * a.max_blocks;
   uint4* kc = static_cast<uint4*>(a.k_cache);
   uint4* vc = static_cast<uint4*>(a.v_cache);
   auto vec_base = [&](int blk, int row) -> size_t {
@@ -89,7 +96,7 @@ __device__ void move_entries(const CompactArgs& a, int b, int kvh, const Compact
         const int r = r0 + rem / vpr, col = rem % vpr;
         const int ds = c.P + r, ss = c.P + c.path[r];
         const int dblk = dst_block(ds / bs);
-        const int sblk = table[ss / bs];
+        const int sblk = c.win[ss / bs - c.first];
         if (dblk >= 0 && (dblk != sblk || ds % bs != ss % bs)) {
           const uint4* cache = which ? vc : kc;
           buf[u] = cache[vec_base(sblk, ss % bs) + col];
@@ -116,7 +123,6 @@ __global__ void __launch_bounds__(kThreads) kv_compact_kernel(CompactArgs a) {
   __shared__ CompactCheck c;
   const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv;
   const int st = check_compact(a, b, c);
-  const int* table = a.block_table + (size_t)b * a.max_blocks;
   if (kvh == 0) {
     if (threadIdx.x == 0) {
       a.err[b] = st;
@@ -126,13 +132,13 @@ __global__ void __launch_bounds__(kThreads) kv_compact_kernel(CompactArgs a) {
       int smap = -1;
       if (!st && r < c.L) {
         const int s = c.P + c.path[r];
-        smap = table[s / a.block_size] * a.block_size + s % a.block_size;
+        smap = c.win[s / a.block_size - c.first] * a.block_size + s % a.block_size;
       }
       a.slot_map[(size_t)b * a.Lmax + r] = smap;
     }
   }
   if (st) return;
-  move_entries(a, b, kvh, c, [&](int lb) { return table[lb]; });
+  move_entries(a, b, kvh, c, [&](int lb) { return c.win[lb - c.first]; });
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -142,14 +148,12 @@ __global__ void __launch_bounds__(kThreads) kv_compact_kernel(CompactArgs a) {
 // ascending m; only the other kept entries are moved.  Since path[r] - r never decreases along
 // the path, the source block m + j of an exchange has not been touched by an earlier exchange.
 //
-// Loads use the table as it was (global memory, never written here); stores use the new row,
-// held in shared memory.  A store lands in a block that is not taken over: if it was an
+// Loads use the table as it was (the checks' shared copy of its window; the input row is never
+// written); stores use the new row, also held in shared memory.  A store lands in a block that is not taken over: if it was an
 // exchange partner m' + j', it now holds the old block m', whose slots lie before every source
 // a later round reads (sources sit at or past their destinations).  So the ascending rounds stay
-// safe, and the new row goes to a separate output: the other CTAs of the sequence keep reading
-// the old one.
-constexpr int kMaxWin = TV_MAX_NODES / 16 + 2;   // logical blocks spanned by P .. P + N - 1
-
+// safe.  The new row goes to a separate output: the CTA of KV head 0 writes the window, and the
+// sequence's CTAs share the copy of the entries outside it, which no CTA of the call changes.
 __global__ void __launch_bounds__(kThreads) kv_compact_remap_kernel(CompactArgs a) {
   __shared__ CompactCheck c;
   __shared__ int win[kMaxWin];          // new table entries of logical blocks first .. last
@@ -158,15 +162,24 @@ __global__ void __launch_bounds__(kThreads) kv_compact_remap_kernel(CompactArgs 
   const int b = blockIdx.x / a.Hkv, kvh = blockIdx.x % a.Hkv;
   const int bs = a.block_size;
   const int* table = a.block_table + (size_t)b * a.max_blocks;
+  // This CTA's share of the row copy, loaded now so that the loads overlap the checks.
+  constexpr int kPre = 4;
+  const int stride = a.Hkv * kThreads, base = kvh * kThreads + threadIdx.x;
+  int pre[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int i = base + u * stride;
+    pre[u] = i < a.max_blocks ? table[i] : 0;
+  }
   const int st = check_compact(a, b, c);
-  const int first = st ? 0 : c.P / bs;
-  const int nwin = st ? 0 : (c.P + a.N - 1) / bs - first + 1;
+  const int first = st ? 0 : c.first;
+  const int nwin = st ? 0 : c.nwin;
   if (!st) {
     const int P = c.P, L = c.L;
     const int m_lo = (P + bs - 1) / bs, m_hi = (P + L - 1) / bs;
     // one thread per window block: copy its entry, and decide a destination block
     for (int i = threadIdx.x; i < nwin; i += kThreads) {
-      win[i] = table[first + i];
+      win[i] = c.win[i];
       const int m = first + i;
       int j = 0;
       if (m >= m_lo && m <= m_hi) {
@@ -204,17 +217,23 @@ __global__ void __launch_bounds__(kThreads) kv_compact_remap_kernel(CompactArgs 
       int smap = -1;
       if (!st && r < c.L) {
         const int s = c.P + c.path[r];
-        smap = table[s / bs] * bs + s % bs;
+        smap = c.win[s / bs - first] * bs + s % bs;
       }
       a.slot_map[(size_t)b * a.Lmax + r] = smap;
     }
-    for (int i = threadIdx.x; i < a.max_blocks; i += kThreads) {
-      const int w = i - first;
-      a.table_out[(size_t)b * a.max_blocks + i] = (w >= 0 && w < nwin) ? win[w] : table[i];
-    }
+    for (int i = threadIdx.x; i < nwin; i += kThreads) a.table_out[(size_t)b * a.max_blocks + first + i] = win[i];
   }
-  if (st) return;
-  move_entries(a, b, kvh, c, [&](int lb) { return shift[lb - first] ? -1 : win[lb - first]; });
+  if (!st) move_entries(a, b, kvh, c, [&](int lb) { return shift[lb - first] ? -1 : win[lb - first]; });
+  // The rest of the row (all of it for a sequence with an error) is copied unchanged, shared
+  // among the sequence's CTAs.
+  int32_t* out = a.table_out + (size_t)b * a.max_blocks;
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int i = base + u * stride;
+    if (i < a.max_blocks && (i < first || i >= first + nwin)) out[i] = pre[u];
+  }
+  for (int i = base + kPre * stride; i < a.max_blocks; i += stride)
+    if (i < first || i >= first + nwin) out[i] = table[i];
 }
 
 }  // namespace
