@@ -16,7 +16,8 @@
  *
  * then commits the accepted path: the GDN state goes back to the last accepted node's state
  * (qwen35-tree-spec §五 用途 2) and the accepted nodes' KV moves to the contiguous slots after
- * the prefix (handbook chapter, note after the listing: the KV is reused, not recomputed).
+ * the prefix, or whole blocks of it are taken over through the block table (handbook chapter,
+ * note after the listing: the KV is reused, not recomputed).
  *
  * Conventions for every call below
  * --------------------------------
