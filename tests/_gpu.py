@@ -187,7 +187,8 @@ def run_compact(case: W.AttnCase, k_cache: torch.Tensor, v_cache: torch.Tensor, 
 
 def run_compact_remap(k_cache, v_cache, block_table, prefix_len, parents, path, path_len,
                       table_out_fill: int = -7) -> dict:
-    """``tv_kv_compact_remap`` on copies of the given tensors; returns everything on the CPU."""
+    """``tv_kv_compact_remap`` on device copies of the given tensors.  The caches stay on the
+    device (the full-size tests gather rows from them); the small outputs come back as numpy."""
     B = block_table.shape[0]
     kc, vc = to_dev(k_cache), to_dev(v_cache)
     table = to_dev(block_table)
