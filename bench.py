@@ -937,6 +937,9 @@ def run_sweep(args) -> None:
             fn()
         torch.cuda.synchronize()
         s, e = ev(enable_timing=True), ev(enable_timing=True)
+        # queued behind a device-side sleep: the events bracket device time even where a call
+        # takes less time on the device than to issue from Python
+        torch.cuda._sleep(4_000_000)
         s.record()
         for _ in range(iters):
             fn()
