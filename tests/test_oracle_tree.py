@@ -117,6 +117,24 @@ def test_accepted_path_generator_gives_valid_paths():
         assert 1 <= len(p) <= 4 and T.is_valid_path(t, p, len(p))
 
 
+def test_candidate_chains_and_their_paths():
+    """A root with chains numbered depth-first: a valid tree whose chain c starts at node
+    1 + (lengths before c) and runs one node deeper per index; the generated paths run down
+    one chain from the root."""
+    lengths = W.CHAIN_LENGTHS
+    t = W.candidate_chains(lengths)
+    assert T.is_valid_tree(t) and len(t) == 1 + sum(lengths) == 40
+    start = 1
+    for n in lengths:
+        assert t[start] == 0
+        assert T.depths(t)[start:start + n] == list(range(1, n + 1))
+        start += n
+    rng = np.random.default_rng(2)
+    for p in W.candidate_chain_paths(lengths, 200, rng):
+        assert p[0] == 0 and T.is_valid_path(t, p, len(p))
+        assert all(b == a + 1 for a, b in zip(p[1:], p[2:]))
+
+
 # ----------------------------------------------------------------------------- accept walk
 def test_accept_walk_hand_example():
     # 6-node tree of the handbook's printed example; tokens chosen so that the target at the
