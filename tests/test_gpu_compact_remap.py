@@ -198,3 +198,27 @@ def test_full_size_paged_batch(workload):
         assert total > 0
     else:
         assert total == 0
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_long_paths_move_in_several_rounds(hd):
+    """Paths of up to 101 entries: more than one load/store round at hd 256 (32 entries per
+    round) and hd 128 (64).  Both kernels, the whole caches, against the oracle."""
+    t = W.candidate_chains([32, 100])
+    paths = [[0] + list(range(33, 33 + L - 1)) for L in (101, 70, 40, 33)]
+    case = W.attn_case([t] * 4, [0, 15, 17, 33], Hq=2, Hkv=2, hd=hd, seed=9, paths=paths)
+    x = dict(k_cache=case.k_cache, v_cache=case.v_cache, block_table=case.block_table,
+             prefix_len=case.prefix_len, parents=case.parents, path=case.path, path_len=case.path_len)
+    res = _run(x)
+    assert (res["err"] == 0).all()
+    ref = _oracle(x)
+    _compare(res, ref)
+    assert ref[5].sum() >= 4
+    comp = _gpu.run_compact(case, case.k_cache, case.v_cache)
+    assert (comp["err"] == 0).all()
+    kc2, vc2, smap, new_len = A.kv_compact(W.f64(case.k_cache), W.f64(case.v_cache), case.block_table.numpy(),
+                                           case.prefix_len.numpy(), case.parents.numpy(), case.path.numpy(),
+                                           case.path_len.numpy())
+    assert np.array_equal(comp["slot_map"], smap) and np.array_equal(comp["new_len"], new_len)
+    assert np.array_equal(_gpu.f32np(comp["k_cache"]), kc2)
+    assert np.array_equal(_gpu.f32np(comp["v_cache"]), vc2)
