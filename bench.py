@@ -739,6 +739,259 @@ def block_table_compaction_report(rnd, torch, tv, W, iters: int = 20) -> dict:
             "copy_form_ms": round(ms_copy, 5), "block_table_form_ms": round(ms_remap, 5)}
 
 
+# ----------------------------------------------------------------------------- wide-tree sweep
+HYBRID_GDN_LAYERS, HYBRID_ATTN_LAYERS, HYBRID_PREFIX = 24, 8, 8192
+GRID_N = (15, 40, 64, 128, 256)
+GRID_B = (1, 8, 32, 128)
+
+
+def device_timed(torch, fn, iters: int, launches: int) -> float:
+    """Mean device time of ``fn`` (ms) over ``iters`` calls issued behind a device-side sleep,
+    so that the events bracket device time even where issuing the launches from Python takes
+    longer than running them (the small trees are launch-latency-bound)."""
+    fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(2e6 + 4e4 * launches * iters))
+    s.record()
+    for _ in range(iters):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def hybrid_point(torch, tv, W, peaks, B: int, N: int, trees, gdn_layers: int, attn_layers: int, prefix: int,
+                 seed: int, iters: int = 3) -> dict:
+    """One verify round of a synthetic hybrid stack (``attn_layers`` groups of gdn_layers /
+    attn_layers GDN layers and one attention layer; 3:1 at 24 + 8) over B sequences of N-node
+    trees, in fork mode and in TreeWY mode, each followed by the accept walk, the stacked GDN
+    commit and the compaction of every attention layer's cache.  Per mode: the round's device
+    time, the GDN part alone (verify + commit per layer), and the measured peak of device memory
+    the mode adds (torch.cuda.max_memory_allocated over the mode's buffers and its rounds; the
+    library allocates nothing).  Fork mode is run only where its snapshots fit the free device
+    memory; otherwise the point reports the bytes it would need."""
+    import numpy as np
+    dev = torch.device("cuda", torch.cuda.current_device())
+    H, d, Hq, Hkv, hd = 16, 128, 16, 4, 128
+    L = gdn_layers
+    i32 = dict(dtype=torch.int32, device=dev)
+    parents = torch.tensor(np.array(trees, dtype=np.int32), device=dev)
+    rng = np.random.default_rng(seed + 17)
+    paths = [W.random_accepted_path(t, rng, 4) for t in trees]
+    Lmax = max(len(p) for p in paths)
+    p_np = np.array([p + [-1] * (Lmax - len(p)) for p in paths], dtype=np.int32)
+    l_np = np.array([len(p) for p in paths], dtype=np.int32)
+    draft, target = W.walk_tokens(trees, p_np, l_np, seed=seed + 18)
+    draft, target = draft.to(dev), target.to(dev)
+    g = W.device_gdn_stack(L, B, N, H, d, seed=seed + 19, device=dev)
+    attn = [W.device_attn_layer(B, N, prefix, Hq, Hkv, hd, seed=seed + 100 + j, device=dev) for j in range(attn_layers)]
+    ws = None
+    if attn_layers:
+        ws = torch.empty(tv.tv_tree_attn_workspace_size(B, N, Hq, Hkv, hd, attn[0]["block_table"].shape[1]),
+                         dtype=torch.uint8, device=dev)
+    a_out = torch.empty((B, N, Hq, hd), dtype=torch.bfloat16, device=dev)
+    path, plen, nxt = torch.empty((B, Lmax), **i32), torch.empty((B,), **i32), torch.empty((B,), **i32)
+    smap, new_len = torch.empty((B, Lmax), **i32), torch.empty((B,), **i32)
+    err = torch.zeros((8 + L, B), **i32)
+    o = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=dev)
+    per_group = L // attn_layers if attn_layers else L
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    max_depth = max(max(_depths(t)) for t in trees)
+
+    def attn_layer(j):
+        x = attn[j]
+        tv.tv_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"], x["block_table"],
+                        x["prefix_len"], parents, a_out, ws, err[4], rope_theta=1e6)
+
+    def compactions():
+        for x in attn:
+            tv.tv_kv_compact(x["k_cache"], x["v_cache"], x["block_table"], x["prefix_len"], parents, path, plen,
+                             smap, new_len, err[5])
+
+    def attn_only():
+        for j in range(attn_layers):
+            attn_layer(j)
+        compactions()
+
+    tv.tv_accept_walk(parents, draft, target, path, plen, nxt, err[1])   # the paths the compactions read
+    torch.cuda.synchronize()
+    out = {"B": B, "N": N, "max_depth": max_depth}
+    if attn_layers:
+        a_ms = device_timed(torch, attn_only, iters, 5 * attn_layers)
+        ab = attn_bytes([prefix] * B, N, Hq, Hkv, hd)
+        af = attn_flops([prefix] * B, [_depths(t) for t in trees], Hq, hd)
+        out["attention"] = {"ms_per_layer_with_compaction": round(a_ms / attn_layers, 5),
+                            "frac_hbm": round(ab / (a_ms / attn_layers * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                            "tflops": round(af / (a_ms / attn_layers * 1e-3) / 1e12, 2)}
+    for mode in ("fork", "wy"):
+        state_bytes = (L * B * N * H * d * d * 2 if mode == "fork" else L * B * N * H * (d + 1) * 4)
+        torch.cuda.synchronize()
+        free, total = torch.cuda.mem_get_info()
+        reserve_free = torch.cuda.memory_reserved() - torch.cuda.memory_allocated()
+        slots = min(FORK_SLOTS, L)
+        extra = B * N * H * (d + 1) * 4 * slots + L * B * H * d * d * 2 if mode == "fork" else L * B * H * d * d * 2
+        if state_bytes + extra > free + reserve_free - (2 << 30):
+            out[mode] = {"exceeds_hbm": True, "state_bytes_predicted": state_bytes,
+                         "free_bytes": free + reserve_free}
+            continue
+        S0 = g["S0"].clone()            # the mode's resident state, an input of both modes
+        torch.cuda.synchronize()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        if mode == "fork":
+            states = torch.empty((L, B, N, H, d, d), dtype=torch.bfloat16, device=dev)
+            w = [torch.empty((B, N, H, d), dtype=torch.float32, device=dev) for _ in range(slots)]
+            lgs = [torch.empty((B, N, H), dtype=torch.float32, device=dev) for _ in range(slots)]
+            w_ready = [torch.cuda.Event() for _ in range(L)]
+            slot_free = [torch.cuda.Event() for _ in range(slots)]
+        else:
+            pv = torch.empty((L, B, N, H, d), dtype=torch.float32, device=dev)
+            lg = torch.empty((L, B, N, H), dtype=torch.float32, device=dev)
+
+        def gdn_layer(l):
+            if mode == "wy":
+                tv.tv_gdn_tree_verify_wy(g["q"][l], g["k"][l], g["v"][l], g["alpha"][l], g["beta"][l], S0[l], parents,
+                                         o, pv[l], lg[l], err[0])
+                return
+            k = l % slots
+            if l >= slots:
+                main.wait_event(slot_free[k])
+            tv.tv_gdn_tree_verify_wy(g["q"][l], g["k"][l], g["v"][l], g["alpha"][l], g["beta"][l], S0[l], parents,
+                                     o, w[k], lgs[k], err[8 + l])
+            w_ready[l].record(main)
+            side.wait_event(w_ready[l])
+            tv.tv_gdn_fork_materialize(g["k"][l], g["alpha"][l], S0[l], parents, w[k], states[l], err[8 + l],
+                                       stream=side)
+            slot_free[k].record(side)
+
+        def commit():
+            tv.tv_accept_walk(parents, draft, target, path, plen, nxt, err[1])
+            if mode == "fork":
+                tv.tv_gdn_commit_layers(tv.TV_MODE_FORK, path, plen, parents, S0, err[2], node_states=states)
+            else:
+                tv.tv_gdn_commit_layers(tv.TV_MODE_WY, path, plen, parents, S0, err[3], pseudo_v=pv, log_gamma=lg,
+                                        k=g["k"])
+
+        def gdn_only():
+            for l in range(L):
+                gdn_layer(l)
+            main.wait_stream(side)
+            commit()
+
+        def hybrid():
+            for l in range(L):
+                gdn_layer(l)
+                if attn_layers and (l + 1) % per_group == 0:
+                    attn_layer((l + 1) // per_group - 1)
+            main.wait_stream(side)
+            commit()
+            if attn_layers:
+                compactions()
+
+        nl = L * (2 if mode == "fork" else 1)
+        g_ms = device_timed(torch, gdn_only, iters, nl + 2)
+        r_ms = device_timed(torch, hybrid, iters, nl + 2 + 5 * attn_layers) if attn_layers else g_ms
+        peak = torch.cuda.max_memory_allocated() - base
+        assert int(err.abs().sum()) == 0, (mode, B, N, err.cpu().tolist())
+        gb = gdn_bytes(B, N, H, d, d, 2, 2, "fork" if mode == "fork" else "wy")
+        per_layer = g_ms / L
+        out[mode] = {"round_ms": round(r_ms, 4), "round_nodes_per_s": round(B * N / (r_ms * 1e-3)),
+                     "gdn_ms_per_layer": round(per_layer, 5),
+                     "gdn_nodes_per_s_per_layer": round(B * N / (per_layer * 1e-3)),
+                     "gdn_frac_hbm": round(gb / (per_layer * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                     "state_bytes": state_bytes, "peak_bytes_measured": int(peak)}
+        if mode == "fork":
+            del states, w, lgs
+        else:
+            del pv, lg
+        del S0
+        torch.cuda.synchronize()
+    del g, attn, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def wide_tree_sweep(torch, tv, W, peaks, Bs=GRID_B, Ns=GRID_N, iters: int = 3) -> dict:
+    """The wide-tree sweep on the synthetic 3:1 hybrid stack: 24 GDN layers (H=16, d=128) and 8
+    tree-attention layers (16q/4kv, hd 128, prefix 8192), bf16, random dynamic trees (1..4
+    children per node, depth <= 8) of N nodes at batch B, fork vs TreeWY."""
+    torch.cuda.empty_cache()
+    rows = []
+    for B in Bs:
+        for N in Ns:
+            trees = W.sweep_trees(N, B)
+            rows.append(hybrid_point(torch, tv, W, peaks, B, N, trees, HYBRID_GDN_LAYERS, HYBRID_ATTN_LAYERS,
+                                     HYBRID_PREFIX, seed=10 * N + B, iters=iters))
+    return {"workload": "3:1 hybrid stack, 24 GDN layers (H=16, d=128) + 8 tree-attention layers (16q/4kv, hd 128, "
+                        "prefix 8192), bf16, random dynamic trees (1..4 children, depth <= 8), inputs drawn on the device",
+            "pages_bytes_per_checkpoint": checkpoint_bytes(24, 16, 128, 128, 2),
+            "timing": "device time of whole rounds issued behind a device-side sleep, mean of 3",
+            "rows": rows}
+
+
+def small_config_lines(torch, tv, W, peaks) -> dict:
+    """Timed lines for the two launch-latency-bound single-sequence workloads: the small fp32
+    layer (B=1, H=2, d=64, the 7-node tree) and the single bf16 layer (B=1, H=16, d=128: a chain
+    of 5 nodes vs the 15-node k=2 d=3 tree, plus its attention layer, 16q/4kv, hd 128, prefix
+    4096), each mode's verify and commit queued behind a device-side sleep."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lines = {}
+
+    def gdn_modes(case):
+        x = {k: getattr(case, k).contiguous().to(dev) for k in ("q", "k", "v", "alpha", "beta", "S0", "parents")}
+        B, N, H, dk, dv = case.shape
+        path, plen = case.path.to(dev), case.path_len.to(dev)
+        out = torch.empty((B, N, H, dv), dtype=x["q"].dtype, device=dev)
+        st = torch.empty((B, N, H, dv, dk), dtype=x["S0"].dtype, device=dev)
+        pv = torch.empty((B, N, H, dv), dtype=torch.float32, device=dev)
+        lg = torch.empty((B, N, H), dtype=torch.float32, device=dev)
+        err = torch.zeros((4, B), dtype=torch.int32, device=dev)
+        S0f, S0w = x["S0"].clone(), x["S0"].clone()
+
+        def fork():
+            tv.tv_gdn_tree_verify_fork(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S0f, x["parents"], out, st,
+                                       err[0], q_scale=case.q_scale)
+            tv.tv_gdn_commit(tv.TV_MODE_FORK, path, plen, x["parents"], S0f, err[1], node_states=st)
+
+        def wy():
+            tv.tv_gdn_tree_verify_wy(x["q"], x["k"], x["v"], x["alpha"], x["beta"], S0w, x["parents"], out, pv, lg,
+                                     err[2], q_scale=case.q_scale)
+            tv.tv_gdn_commit(tv.TV_MODE_WY, path, plen, x["parents"], S0w, err[3], pseudo_v=pv, log_gamma=lg,
+                             k=x["k"])
+
+        r = {}
+        for name, fn in (("fork", fork), ("wy", wy)):
+            ms = device_timed(torch, fn, 50, 2)
+            r[name] = {"verify_commit_ms": round(ms, 5), "nodes_per_s": round(B * N / (ms * 1e-3))}
+        assert int(err.abs().sum()) == 0, err
+        return r
+
+    lines["small_fp32_layer"] = dict(workload="1 GDN layer, B=1, H=2, d=64, fp32, 7-node k=2 d=2 tree",
+                                     bound="launch latency", **gdn_modes(W.small_fp32_case()))
+    for tree in ("chain", "tree"):
+        case = W.single_layer_gdn_case(tree)
+        a = W.single_layer_attn_case(tree)
+        B, N, Hq, Hkv, hd = a.shape
+        x = {k: getattr(a, k).contiguous().to(dev) for k in
+             ("q", "k_new", "v_new", "k_cache", "v_cache", "block_table", "prefix_len", "parents")}
+        out = torch.empty((B, N, Hq, hd), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(tv.tv_tree_attn_workspace_size(B, N, Hq, Hkv, hd, x["block_table"].shape[1]),
+                         dtype=torch.uint8, device=dev)
+        err = torch.zeros((B,), dtype=torch.int32, device=dev)
+        a_ms = device_timed(torch, lambda: tv.tv_tree_attn(x["q"], x["k_new"], x["v_new"], x["k_cache"], x["v_cache"],
+                                                           x["block_table"], x["prefix_len"], x["parents"], out, ws,
+                                                           err, rope_theta=1e6), 50, 4)
+        assert int(err.abs().sum()) == 0, err
+        name = "single_bf16_layer_chain5" if tree == "chain" else "single_bf16_layer_k2d3"
+        lines[name] = dict(workload=f"1 GDN layer, B=1, H=16, d=128, bf16, {N}-node "
+                                    f"{'chain' if tree == 'chain' else 'k=2 d=3 tree'}; attention 16q/4kv hd 128 "
+                                    f"prefix 4096", bound="launch latency", **gdn_modes(case),
+                           attention={"ms": round(a_ms, 5), "nodes_per_s": round(N / (a_ms * 1e-3))})
+    return lines
+
+
 def run_ours(args) -> None:
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -826,6 +1079,7 @@ def run_ours(args) -> None:
         one_pass = one_pass_fork_report(rnd, torch, tv)
         remap = block_table_compaction_report(rnd, torch, tv, W)
     peaks = load_peaks()
+    step_peak = torch.cuda.max_memory_allocated()
     B, N, H, dk, dv = rnd.B, rnd.N, rnd.H, rnd.dk, rnd.dv
     L_sum = int(rnd.gdn_host[0].path_len.sum())
     a = rnd.attn_host
@@ -871,19 +1125,43 @@ def run_ours(args) -> None:
     mem = {"fork_checkpoint_bytes": rnd.fork_state_bytes, "wy_pseudo_value_bytes": rnd.wy_state_bytes,
            "pages_bytes_per_checkpoint": checkpoint_bytes(24, 16, 128, 128, 2),
            "pages_accounting_fork_bytes": checkpoint_bytes(24, 16, 128, 128, 2) * B * N,
-           "peak_allocated_bytes": torch.cuda.max_memory_allocated()}
+           "peak_allocated_bytes": step_peak}
+    # The per-mode figures below run on a clean device: the step's buffers are freed first.
+    trees_b64 = [list(t) for t in rnd.gdn_host[0].trees]
+    fork_rate = rows["fork_verify"]["nodes_per_s_per_layer"]
+    wy_rate = rows["wy_verify"]["nodes_per_s_per_layer"]
+    layers, aB, launches_per_step = rnd.layers, rnd.aB, rnd.launches_per_step
+    del rnd
+    import gc
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    per_mode = sweep = small = None
+    if not args.no_grid and world == 1:
+        # measured peak device memory per mode on the batch-64 GDN stack alone (24 layers, verify +
+        # accept walk + stacked commit; the library allocates nothing, so this is every buffer the
+        # mode adds to the inputs)
+        pm = hybrid_point(torch, tv, W, peaks, B, N, trees_b64, LAYERS, 0, 0, seed=64)
+        per_mode = {m: {"peak_bytes_measured": pm[m]["peak_bytes_measured"], "state_bytes": pm[m]["state_bytes"],
+                        "gdn_ms_per_layer_alone": pm[m]["gdn_ms_per_layer"]} for m in ("fork", "wy")}
+        per_mode["pages_accounting_fork_bytes"] = checkpoint_bytes(24, 16, 128, 128, 2) * B * N
+        small = small_config_lines(torch, tv, W, peaks)
+        sweep = wide_tree_sweep(torch, tv, W, peaks)
     line = {"metric": METRIC, "value": round(value, 1), "unit": "nodes/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "ms_per_step_min": round(step_ms[0], 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "layers": rnd.layers, "global_batch": B * world,
-                       "nodes_per_tree": N, "attn_batch": rnd.aB * world,
+            "config": {"workload": WORKLOAD, "layers": layers, "global_batch": B * world,
+                       "nodes_per_tree": N, "attn_batch": aB * world,
                        "l2": "working set >> 129 MB L2 (fork checkpoints 1.3 GB per layer)",
                        "parallelism": f"replicas x{world}"},
-            "gpu_launches": rnd.launches_per_step * args.steps, "clocks": clk, "roofline": roof,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk, "roofline": roof,
+            "fork_nodes_per_s_per_layer": fork_rate, "wy_nodes_per_s_per_layer": wy_rate,
+            "peak_memory_per_mode": per_mode,
             "rows": rows, "accepted_tokens": accepted, "state_memory": mem, "selective_fork": selective,
             "lazy_commit": lazy,
             "one_pass_fork": one_pass, "block_table_compaction": remap, "e2e": e2e,
+            "small_workloads": small, "wide_tree_sweep": sweep,
             "cpu_baseline": cpu_base}
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -987,6 +1265,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-reports", action="store_true",
                     help="skip the selective-fork, lazy-commit and one-pass-fork reports after the timed steps")
+    ap.add_argument("--no-grid", action="store_true",
+                    help="skip the per-mode memory, the small workloads and the wide-tree sweep after the step")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the benchmark: per-layer GDN verify times across tree sizes (one JSON line)")
     args = ap.parse_args()

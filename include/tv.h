@@ -69,7 +69,8 @@ enum tv_status {
   TV_ERR_CUDA = -5,
   TV_ERR_TIMEOUT = -6,
   TV_ERR_CAPACITY = -7,     /* block table too short for prefix_len + N slots */
-  TV_ERR_BAD_BLOCK = -8,    /* a block-table entry outside [0, num_blocks) */
+  TV_ERR_BAD_BLOCK = -8,    /* a block-table entry outside [0, num_blocks), or (compaction)
+                               two logical blocks of the tree's window on one physical block */
   TV_ERR_SCRATCH = -9       /* tv_tree_attn_static: the call needs more than
                                TV_STATIC_SCRATCH_BYTES of scratch */
 };
@@ -391,10 +392,13 @@ TV_API int tv_tree_attn(const void* q, const void* k_new, const void* v_new, voi
  *  - Size limit: when tv_tree_attn_workspace_size(B, N, Hq, Hkv, hd, max_blocks, block_size)
  *    exceeds TV_STATIC_SCRATCH_BYTES the call returns TV_ERR_SCRATCH before any CUDA call
  *    and launches nothing; use tv_tree_attn with a workspace for such sizes.
- *  - Set-up: the first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress; a failure returns TV_ERR_CUDA) and caches it.  That lookup may
- *    load a module, so make the first call on each device in set-up code, before any stream
- *    capture.
+ *  - Argument errors: every host-side check of tv_tree_attn (null or misaligned pointers,
+ *    sizes) runs before any CUDA call, as does the size limit below.
+ *  - Set-up: the first call in each CUDA context looks up the array's device address
+ *    (cudaGetSymbolAddress; a failure returns TV_ERR_CUDA) and caches it with that context.
+ *    That lookup may load a module, so make the first call on each device in set-up code,
+ *    before any stream capture.  A call made in a new context of the device (e.g. after
+ *    cudaDeviceReset) looks the address up again: the old one died with the old context.
  *  - Shared state: the scratch is one array per device for the whole process.  Its contents
  *    persist between calls; nothing in it has to start at zero (every call writes each
  *    scratch entry it reads).  Two calls whose execution overlaps on the same device (other
@@ -424,6 +428,10 @@ TV_API int tv_tree_attn_static(const void* q, const void* k_new, const void* v_n
  *   new_len     [B] int32         out prefix_len + L (prefix_len on error)
  *   err         [B] int32         out 0, TV_ERR_BAD_TREE, TV_ERR_BAD_PATH, TV_ERR_CAPACITY
  *                                 or TV_ERR_BAD_BLOCK
+ * Precondition, checked: the table entries of the logical blocks that hold slots prefix_len ..
+ * prefix_len + N - 1 (the window every source and destination lies in) are distinct physical
+ * blocks.  Were two of them the same block, a store could overwrite a source before it is read;
+ * such a sequence reports TV_ERR_BAD_BLOCK and is skipped.
  * Supported: hd in {64, 128, 256}; block_size = 16.
  * ---------------------------------------------------------------------------------------- */
 TV_API int tv_kv_compact(void* k_cache, void* v_cache, int num_blocks, const int32_t* block_table,
@@ -457,6 +465,9 @@ TV_API int tv_kv_compact(void* k_cache, void* v_cache, int num_blocks, const int
  *   prefix_len, parents, accepted_path, accepted_len, slot_map, new_len, err: as for
  *                                                tv_kv_compact (slot_map under the old rows)
  *   remapped        [B] int32               out  exchanges made (0 on error)
+ * Precondition, checked as for tv_kv_compact: the window's table entries are distinct (an
+ * exchange of two entries naming one block would lose none but move data twice);
+ * TV_ERR_BAD_BLOCK otherwise, the row copied unchanged.
  * Supported: hd in {64, 128, 256}; block_size = 16; N <= TV_MAX_NODES.
  * ---------------------------------------------------------------------------------------- */
 TV_API int tv_kv_compact_remap(void* k_cache, void* v_cache, int num_blocks, const int32_t* block_table,
@@ -487,6 +498,23 @@ TV_API int tv_kv_compact_remap(void* k_cache, void* v_cache, int num_blocks, con
 TV_API int tv_accept_walk(const int32_t* parents, const int32_t* draft_tokens, const int32_t* target_tokens,
                           int B, int N, int Lmax, int32_t* accepted_path, int32_t* accepted_len,
                           int32_t* next_token, int32_t* err, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * tv_test_bounded_wait -- test support for the bounded device waits.
+ *
+ * The pages have no counterpart: this checks a property of the library.  Every wait of the
+ * tensor-core kernels on a shared-memory mbarrier (copies landed, MMAs done) gives up after a
+ * bounded number of polls, and the kernel then reports TV_ERR_TIMEOUT in err[b] and returns.
+ * This call launches one thread that runs that same wait on a barrier nothing arrives on (no
+ * copy or MMA is in flight), so a test can make it run out:
+ *   max_polls   polls before giving up; 0 = the limit the library's kernels use
+ *   arrive      nonzero: the thread arrives on the barrier first, so the wait succeeds
+ *   status      [1] int32 out   TV_OK or TV_ERR_TIMEOUT
+ *   elapsed_ns  [1] int64 out   device time the wait took (the %globaltimer clock)
+ * Returns TV_ERR_INVALID_ARG for a null or misaligned pointer.
+ * ---------------------------------------------------------------------------------------- */
+TV_API int tv_test_bounded_wait(unsigned max_polls, int arrive, int32_t* status, int64_t* elapsed_ns,
+                                tv_stream_t stream);
 
 #ifdef __cplusplus
 }

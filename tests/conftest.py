@@ -27,3 +27,13 @@ def read_golden(name: str) -> list[str]:
 @pytest.fixture
 def golden():
     return read_golden
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Worst parity margins of the bf16-I/O comparisons that ran (GPU tests only)."""
+    mod = sys.modules.get("_gpu")
+    if mod is None or not getattr(mod, "MARGINS", None):
+        return
+    terminalreporter.section("parity margins (bf16 I/O; bound = 2e-2 RMS(ref) + 2^-8 |ref| if stored in bf16)")
+    for line in mod.margin_summary():
+        terminalreporter.write_line(line)

@@ -48,7 +48,7 @@ def test_enum_values_match_header():
 
 def test_status_strings_and_version():
     assert tv.status_string(0) == "ok"
-    for code in range(-8, 0):
+    for code in range(-9, 0):
         assert tv.status_string(code) and tv.status_string(code) != "unknown status"
     assert tv.status_string(99) == "unknown status"
     assert tv.lib.tv_version() >= 100
@@ -168,3 +168,29 @@ def test_block_table_compaction_argument_checks():
     assert call(a15=32) == tv.TV_ERR_UNSUPPORTED
     assert call(a8=257) == tv.TV_ERR_UNSUPPORTED
     del keep
+
+
+def test_static_attention_rejects_bad_arguments_before_any_cuda_call():
+    # Hq % Hkv != 0 (the workspace size is then 0) and null pointers: refused by the host-side
+    # checks of tv_tree_attn, which run before the scratch lookup (no CUDA call is made, so this
+    # holds without a GPU).
+    L = tv.lib
+    assert L.tv_tree_attn_static(None, None, None, None, None, 8, None, 4, None, None,
+                                 1, 3, 3, 2, 64, 16, 1e6, 0.125, None, None, None) == tv.TV_ERR_INVALID_ARG
+    assert L.tv_tree_attn_static(None, None, None, None, None, 8, None, 4, None, None,
+                                 1, 3, 4, 2, 64, 16, 1e6, 0.125, None, None, None) == tv.TV_ERR_INVALID_ARG
+
+
+@cpu_only
+def test_static_attention_rejects_unsupported_sizes_before_any_cuda_call():
+    keep, p = _fake()
+    a = [p] * 5 + [4, p, 2, p, p, 1, 3, 4, 2, 96, 16, 1e6, 0.1, p, p, None]
+    assert tv.lib.tv_tree_attn_static(*a) == tv.TV_ERR_UNSUPPORTED
+    a = [p] * 5 + [4, p, 2, p, p, 1, 3, 4, 2, 64, 16, 0.0, 0.1, p, p, None]     # rope_theta <= 0
+    assert tv.lib.tv_tree_attn_static(*a) == tv.TV_ERR_INVALID_ARG
+    del keep
+
+
+def test_bounded_wait_probe_rejects_null_outputs():
+    assert tv.lib.tv_test_bounded_wait(100, 0, None, None, None) == tv.TV_ERR_INVALID_ARG
+    assert tv.status_string(tv.TV_ERR_TIMEOUT) == "device wait timed out"

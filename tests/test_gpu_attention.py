@@ -30,7 +30,7 @@ def _check_attn(case, batch=None):
         vg = A.logical_rows(vc_got, tab, P + N)
         assert np.array_equal(kg[:P], A.logical_rows(f["k_cache"], tab, P))
         assert np.array_equal(vg[:P], A.logical_rows(f["v_cache"], tab, P))
-        _gpu.assert_close(kg[P:], kr_ref[b], "bf16", "rotated node keys in cache")
+        _gpu.assert_close(kg[P:], kr_ref[b], "bf16", "rotated node keys in cache", stored="bf16")
         assert np.array_equal(vg[P:], f["v_new"][b])
     return res
 
@@ -87,8 +87,10 @@ def test_paged_b32_full_size_sampled():
         assert np.array_equal(A.logical_rows(vc_comp, tab, n), A.logical_rows(vc2, tab, n))
 
 
-@pytest.mark.parametrize("N,B", [(40, 4), (128, 2)])
+@pytest.mark.parametrize("N,B", [(40, 4), (128, 2), (256, 2), (40, 128)])
 def test_wide_tree_attention_layer_sampled(N, B):
+    """Attention layers of the wide-tree sweep (16q/4kv, hd 128, prefix 8192), up to N=256 and
+    B=128; the first and last sequences against the oracle."""
     case = W.sweep_attn_layer(N, B)
     _check_attn(case, batch=[0, B - 1])
 
@@ -135,3 +137,35 @@ def test_compaction_overlaps_and_errors():
     assert np.array_equal(comp["new_len"], new_len)
     assert np.array_equal(_gpu.f32np(comp["k_cache"]), kc2)
     assert np.array_equal(_gpu.f32np(comp["v_cache"]), vc2)
+
+
+@pytest.mark.parametrize("form", ["move", "remap"])
+def test_compaction_rejects_a_window_with_a_repeated_block(form):
+    # Logical blocks 1 and 2 of sequence 1 (its tree's slots 20 .. 35) name one physical block:
+    # a store could overwrite a source before it is read, so the sequence is refused and its
+    # cache left as it was; sequence 0 is compacted as usual.
+    tree = [-1, 0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14]
+    paths = [[0, 1, 2, 3], [0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15]]
+    case = W.attn_case([tree] * 2, [20, 20], Hq=2, Hkv=2, hd=64, seed=6, paths=paths)
+    case.block_table[1, 2] = case.block_table[1, 1]
+    f = _gpu.attn_f64(case)
+    if form == "move":
+        comp = _gpu.run_compact(case, case.k_cache, case.v_cache)
+        kc, vc = _gpu.f32np(comp["k_cache"]), _gpu.f32np(comp["v_cache"])
+    else:
+        comp = _gpu.run_compact_remap(case.k_cache, case.v_cache, case.block_table, case.prefix_len, case.parents,
+                                      case.path, case.path_len)
+        kc, vc = _gpu.f32np(comp["k_cache"].cpu()), _gpu.f32np(comp["v_cache"].cpu())
+        assert np.array_equal(comp["table"][1], case.block_table.numpy()[1])
+        assert int(comp["remapped"][1]) == 0
+    assert comp["err"].tolist() == [0, tv.TV_ERR_BAD_BLOCK]
+    assert comp["new_len"][1] == 20 and (comp["slot_map"][1] == -1).all()
+    for blk in set(case.block_table.numpy()[1]):
+        assert np.array_equal(kc[blk], f["k_cache"][blk]) and np.array_equal(vc[blk], f["v_cache"][blk])
+    kc2, vc2, smap, new_len = A.kv_compact(f["k_cache"], f["v_cache"], f["block_table"][:1], f["prefix_len"][:1],
+                                           f["parents"][:1], case.path.numpy()[:1], case.path_len.numpy()[:1])
+    assert np.array_equal(comp["slot_map"][0], smap[0]) and comp["new_len"][0] == new_len[0]
+    tab = f["block_table"][0]
+    n = int(new_len[0])
+    assert np.array_equal(A.logical_rows(kc, tab, n), A.logical_rows(kc2, tab, n))
+

@@ -66,7 +66,9 @@ def _cases():
     a = W.single_layer_attn_case("tree")                                        # hd 128, P 4096
     b = W.attn_case([W.random_tree(33, rng) for _ in range(4)], [0, 17, 300, 2049],
                     Hq=8, Hkv=2, hd=256, seed=5)                                # hd 256, ragged
-    return a, b
+    c = W.attn_case([W.random_tree(7, rng) for _ in range(3)], [0, 5, 70],
+                    Hq=4, Hkv=2, hd=64, seed=6)                                 # hd 64: CUDA-core partials
+    return a, b, c
 
 
 @pytest.mark.gpu

@@ -44,7 +44,7 @@ EXPORTED = ("tv_status_string", "tv_last_cuda_error", "tv_version", "tv_tree_pre
             "tv_accept_walk", "tv_gdn_tree_verify_fork_selective", "tv_gdn_commit_selective",
             "tv_gdn_tree_verify_wy_lazy", "tv_gdn_fork_workspace_size", "tv_gdn_tree_verify_fork_ws",
             "tv_gdn_fork_materialize", "tv_gdn_fork_materialize_selective", "tv_gdn_commit_layers",
-            "tv_kv_compact_remap")
+            "tv_kv_compact_remap", "tv_test_bounded_wait")
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -81,6 +81,7 @@ _SIGNATURES = {
     "tv_kv_compact": (_I, [_P, _P, _I, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "tv_kv_compact_remap": (_I, [_P, _P, _I, _P, _P, _I, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                  _P]),
+    "tv_test_bounded_wait": (_I, [ctypes.c_uint, _I, _P, _P, _P]),
 }
 
 
@@ -335,3 +336,11 @@ def tv_accept_walk(parents, draft_tokens, target_tokens, accepted_path, accepted
     _check(lib.tv_accept_walk(_ptr(parents), _ptr(draft_tokens), _ptr(target_tokens), B, N, accepted_path.shape[1],
                               _ptr(accepted_path), _ptr(accepted_len), _ptr(next_token), _ptr(err), _stream(stream)),
            "tv_accept_walk")
+
+
+def tv_test_bounded_wait(max_polls: int, arrive: bool, status, elapsed_ns, stream=None) -> None:
+    """One thread waits on a shared-memory barrier with the library's bounded wait (nothing
+    arrives unless ``arrive``): status [1] int32 gets TV_OK or TV_ERR_TIMEOUT, elapsed_ns [1]
+    int64 the device time of the wait.  max_polls 0 = the limit the kernels use."""
+    _check(lib.tv_test_bounded_wait(int(max_polls), int(bool(arrive)), _ptr(status), _ptr(elapsed_ns),
+                                    _stream(stream)), "tv_test_bounded_wait")

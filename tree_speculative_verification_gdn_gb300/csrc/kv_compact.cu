@@ -64,6 +64,10 @@ __device__ int check_compact(const CompactArgs& a, int b, CompactCheck& c) {
     c.nwin = last - first + 1;
   }
   if (__syncthreads_or(bad_path)) return TV_ERR_BAD_PATH;
+  // The window's entries are in c.win (the barrier above).  Two logical blocks of the window on
+  // one physical block would let a store overwrite a source before it is read.
+  for (int i = threadIdx.x; i <= last - first; i += kThreads)
+    for (int u = 0; u < i; ++u) bad_block |= c.win[u] == c.win[i];
   if (__syncthreads_or(bad_block)) return TV_ERR_BAD_BLOCK;
   return 0;
 }

@@ -272,13 +272,15 @@ size_t tv_tree_attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int ma
   return tv::attn_workspace_size(B, N, Hq, Hkv, hd, max_blocks, block_size);
 }
 
-int tv_tree_attn(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
-                 int num_blocks, const int32_t* block_table, int max_blocks, const int32_t* prefix_len,
-                 const int32_t* parents, int B, int N, int Hq, int Hkv, int hd, int block_size,
-                 float rope_theta, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
-                 int32_t* err, tv_stream_t stream) {
+}  // extern "C"
+
+int tv::tree_attn_check_args(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                             const void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
+                             const int32_t* prefix_len, const int32_t* parents, int B, int N, int Hq, int Hkv,
+                             int hd, int block_size, float rope_theta, float sm_scale, const void* out,
+                             const int32_t* err) {
   if (!a16(q) || !a16(k_new) || !a16(v_new) || !a16(k_cache) || !a16(v_cache) || !a4(block_table) ||
-      !a4(prefix_len) || !a4(parents) || !a16(out) || !a16(workspace) || !a4(err))
+      !a4(prefix_len) || !a4(parents) || !a16(out) || !a4(err))
     return TV_ERR_INVALID_ARG;
   if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || num_blocks < 1 || max_blocks < 1 ||
       !(rope_theta > 0.f) || !isfinite(rope_theta) || !isfinite(sm_scale))
@@ -286,6 +288,21 @@ int tv_tree_attn(const void* q, const void* k_new, const void* v_new, void* k_ca
   if (N > TV_MAX_NODES || (hd != 64 && hd != 128 && hd != 256) || block_size != TV_BLOCK_SIZE)
     return TV_ERR_UNSUPPORTED;
   if (B > 65535) return TV_ERR_UNSUPPORTED;
+  return TV_OK;
+}
+
+extern "C" {
+
+int tv_tree_attn(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                 int num_blocks, const int32_t* block_table, int max_blocks, const int32_t* prefix_len,
+                 const int32_t* parents, int B, int N, int Hq, int Hkv, int hd, int block_size,
+                 float rope_theta, float sm_scale, void* out, void* workspace, size_t workspace_bytes,
+                 int32_t* err, tv_stream_t stream) {
+  const int st = tv::tree_attn_check_args(q, k_new, v_new, k_cache, v_cache, num_blocks, block_table, max_blocks,
+                                          prefix_len, parents, B, N, Hq, Hkv, hd, block_size, rope_theta,
+                                          sm_scale, out, err);
+  if (st != TV_OK) return st;
+  if (!a16(workspace)) return TV_ERR_INVALID_ARG;
   if (workspace_bytes < tv::attn_workspace_size(B, N, Hq, Hkv, hd, max_blocks, block_size))
     return TV_ERR_INVALID_ARG;
   tv::AttnArgs a{q, k_new, v_new, k_cache, v_cache, num_blocks, block_table, max_blocks, prefix_len, parents,

@@ -119,6 +119,12 @@ struct AttnArgs {
   int32_t* err;
 };
 size_t attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int block_size);
+// Host-side argument checks of tv_tree_attn other than the workspace: TV_OK or the status the
+// call returns.  Makes no CUDA call.
+int tree_attn_check_args(const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                         const void* v_cache, int num_blocks, const int32_t* block_table, int max_blocks,
+                         const int32_t* prefix_len, const int32_t* parents, int B, int N, int Hq, int Hkv, int hd,
+                         int block_size, float rope_theta, float sm_scale, const void* out, const int32_t* err);
 // Split-KV partials on the tensor cores (head dim 128 or 256, Hq/Hkv dividing 128); the
 // CUDA-core partial kernel covers every other supported shape.
 bool attn_tc_supported(const AttnArgs& a);

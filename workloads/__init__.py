@@ -387,3 +387,64 @@ def sweep_gdn_layer(N: int, B: int, layer: int = 0, seed: int = 0) -> GDNCase:
 def sweep_attn_layer(N: int, B: int, layer: int = 0, seed: int = 0) -> AttnCase:
     return attn_case(sweep_trees(N, B, seed), [8192] * B, Hq=16, Hkv=4, hd=128,
                      seed=seed * 1000 + 500 + layer, rope_theta=1e6)
+
+
+# ----------------------------------------------------------------------------- device-drawn stacks
+# The wide-tree sweep's largest stacks (24 GDN layers at B=128, N=256: ~10 GB of inputs, and 8
+# paged attention layers of ~2 GB each) take too long to draw with numpy, so the benchmark draws
+# them on the device with a seeded torch generator, in the same distributions as gdn_case and
+# attn_case.  Only the benchmark uses these; the parity tests use the numpy cases above.
+def _device_gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def device_gdn_stack(layers: int, B: int, N: int, H: int, d: int, seed: int, device) -> dict:
+    """Stacked inputs of ``layers`` independent GDN layers, bf16 I/O and state: q, k
+    [layers,B,N,H,d] unit-norm per (node, head); v [layers,B,N,H,d] ~ N(0,1); alpha =
+    exp(-softplus(x)), beta = sigmoid(x) [layers,B,N,H] fp32 with x ~ N(0,1); S0
+    [layers,B,H,d,d] ~ N(0, 0.02^2).  Draw order: q, k, v, x_alpha, x_beta, S0."""
+    g = _device_gen(seed, device)
+    f32 = dict(device=device, dtype=torch.float32, generator=g)
+
+    def unit(shape):
+        x = torch.randn(shape, **f32)
+        return (x / torch.linalg.vector_norm(x, dim=-1, keepdim=True)).to(torch.bfloat16)
+
+    shape = (layers, B, N, H, d)
+    q = unit(shape)
+    k = unit(shape)
+    v = torch.randn(shape, **f32).to(torch.bfloat16)
+    alpha = torch.exp(-torch.nn.functional.softplus(torch.randn((layers, B, N, H), **f32)))
+    beta = torch.sigmoid(torch.randn((layers, B, N, H), **f32))
+    S0 = (0.02 * torch.randn((layers, B, H, d, d), **f32)).to(torch.bfloat16)
+    return dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0)
+
+
+def device_attn_layer(B: int, N: int, prefix: int, Hq: int, Hkv: int, hd: int, seed: int, device) -> dict:
+    """One paged attention layer, bf16: q [B,N,Hq,hd], k_new, v_new [B,N,Hkv,hd] ~ N(0,1); the
+    caches [num_blocks,Hkv,16,hd] ~ N(0,1) (the prefix's keys taken as already rotated); a
+    block table [B, max_blocks] that hands each sequence ceil((prefix + N) / 16) blocks of a
+    random permutation; prefix_len [B] = prefix.  Draw order: q, k_new, v_new, permutation,
+    K cache, V cache."""
+    g = _device_gen(seed, device)
+    f32 = dict(device=device, dtype=torch.float32, generator=g)
+    q = torch.randn((B, N, Hq, hd), **f32).to(torch.bfloat16)
+    k_new = torch.randn((B, N, Hkv, hd), **f32).to(torch.bfloat16)
+    v_new = torch.randn((B, N, Hkv, hd), **f32).to(torch.bfloat16)
+    need = (prefix + N + BLOCK_SIZE - 1) // BLOCK_SIZE
+    num_blocks = B * need
+    perm = torch.randperm(num_blocks, device=device, generator=g).to(torch.int32)
+    table = perm.view(B, need).contiguous()
+    cache = (num_blocks, Hkv, BLOCK_SIZE, hd)
+    k_cache = torch.empty(cache, device=device, dtype=torch.bfloat16)
+    v_cache = torch.empty(cache, device=device, dtype=torch.bfloat16)
+    for c in (k_cache, v_cache):           # drawn in slices: fp32 staging of one slice at a time
+        step = max(1, (1 << 28) // (Hkv * BLOCK_SIZE * hd))
+        for s in range(0, num_blocks, step):
+            e = min(num_blocks, s + step)
+            c[s:e] = torch.randn((e - s,) + cache[1:], **f32).to(torch.bfloat16)
+    prefix_len = torch.full((B,), prefix, device=device, dtype=torch.int32)
+    return dict(q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache, block_table=table,
+                prefix_len=prefix_len)
