@@ -276,3 +276,28 @@ def test_commit_of_a_layer_stack_in_one_launch_equals_per_layer_commits(mode, ki
     assert (err.cpu() == 0).all()
     for l in range(len(cases)):
         assert torch.equal(S0[l].cpu(), want[l])
+
+
+@pytest.mark.parametrize("shape", ["shallow", "depth9", "depth15", "chain20", "chain64", "forest", "single"])
+def test_small_tree_solve_variants(shape):
+    """bf16, d=128 trees of at most 64 nodes (the row-per-thread TreeWY kernel): root paths held
+    in registers for depths below 4, 10 and 16, the shared-memory solve of deeper trees, a forest
+    and a single node, every output against the oracle."""
+    rng = np.random.default_rng(77)
+    if shape == "shallow":
+        trees = [W.full_tree(3, 3)[:33], W.full_tree(2, 3)]
+        trees = [t + [0] * (33 - len(t)) if len(t) < 33 else t for t in trees]
+    elif shape == "depth9":
+        trees = [W.chain(10) + [3, 4, 5], W.chain(10) + [0, 10, 11]]
+    elif shape == "depth15":
+        trees = [W.chain(16) + [2, 7], W.chain(16) + [0, 16]]
+    elif shape == "chain20":
+        trees = [W.chain(20), W.chain(20)]
+    elif shape == "chain64":
+        trees = [W.chain(64)]
+    elif shape == "forest":
+        trees = [[-1, -1, 0, 1, -1, 2, 3, 4, 4], [-1, 0, -1, 2, 1, -1, 5, 6, 0]]
+    else:
+        trees = [[-1], [-1]]
+    case = W.gdn_case(trees, H=3, dk=128, dv=128, io="bf16", state="bf16", seed=len(shape))
+    _check_all(case)

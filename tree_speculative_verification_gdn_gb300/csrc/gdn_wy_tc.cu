@@ -44,6 +44,14 @@ __device__ __forceinline__ void tmem_wait_ld16x2(uint32_t* a, uint32_t* c) {
                "+r"(c[15]));
 }
 
+// After tcgen05.wait::ld: every later use of r[0..N) depends on the wait (the empty asm
+// statements are volatile, so they stay after it, and each "writes" its register).
+template <int NR>
+__device__ __forceinline__ void tie_after_wait(uint32_t* r) {
+#pragma unroll
+  for (int k = 0; k < NR; ++k) asm volatile("" : "+r"(r[k]));
+}
+
 struct TcHead {
   uint64_t tma_bar;
   uint64_t mma_bar;
@@ -531,6 +539,489 @@ __global__ void __launch_bounds__(kThreads) gdn_wy_tc_kernel(GdnArgs a, float* _
   if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Trees of at most 64 nodes: one thread per state row, the root path's pseudo-values in
+// registers.
+//
+// 128 threads; thread r owns state row r, which is TMEM lane r of the S_0 contraction.  The key
+// and query tiles are staged stacked, [K; Q] per 64-column k-block, so that two groups of
+// tcgen05 MMAs run from the same shared memory at once:
+//   D1 = S_0 [K; Q]^T   (M = 128 rows, N = 2 Npad)  -> (S_0 k_i)_r and (S_0 q_i)_r in lane r;
+//   D2 = [K; Q] K^T     (M = 128, N = Npad)         -> k_m.k_j (lane m < Npad) and q_m.k_j
+//                                                      (lane Npad + m) for every node pair.
+// Warp 2 issues the copies and, as soon as they land, the MMAs, while warps 0-1 analyse the tree:
+// depths, log(gamma), and the depth-first pre-order of the nodes.  Lane m of D2 then forms the
+// coefficients of its node's root path, beta_i Gamma_ij (k_i.k_j) and q_scale Gamma_ij (q_i.k_j),
+// and every thread turns its row of D1 into a_i and b_i, stored by pre-order position.
+//
+// The solve visits the nodes in pre-order.  When a node at depth d is visited, the last node
+// visited at each depth t < d is its ancestor at depth t, so a thread keeps the pseudo-values
+// of the current root path in registers, w_i = a_i - sum_t c_{i,t} w_t and o_i = b_i +
+// sum_t e_{i,t} w_t + e_{i,i} w_i read no shared memory but a_i, b_i and the coefficients, and
+// no thread ever waits for another.  Trees deeper than the register path (15) keep every w in
+// shared memory instead and read the ancestors' from there.  The operation order per element is
+// the kernel's above, except that the dot products come from the tensor cores.
+constexpr int kSmallN = 64;
+constexpr int kSThreads = 128;
+
+struct TcHeadS {
+  uint64_t tma_bar;
+  uint64_t mma_bar;
+  uint32_t tmem_base;
+  int flag, total, fail, maxdepth, mma_issued;
+  int par[kSmallN];
+  int depth[kSmallN];
+  int size[kSmallN];     // nodes in the subtree
+  int sib[kSmallN];      // nodes in the subtrees of earlier siblings
+  int pos[kSmallN];      // pre-order position of each node
+  int2 meta[kSmallN];    // per position: {node | depth << 8, e_ii (register walk) or first entry (deep)}
+  float4 np[kSmallN];    // per node: {beta, gamma, position, -}
+  float lg[kSmallN];
+  float beta[kSmallN];
+  float gam[kSmallN];
+  int lz_nodes[kLazyMaxLen];
+  float lz_g[kLazyMaxLen];
+  float lz_lga;
+  int lz_L, lz_status, lz_pad[3];
+};
+static_assert(sizeof(TcHeadS) % 16 == 0, "the entry table after the head is 16-byte aligned");
+
+struct WySmallLayout {
+  uint32_t kq, v, head, ent, anc, lz_w, lz_k, total;
+};
+// Byte offsets from the 1024-byte aligned base: S_0 tile, stacked [K; Q] tiles, V tile (when it
+// fits), head, path-entry coefficients (cap float2 {c, e}), the entries' ancestor positions
+// (cap int, deep trees only), lazy-commit rows.  The second k-block's
+// D2 A operand reads 128 rows from its start, so the allocation extends at least 16 KB past it.
+__host__ __device__ inline WySmallLayout wy_small_layout(int Npad, int cap, bool lazy, bool v_in_smem) {
+  WySmallLayout L{};
+  L.kq = kTileA;
+  const uint32_t region = (uint32_t)(2 * Npad) * 128u;   // [K; Q] rows of one k-block
+  L.v = L.kq + 2 * region;
+  L.head = L.v + (v_in_smem ? 2u * (uint32_t)Npad * 128u : 0u);
+  L.ent = L.head + (uint32_t)sizeof(TcHeadS);
+  L.anc = L.ent + (uint32_t)cap * 8u;
+  uint32_t end = (L.anc + (uint32_t)cap * 4u + 15u) & ~15u;
+  L.lz_w = end;
+  L.lz_k = L.lz_w + (lazy ? (uint32_t)kLazyMaxLen * kD * 4u : 0u);
+  end = L.lz_k + (lazy ? (uint32_t)kLazyMaxLen * kD * 2u : 0u);
+  const uint32_t overrun = L.kq + region + 128u * 128u;
+  L.total = end > overrun ? end : overrun;
+  return L;
+}
+
+__device__ __forceinline__ void bar_sync_named(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// The solve with the root path in registers (every depth < D, D even); see above.  ab[p][r]
+// holds {a, b} of the node at position p, ce[p][t] its {c, e} of the ancestor at depth t, zero
+// for t >= depth (those terms vanish), and meta[p] = {node | depth << 8, e_ii}.  Every load of
+// an iteration depends on p alone, so the loads of the next nodes run ahead of the arithmetic.
+template <int D>
+__device__ __forceinline__ void wy_small_walk_regs(const float2* __restrict__ ab, const int2* __restrict__ meta,
+                                                   const float2* __restrict__ ce, int N, int H, int r,
+                                                   bf16* __restrict__ outb, float* __restrict__ pvb) {
+  float pw[D];
+#pragma unroll
+  for (int t = 0; t < D; ++t) pw[t] = 0.f;
+#pragma unroll 2
+  for (int p = 0; p < N; ++p) {
+    const int2 m = meta[p];
+    const float2 x = ab[p * kD + r];
+    float w = x.x, o = x.y;
+#pragma unroll
+    for (int t = 0; t < D; t += 2) {
+      const float4 q = *reinterpret_cast<const float4*>(ce + p * D + t);   // entries t and t + 1
+      w = fmaf(-q.x, pw[t], w);
+      o = fmaf(q.y, pw[t], o);
+      w = fmaf(-q.z, pw[t + 1], w);
+      o = fmaf(q.w, pw[t + 1], o);
+    }
+    o = fmaf(__int_as_float(m.y), w, o);
+    const int d = m.x >> 8;
+#pragma unroll
+    for (int t = 0; t < D; ++t)
+      if (t == d) pw[t] = w;
+    const size_t ni = (size_t)(m.x & 255) * H * kD;
+    outb[ni + r] = from_f32<bf16>(o);
+    pvb[ni + r] = w;
+  }
+}
+
+// One thread: D1 = S_0 [K; Q]^T and D2 = [K; Q] K^T, committed to hd.mma_bar.
+__device__ __forceinline__ void wy_small_issue_mma(uint32_t tmem, const unsigned char* sA, const unsigned char* sKQ,
+                                                   uint32_t region, int Npad, TcHeadS& hd) {
+  tc_fence_after();
+  const uint32_t id1 = idesc_bf16_f32(128, 2 * Npad), id2 = idesc_bf16_f32(128, Npad);
+  const uint32_t a0 = smem_addr(sA), kq0 = smem_addr(sKQ);
+  for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t ad = sw128_desc(a0 + kb * (kTileA / 2) + ks * 32);
+      const uint64_t kq = sw128_desc(kq0 + kb * region + ks * 32);
+      const uint32_t acc = (kb | ks) ? 1u : 0u;
+      mma_bf16(tmem, ad, kq, id1, acc);
+      mma_bf16(tmem + (uint32_t)(2 * Npad), kq, kq, id2, acc);
+    }
+  }
+  mma_commit(&hd.mma_bar);
+  hd.mma_issued = 1;
+}
+
+template <bool LAZY>
+__global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
+    GdnArgs a, float* __restrict__ pseudo_v, float* __restrict__ log_gamma, int cap, int Npad, uint32_t tmem_cols,
+    int v_in_smem, const __grid_constant__ CUtensorMap mS0, const __grid_constant__ CUtensorMap mK,
+    const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mV,
+    const __grid_constant__ WyLazy lz) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const WySmallLayout Ly = wy_small_layout(Npad, cap, LAZY, v_in_smem != 0);
+  unsigned char* sA = smem;
+  unsigned char* sKQ = smem + Ly.kq;
+  unsigned char* sV = smem + Ly.v;
+  TcHeadS& hd = *reinterpret_cast<TcHeadS*>(smem + Ly.head);
+  float2* ce = reinterpret_cast<float2*>(smem + Ly.ent);    // per path entry: {c, e}
+  int* anc = reinterpret_cast<int*>(smem + Ly.anc);         // per path entry: the ancestor's position
+  const uint32_t region = (uint32_t)(2 * Npad) * 128u;
+
+  const int N = a.N, H = a.H;
+  const int b = blockIdx.x / H, h = blockIdx.x % H;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+
+  const bool own = tid < N;   // warps 0-1 analyse the tree, one node per thread
+  const size_t nh_own = ((size_t)b * N + tid) * H + h;
+  const int par_own = own ? __ldg(a.parents + (size_t)b * N + tid) : -1;
+  const float alpha_own = own ? __ldg(a.alpha + nh_own) : 1.f;
+  const float beta_own = own ? __ldg(a.beta + nh_own) : 0.f;
+
+  if (tid == 0) {
+    mbar_init(&hd.tma_bar, 1);
+    mbar_init(&hd.mma_bar, 1);
+    hd.fail = 0;
+    hd.flag = 0;
+    hd.maxdepth = 0;
+    hd.mma_issued = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(&hd.tmem_base, tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = hd.tmem_base;
+
+  int* lz_nodes = hd.lz_nodes;
+  float* lz_g = hd.lz_g;
+  float* lz_w = reinterpret_cast<float*>(smem + Ly.lz_w);  // [L][128]
+  bf16* lz_k = reinterpret_cast<bf16*>(smem + Ly.lz_k);    // [L][128]
+
+  if (warp >= 2) {
+    if (tid == 64) {
+      mbar_arrive_expect_tx(&hd.tma_bar, kTileA + (uint32_t)(v_in_smem ? 6 : 4) * (uint32_t)Npad * 128u);
+      for (int kb = 0; kb < 2; ++kb) {
+        tma_load_2d(sA + kb * (kTileA / 2), &mS0, kb * 64, (b * H + h) * kD, &hd.tma_bar);
+        tma_load_4d(sKQ + kb * region, &mK, kb * 64, h, 0, b, &hd.tma_bar);
+        tma_load_4d(sKQ + kb * region + Npad * 128, &mQ, kb * 64, h, 0, b, &hd.tma_bar);
+        if (v_in_smem) tma_load_4d(sV + kb * Npad * 128, &mV, kb * 64, h, 0, b, &hd.tma_bar);
+      }
+      // Without a commit to fold in, the MMAs start as soon as the tiles have landed.
+      if (!LAZY) {
+        if (mbar_wait(&hd.tma_bar, 0)) wy_small_issue_mma(tmem, sA, sKQ, region, Npad, hd);
+        else hd.fail = 1;
+      }
+    }
+    if (LAZY) {
+      // The previous round's accepted path (TreeWY abstract: rebuild only the accepted state):
+      // warps 2-3 stage the path's w and key rows from the unchecked entries, clamped into
+      // range, while warp 2 checks the links, one entry per lane.
+      const int Lraw = lz.len[b];
+      const int Lc = Lraw < 0 ? 0 : min(Lraw, min(kLazyMaxLen, min(lz.Lmax, lz.Np)));
+      for (int x = tid - 64; x < Lc * kD; x += 64) {
+        const int e = lz.path[(size_t)b * lz.Lmax + x / kD];
+        const int node = e < 0 ? 0 : (e >= lz.Np ? lz.Np - 1 : e);
+        const size_t nh = ((size_t)b * lz.Np + node) * H + h;
+        lz_w[x] = lz.pseudo_v[nh * kD + x % kD];
+        lz_k[x] = static_cast<const bf16*>(lz.k)[nh * kD + x % kD];
+      }
+      if (warp == 2) {
+        const bool len_ok = Lraw >= 1 && Lraw <= lz.Lmax && Lraw <= lz.Np && Lraw <= kLazyMaxLen;
+        int node = -1, pn = -1;
+        float lgt = 0.f;
+        if (len_ok && lane < Lraw) {
+          node = lz.path[(size_t)b * lz.Lmax + lane];
+          if (node >= 0 && node < lz.Np) {
+            pn = lz.parents[(size_t)b * lz.Np + node];
+            lgt = lz.log_gamma[((size_t)b * lz.Np + node) * H + h];
+          }
+        }
+        int prev = __shfl_up_sync(0xffffffffu, node, 1);
+        if (lane == 0) prev = -1;
+        const bool mine = lane >= Lraw || (node >= 0 && node < lz.Np && pn == prev);
+        const bool ok = len_ok && __all_sync(0xffffffffu, mine);
+        const float lga = __shfl_sync(0xffffffffu, lgt, ok ? Lraw - 1 : 0);
+        if (ok && lane < Lraw) {
+          lz_nodes[lane] = node;
+          lz_g[lane] = expf(lga - lgt);   // gamma_a / gamma_t
+        }
+        if (lane == 0) {
+          hd.lz_L = ok ? Lraw : 0;
+          hd.lz_status = ok ? 0 : TV_ERR_BAD_PATH;
+          hd.lz_lga = lga;
+        }
+      }
+    }
+  } else {
+    // Tree analysis, warps 0-1 (named barrier 1): a parent must be -1 or an earlier node.
+    if (own) {
+      hd.par[tid] = par_own;
+      if (par_own < -1 || par_own >= tid) hd.flag = 1;
+      hd.lg[tid] = logf(alpha_own);
+      hd.beta[tid] = beta_own;
+      hd.size[tid] = 0;
+    }
+    bar_sync_named(1, 64);
+    if (!hd.flag) {
+      if (own) {  // depth and log(gamma) along the root path; every node counts in its ancestors' subtrees
+        int d = 0;
+        float lg = hd.lg[tid];
+        atomicAdd(&hd.size[tid], 1);
+        for (int j = par_own; j >= 0; j = hd.par[j]) {
+          lg += hd.lg[j];
+          ++d;
+          atomicAdd(&hd.size[j], 1);
+        }
+        hd.depth[tid] = d;
+        atomicMax(&hd.maxdepth, d);
+        hd.gam[tid] = lg;  // log(gamma) for now, moved to lg below
+      }
+      bar_sync_named(1, 64);
+      if (own) {
+        int sib = 0;  // the subtrees of earlier siblings come first in pre-order
+#pragma unroll 8
+        for (int s = 0; s < tid; ++s) sib += (hd.par[s] == par_own) ? hd.size[s] : 0;
+        hd.sib[tid] = sib;
+        hd.lg[tid] = hd.gam[tid];
+        hd.gam[tid] = expf(hd.gam[tid]);
+      }
+      bar_sync_named(1, 64);
+      if (own) {  // pre-order position: depth + the earlier-sibling counts along the root path
+        int p = hd.depth[tid];
+        for (int j = tid; j >= 0; j = hd.par[j]) p += hd.sib[j];
+        hd.pos[tid] = p;
+        hd.meta[p].x = tid | (hd.depth[tid] << 8);
+      }
+      bar_sync_named(1, 64);
+      const int maxd = hd.maxdepth;
+      if (maxd < 16) {
+        // Register walk: position p's entries at ce[p * D + t], D = the walk's path length;
+        // zero-filled, so the entries past a node's depth contribute nothing.
+        const int D = maxd < 4 ? 4 : (maxd < 10 ? 10 : 16);
+        for (int x = tid; x < N * D; x += 64) ce[x] = make_float2(0.f, 0.f);
+      } else {
+        if (warp == 0) {  // path entries per position: exclusive scan of (depth + 1) in pre-order
+          int carry = 0;
+          for (int base = 0; base < N; base += 32) {
+            const int p = base + lane;
+            const int x0 = (p < N) ? (hd.meta[p].x >> 8) + 1 : 0;
+            int x = x0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const int y = __shfl_up_sync(0xffffffffu, x, o);
+              if (lane >= o) x += y;
+            }
+            if (p < N) hd.meta[p].y = carry + x - x0;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+          }
+          if (lane == 0) hd.total = carry;
+        }
+        bar_sync_named(1, 64);
+        if (own) {  // entries root first, with the ancestor's position
+          const int d = hd.depth[tid], e0 = hd.meta[hd.pos[tid]].y;
+          int j = tid;
+          for (int t = d; t >= 0; --t) {
+            anc[e0 + t] = hd.pos[j];
+            j = hd.par[j];
+          }
+        }
+      }
+      if (own) hd.np[tid] = make_float4(hd.beta[tid], hd.gam[tid], __int_as_float(hd.pos[tid]), 0.f);
+    }
+  }
+  __syncthreads();
+  int status = hd.flag ? TV_ERR_BAD_TREE : 0;
+  if (LAZY && !status) status = hd.lz_status;
+
+  if (LAZY) {
+    if (!mbar_wait(&hd.tma_bar, 0)) hd.fail = 1;
+    __syncthreads();
+    if (!status && !hd.fail) {
+      // S_0 <- gamma_a S_0 + sum_t (gamma_a / gamma_t) w_t k_t^T on the swizzled tile, in the
+      // commit kernel's operation order; the committed state also goes back to HBM.  Thread r
+      // takes row r, one k-block (64 columns) at a time.
+      const int row = tid, L = hd.lz_L;
+      const float gam = expf(hd.lz_lga);
+      for (int kb = 0; kb < 2; ++kb) {
+        unsigned char* rowp = sA + kb * (kTileA / 2) + row * 128;
+        uint4* g = reinterpret_cast<uint4*>(static_cast<bf16*>(const_cast<void*>(a.S0)) +
+                                            (((size_t)b * H + h) * kD + row) * kD + kb * 64);
+        float x[8][8];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          unpack8(*reinterpret_cast<const uint4*>(rowp + ((ch ^ (row & 7)) << 4)), x[ch]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[ch][e] *= gam;
+        }
+        for (int t = 0; t < L; ++t) {
+          const float c = lz_g[t] * lz_w[t * kD + row];
+          const uint4* kr = reinterpret_cast<const uint4*>(lz_k + t * kD + kb * 64);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            float kf[8];
+            unpack8(kr[ch], kf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[ch][e] = fmaf(c, kf[e], x[ch][e]);
+          }
+        }
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 pk = pack8(x[ch]);
+          *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4)) = pk;
+          g[ch] = pk;
+        }
+      }
+      fence_proxy_async();  // the MMA reads the tile through the async proxy
+      __syncthreads();
+      if (tid == 64) wy_small_issue_mma(tmem, sA, sKQ, region, Npad, hd);
+    }
+  }
+  const bool run = !status && !hd.fail;
+  if (run && !mbar_wait(&hd.mma_bar, 0)) hd.fail = 1;
+  tc_fence_after();
+  __syncthreads();
+
+  if (run && !hd.fail) {
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const int r = tid;
+    // Path-entry coefficients.  Lane m of D2 holds row m of [K; Q] K^T; its Npad dot products go
+    // to a padded shared-memory row (the S_0 and [K; Q] tiles are free now), then the thread
+    // forms the entries of its node: c = beta_i Gamma_ij (k_i.k_j) for strict ancestors (K
+    // lanes), e = q_scale Gamma_ij (q_i.k_j) for the path including i (Q lanes).
+    const int rs = Npad + 4;                     // row stride in floats (16-byte rows, no conflicts)
+    float* d2 = reinterpret_cast<float*>(sA);    // [2 Npad][rs]
+    {
+      uint32_t v64[64];                          // every thread of the warp takes part in each load
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (c < Npad / 16) tmem_ld16_nowait(tmem + lane_base + (uint32_t)(2 * Npad + 16 * c), v64 + 16 * c);
+      tmem_wait_ld();
+      tie_after_wait<64>(v64);
+      if (r < 2 * Npad) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (c < Npad / 16) {
+#pragma unroll
+            for (int u = 0; u < 16; u += 4)
+              *reinterpret_cast<float4*>(d2 + r * rs + 16 * c + u) =
+                  make_float4(__uint_as_float(v64[16 * c + u]), __uint_as_float(v64[16 * c + u + 1]),
+                              __uint_as_float(v64[16 * c + u + 2]), __uint_as_float(v64[16 * c + u + 3]));
+          }
+      }
+    }
+    const int maxd = hd.maxdepth;
+    const int D = maxd < 4 ? 4 : (maxd < 10 ? 10 : 16);
+    {
+      const bool is_k = r < Npad;
+      const int i = is_k ? r : r - Npad;
+      if (r < 2 * Npad && i < N) {
+        const int d = hd.depth[i], p = hd.pos[i];
+        const float lgi = hd.lg[i];
+        const float pre = is_k ? hd.beta[i] : a.q_scale;
+        // register walk: strided entries, e_ii in meta; deep trees: the packed list, e_ii at t = d
+        float* dst = reinterpret_cast<float*>(ce + (maxd < 16 ? p * D : hd.meta[p].y)) + (is_k ? 0 : 1);
+        int j = is_k ? hd.par[i] : i;
+        for (int t = is_k ? d - 1 : d; t >= 0; --t) {   // root path, i (or its parent) first
+          const float v = pre * expf(lgi - hd.lg[j]) * d2[r * rs + j];
+          if (maxd < 16 && t == d) hd.meta[p].y = __float_as_int(v);
+          else dst[2 * t] = v;
+          j = hd.par[j];
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // the entries are complete; the tiles' space is free for a and b
+    tc_fence_after();
+
+    // a_i[r] = beta_i (v_i[r] - gamma_i (S_0 k_i)_r) and b_i[r] = q_scale gamma_i (S_0 q_i)_r ->
+    // ab[pos(i)][r]; 16 nodes per load pair.  The tiles are free: ab spans the S_0 tile and as
+    // much of the [K; Q] tiles as it needs.
+    float2* ab = reinterpret_cast<float2*>(sA);
+    const bf16* __restrict__ v = static_cast<const bf16*>(a.v);
+    const float q_scale = a.q_scale;
+    for (int c = 0; c < Npad / 16; ++c) {
+      uint32_t dk[16], dq[16];
+      tmem_ld16_nowait(tmem + lane_base + (uint32_t)(16 * c), dk);
+      tmem_ld16_nowait(tmem + lane_base + (uint32_t)(Npad + 16 * c), dq);
+      tmem_wait_ld16x2(dk, dq);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int i = 16 * c + u;
+        if (i < N) {
+          float vv;
+          if (v_in_smem) {
+            const int cc = r % 64;
+            vv = to_f32(*(reinterpret_cast<const bf16*>(sV + (r / 64) * Npad * 128 + i * 128 +
+                                                         (((cc / 8) ^ (i & 7)) << 4)) + (cc % 8)));
+          } else {
+            vv = to_f32(v[(((size_t)b * N + i) * H + h) * kD + r]);
+          }
+          const float4 q = hd.np[i];   // {beta, gamma, position}
+          ab[__float_as_int(q.z) * kD + r] =
+              make_float2(q.x * (vv - q.y * __uint_as_float(dk[u])), q_scale * q.y * __uint_as_float(dq[u]));
+        }
+      }
+    }
+    bf16* __restrict__ outb = static_cast<bf16*>(a.out) + ((size_t)b * N * H + h) * kD;
+    float* __restrict__ pvb = pseudo_v + ((size_t)b * N * H + h) * kD;
+    if (maxd < 4) {
+      wy_small_walk_regs<4>(ab, hd.meta, ce, N, H, r, outb, pvb);
+    } else if (maxd < 10) {
+      wy_small_walk_regs<10>(ab, hd.meta, ce, N, H, r, outb, pvb);
+    } else if (maxd < 16) {
+      wy_small_walk_regs<16>(ab, hd.meta, ce, N, H, r, outb, pvb);
+    } else {
+      // Deep trees: every w stays in ab (in place of a) and the ancestors' are read from there.
+      for (int p = 0; p < N; ++p) {
+        const int2 m = hd.meta[p];
+        const int nid = m.x & 255, d = m.x >> 8, e0 = m.y;
+        float2 x = ab[p * kD + r];
+        float w = x.x, o = x.y;
+        for (int t = 0; t < d; ++t) {
+          const float2 q = ce[e0 + t];
+          const float wj = ab[anc[e0 + t] * kD + r].x;
+          w = fmaf(-q.x, wj, w);
+          o = fmaf(q.y, wj, o);
+        }
+        o = fmaf(ce[e0 + d].y, w, o);
+        ab[p * kD + r].x = w;
+        const size_t ni = (size_t)nid * H * kD;
+        outb[ni + r] = from_f32<bf16>(o);
+        pvb[ni + r] = w;
+      }
+    }
+    for (int i = tid; i < N; i += kSThreads) log_gamma[((size_t)b * N + i) * H + h] = hd.lg[i];
+  }
+  if (h == 0 && tid == 0) a.err[b] = status ? status : (hd.fail ? TV_ERR_TIMEOUT : 0);
+  if (tid == 0) {  // nothing in flight may outlive the CTA's shared memory and TMEM (bounded waits)
+    if (hd.fail || status) mbar_wait(&hd.tma_bar, 0);
+    if (hd.mma_issued && (hd.fail || status)) mbar_wait(&hd.mma_bar, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, tmem_cols);
+}
+
 }  // namespace
 
 bool gdn_wy_tc_supported(const GdnArgs& a) {
@@ -541,12 +1032,63 @@ bool gdn_wy_lazy_fits(int N) {
   const int Npad = (N + 15) / 16 * 16;
   int cap = N * (N + 1) / 2;
   if (cap > kPathCap) cap = kPathCap;
+  if (N <= kSmallN)
+    return 1024 + wy_small_layout(Npad, N * (N + 1) / 2 > 16 * N ? N * (N + 1) / 2 : 16 * N, true, false).total <=
+           227 * 1024;
   return 1024 + kTileA + (size_t)4 * Npad * 128 + sizeof(TcHead) + (size_t)cap * 12 + 16 +
              (size_t)kLazyMaxLen * kD * 6 <= 227 * 1024;
 }
 
+namespace {
+
+// The row-per-thread kernel for trees of at most 64 nodes.
+cudaError_t launch_gdn_wy_tc_small(const GdnArgs& a, float* pseudo_v, float* log_gamma, const WyLazy& lz,
+                                   cudaStream_t s) {
+  const int Npad = (a.N + 15) / 16 * 16;
+  const uint32_t cols = 3 * Npad <= 128 ? 128u : 256u;   // D1 (2 Npad columns) and D2 (Npad)
+  // path entries: the packed lists of a deep tree (sum of depth + 1 <= N (N + 1) / 2) or the
+  // position-strided table of the register walk (N x 16)
+  const int cap = a.N * (a.N + 1) / 2 > 16 * a.N ? a.N * (a.N + 1) / 2 : 16 * a.N;
+  const bool lazy = lz.path != nullptr;
+  size_t smem = 1024 + wy_small_layout(Npad, cap, lazy, true).total;
+  const int v_in_smem = smem <= 227 * 1024;
+  if (!v_in_smem) smem = 1024 + wy_small_layout(Npad, cap, lazy, false).total;
+  auto kern = lazy ? gdn_wy_tc_small_kernel<true> : gdn_wy_tc_small_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  // TMEM: the CTAs resident on one SM must fit in its 512 columns; pad shared memory if needed.
+  for (;;) {
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSThreads, smem);
+    if (e != cudaSuccess) return e;
+    if ((uint32_t)occ * cols <= 512u || smem >= 227 * 1024) break;
+    smem += 8 * 1024;
+    if (smem > 227 * 1024) smem = 227 * 1024;
+  }
+  CUtensorMap mS0, mK, mQ, mV;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.B * a.H * kD};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!make_map_bf16_sw128(&mS0, a.S0, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)a.H, (cuuint64_t)a.N, (cuuint64_t)a.B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)a.H * kD * 2, (cuuint64_t)a.N * a.H * kD * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)Npad, 1};
+    if (!make_map_bf16_sw128(&mK, a.k, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16_sw128(&mQ, a.q, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16_sw128(&mV, a.v, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  kern<<<a.B * a.H, kSThreads, smem, s>>>(a, pseudo_v, log_gamma, cap, Npad, cols, v_in_smem, mS0, mK, mQ, mV, lz);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_gdn_wy_tc(const GdnArgs& a, float* pseudo_v, float* log_gamma, const WyLazy& lz,
                              cudaStream_t s) {
+  if (a.N <= kSmallN) return launch_gdn_wy_tc_small(a, pseudo_v, log_gamma, lz, s);
   const int Npad = (a.N + 15) / 16 * 16;
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * Npad)) cols <<= 1;
