@@ -35,10 +35,14 @@ AttnPlan plan_attn(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int bs
   AttnPlan p;
   const long long slots = (long long)max_blocks * bs;
   const long long work = (long long)B * Hkv * slots;
-  // ~768 (sequence, KV head, chunk) items, about five per SM of a 152-SM GPU: longer chunks
-  // mean fewer CTA set-ups and partial rows to combine, shorter ones a smaller tail.  A fixed
-  // count keeps the workspace size a function of the sizes alone.
-  long long chunk = (work + 767) / 768;
+  // About 1536 partial CTAs -- (sequence, KV head, chunk) items times the tiles of 128 query
+  // rows each item has, ten per SM of a 152-SM GPU: longer chunks mean fewer CTA set-ups and
+  // partial rows to combine, shorter ones a smaller tail.  With two row tiles (the 40-node trees
+  // of a 4-head group) that is ~768 items, the best of a sweep over 512 .. 2048; wider trees
+  // take longer chunks rather than more CTAs.  The count depends on the sizes alone, and so does
+  // the workspace size.
+  const long long mtiles = ((long long)(Hq / Hkv) * N + 127) / 128;
+  long long chunk = (work * mtiles + 1535) / 1536;
   chunk = (chunk + 127) / 128 * 128;
   if (chunk < 128) chunk = 128;
   if (chunk > 8192) chunk = 8192;
