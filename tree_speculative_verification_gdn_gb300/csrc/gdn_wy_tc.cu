@@ -691,6 +691,14 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
   const int b = blockIdx.x / H, h = blockIdx.x % H;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
+  // Lazy commit: warps 2-3 start the previous path's loads at once (its length and every entry
+  // up to the row length); the staging below waits for them.
+  int lz_len = 0, lz_ent[kLazyMaxLen];
+  if (LAZY && warp >= 2) {
+    lz_len = lz.len[b];
+#pragma unroll
+    for (int t = 0; t < kLazyMaxLen; ++t) lz_ent[t] = t < lz.Lmax ? lz.path[(size_t)b * lz.Lmax + t] : 0;
+  }
   const bool own = tid < N;   // warps 0-1 analyse the tree, one node per thread
   const size_t nh_own = ((size_t)b * N + tid) * H + h;
   const int par_own = own ? __ldg(a.parents + (size_t)b * N + tid) : -1;
@@ -736,21 +744,37 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
       // The previous round's accepted path (TreeWY abstract: rebuild only the accepted state):
       // warps 2-3 stage the path's w and key rows from the unchecked entries, clamped into
       // range, while warp 2 checks the links, one entry per lane.
-      const int Lraw = lz.len[b];
+      const int Lraw = lz_len;
       const int Lc = Lraw < 0 ? 0 : min(Lraw, min(kLazyMaxLen, min(lz.Lmax, lz.Np)));
-      for (int x = tid - 64; x < Lc * kD; x += 64) {
-        const int e = lz.path[(size_t)b * lz.Lmax + x / kD];
-        const int node = e < 0 ? 0 : (e >= lz.Np ? lz.Np - 1 : e);
-        const size_t nh = ((size_t)b * lz.Np + node) * H + h;
-        lz_w[x] = lz.pseudo_v[nh * kD + x % kD];
-        lz_k[x] = static_cast<const bf16*>(lz.k)[nh * kD + x % kD];
+      // Every path entry first, then every row element (columns u and u + 64 of each entry), so
+      // the loads of each kind are in flight together.
+      const int u = tid - 64;
+      int node[kLazyMaxLen];
+#pragma unroll
+      for (int t = 0; t < kLazyMaxLen; ++t) {
+        const int e = t < Lc ? lz_ent[t] : 0;
+        node[t] = e < 0 ? 0 : (e >= lz.Np ? lz.Np - 1 : e);
       }
-      if (warp == 2) {
+#pragma unroll
+      for (int t = 0; t < kLazyMaxLen; ++t) {
+        if (t < Lc) {
+          const size_t nh = ((size_t)b * lz.Np + node[t]) * H + h;
+          const float* w = lz.pseudo_v + nh * kD;
+          const bf16* k = static_cast<const bf16*>(lz.k) + nh * kD;
+          lz_w[t * kD + u] = w[u];
+          lz_w[t * kD + u + 64] = w[u + 64];
+          lz_k[t * kD + u] = k[u];
+          lz_k[t * kD + u + 64] = k[u + 64];
+        }
+      }
+      if (warp == 2) {  // the path's links, one entry per lane
         const bool len_ok = Lraw >= 1 && Lraw <= lz.Lmax && Lraw <= lz.Np && Lraw <= kLazyMaxLen;
         int node = -1, pn = -1;
         float lgt = 0.f;
         if (len_ok && lane < Lraw) {
-          node = lz.path[(size_t)b * lz.Lmax + lane];
+#pragma unroll
+          for (int t = 0; t < kLazyMaxLen; ++t)
+            if (t == lane) node = lz_ent[t];
           if (node >= 0 && node < lz.Np) {
             pn = lz.parents[(size_t)b * lz.Np + node];
             lgt = lz.log_gamma[((size_t)b * lz.Np + node) * H + h];
@@ -770,6 +794,49 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
           hd.lz_status = ok ? 0 : TV_ERR_BAD_PATH;
           hd.lz_lga = lga;
         }
+      }
+      bar_sync_named(2, 64);
+      if (!hd.lz_status) {
+        // While warps 0-1 analyse the tree: S_0 <- gamma_a S_0 + sum_t (gamma_a / gamma_t) w_t
+        // k_t^T on the swizzled tile, in the commit kernel's operation order, thread u taking
+        // rows u and u + 64, one k-block (64 columns) at a time.  The MMAs then read the
+        // committed state; it goes back to HBM after the join, if the sequence runs.
+        const bool landed = mbar_wait(&hd.tma_bar, 0);
+        if (landed) {
+          const int L = hd.lz_L;
+          const float gam = expf(hd.lz_lga);
+          for (int row = tid - 64; row < kD; row += 64) {
+            for (int kb = 0; kb < 2; ++kb) {
+              unsigned char* rowp = sA + kb * (kTileA / 2) + row * 128;
+              float x[8][8];
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch) {
+                unpack8(*reinterpret_cast<const uint4*>(rowp + ((ch ^ (row & 7)) << 4)), x[ch]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[ch][e] *= gam;
+              }
+              for (int t = 0; t < L; ++t) {
+                const float c = lz_g[t] * lz_w[t * kD + row];
+                const uint4* kr = reinterpret_cast<const uint4*>(lz_k + t * kD + kb * 64);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                  float kf[8];
+                  unpack8(kr[ch], kf);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) x[ch][e] = fmaf(c, kf[e], x[ch][e]);
+                }
+              }
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4)) = pack8(x[ch]);
+            }
+          }
+          fence_proxy_async();  // the MMA reads the tile through the async proxy
+        } else if (tid == 64) {
+          hd.fail = 1;
+        }
+        bar_sync_named(2, 64);
+        if (tid == 64 && landed) wy_small_issue_mma(tmem, sA, sKQ, region, Npad, hd);
       }
     }
   } else {
@@ -853,47 +920,13 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
   int status = hd.flag ? TV_ERR_BAD_TREE : 0;
   if (LAZY && !status) status = hd.lz_status;
 
-  if (LAZY) {
-    if (!mbar_wait(&hd.tma_bar, 0)) hd.fail = 1;
-    __syncthreads();
-    if (!status && !hd.fail) {
-      // S_0 <- gamma_a S_0 + sum_t (gamma_a / gamma_t) w_t k_t^T on the swizzled tile, in the
-      // commit kernel's operation order; the committed state also goes back to HBM.  Thread r
-      // takes row r, one k-block (64 columns) at a time.
-      const int row = tid, L = hd.lz_L;
-      const float gam = expf(hd.lz_lga);
-      for (int kb = 0; kb < 2; ++kb) {
-        unsigned char* rowp = sA + kb * (kTileA / 2) + row * 128;
-        uint4* g = reinterpret_cast<uint4*>(static_cast<bf16*>(const_cast<void*>(a.S0)) +
-                                            (((size_t)b * H + h) * kD + row) * kD + kb * 64);
-        float x[8][8];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          unpack8(*reinterpret_cast<const uint4*>(rowp + ((ch ^ (row & 7)) << 4)), x[ch]);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[ch][e] *= gam;
-        }
-        for (int t = 0; t < L; ++t) {
-          const float c = lz_g[t] * lz_w[t * kD + row];
-          const uint4* kr = reinterpret_cast<const uint4*>(lz_k + t * kD + kb * 64);
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            float kf[8];
-            unpack8(kr[ch], kf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[ch][e] = fmaf(c, kf[e], x[ch][e]);
-          }
-        }
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 pk = pack8(x[ch]);
-          *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4)) = pk;
-          g[ch] = pk;
-        }
-      }
-      fence_proxy_async();  // the MMA reads the tile through the async proxy
-      __syncthreads();
-      if (tid == 64) wy_small_issue_mma(tmem, sA, sKQ, region, Npad, hd);
+  if (LAZY && !status && !hd.fail) {
+    // The committed state back to HBM (rows of the updated tile, 16 bytes per copy).
+    bf16* g = static_cast<bf16*>(const_cast<void*>(a.S0)) + ((size_t)b * H + h) * kD * kD;
+    for (int x = tid; x < 2 * kD * 8; x += kSThreads) {
+      const int row = x >> 4, kb = (x >> 3) & 1, ch = x & 7;
+      reinterpret_cast<uint4*>(g + (size_t)row * kD + kb * 64)[ch] =
+          *reinterpret_cast<const uint4*>(sA + kb * (kTileA / 2) + row * 128 + ((ch ^ (row & 7)) << 4));
     }
   }
   const bool run = !status && !hd.fail;
