@@ -159,7 +159,7 @@ constexpr int kStride = 8 * kLPR;  // lane l holds columns l * 8 + j * kStride .
 // owns rows rl, rl + 32, ... of the head.  All of them are loaded before the path check; the
 // path's log(gamma), w rows and keys are then fetched in one phase into shared memory.
 template <typename TIO, typename TS, int DK>
-__global__ void __launch_bounds__(kThreads, 3) commit_wy_kernel(CommitArgs a0) {
+__global__ void __launch_bounds__(kThreads, 4) commit_wy_kernel(CommitArgs a0) {
   constexpr int CPL = DK / kLPR;
   __shared__ PathCheck pc;
   __shared__ float coef[TV_MAX_NODES];
