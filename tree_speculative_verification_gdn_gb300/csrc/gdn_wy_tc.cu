@@ -575,6 +575,7 @@ struct TcHeadS {
   int sib[kSmallN];      // nodes in the subtrees of earlier siblings
   int pos[kSmallN];      // pre-order position of each node
   int2 meta[kSmallN];    // per position: {node | depth << 8, e_ii (register walk) or first entry (deep)}
+  unsigned long long key[kSmallN];  // root-to-node path, 7 bits per level, root in the top bits
   float4 np[kSmallN];    // per node: {beta, gamma, position, -}
   float lg[kSmallN];
   float beta[kSmallN];
@@ -850,34 +851,56 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
     }
     bar_sync_named(1, 64);
     if (!hd.flag) {
-      if (own) {  // depth and log(gamma) along the root path; every node counts in its ancestors' subtrees
+      if (own) {  // depth, log(gamma) and the path key along the root path
         int d = 0;
         float lg = hd.lg[tid];
-        atomicAdd(&hd.size[tid], 1);
+        unsigned long long key = (unsigned long long)(tid + 1) << 56;
         for (int j = par_own; j >= 0; j = hd.par[j]) {
           lg += hd.lg[j];
           ++d;
-          atomicAdd(&hd.size[j], 1);
+          key = (key >> 7) | ((unsigned long long)(j + 1) << 56);
         }
         hd.depth[tid] = d;
         atomicMax(&hd.maxdepth, d);
         hd.gam[tid] = lg;  // log(gamma) for now, moved to lg below
+        hd.key[tid] = key;
       }
       bar_sync_named(1, 64);
-      if (own) {
-        int sib = 0;  // the subtrees of earlier siblings come first in pre-order
+      if (hd.maxdepth <= 8) {
+        // Pre-order with children in index order is the lexicographic order of the root-to-node
+        // index paths; up to depth 8 a path is one 64-bit key, so a node's position is the
+        // number of smaller keys.
+        if (own) {
+          const unsigned long long k = hd.key[tid];
+          int p = 0;
 #pragma unroll 8
-        for (int s = 0; s < tid; ++s) sib += (hd.par[s] == par_own) ? hd.size[s] : 0;
-        hd.sib[tid] = sib;
-        hd.lg[tid] = hd.gam[tid];
-        hd.gam[tid] = expf(hd.gam[tid]);
-      }
-      bar_sync_named(1, 64);
-      if (own) {  // pre-order position: depth + the earlier-sibling counts along the root path
-        int p = hd.depth[tid];
-        for (int j = tid; j >= 0; j = hd.par[j]) p += hd.sib[j];
-        hd.pos[tid] = p;
-        hd.meta[p].x = tid | (hd.depth[tid] << 8);
+          for (int j = 0; j < N; ++j) p += hd.key[j] < k ? 1 : 0;
+          hd.pos[tid] = p;
+          hd.meta[p].x = tid | (hd.depth[tid] << 8);
+          hd.lg[tid] = hd.gam[tid];
+          hd.gam[tid] = expf(hd.gam[tid]);
+        }
+      } else {
+        if (own) {  // deeper trees: every node counts in its own and its ancestors' subtrees
+          atomicAdd(&hd.size[tid], 1);
+          for (int j = par_own; j >= 0; j = hd.par[j]) atomicAdd(&hd.size[j], 1);
+        }
+        bar_sync_named(1, 64);
+        if (own) {
+          int sib = 0;  // the subtrees of earlier siblings come first in pre-order
+#pragma unroll 8
+          for (int s = 0; s < tid; ++s) sib += (hd.par[s] == par_own) ? hd.size[s] : 0;
+          hd.sib[tid] = sib;
+          hd.lg[tid] = hd.gam[tid];
+          hd.gam[tid] = expf(hd.gam[tid]);
+        }
+        bar_sync_named(1, 64);
+        if (own) {  // pre-order position: depth + the earlier-sibling counts along the root path
+          int p = hd.depth[tid];
+          for (int j = tid; j >= 0; j = hd.par[j]) p += hd.sib[j];
+          hd.pos[tid] = p;
+          hd.meta[p].x = tid | (hd.depth[tid] << 8);
+        }
       }
       bar_sync_named(1, 64);
       const int maxd = hd.maxdepth;
