@@ -6,16 +6,17 @@
 // and every S_i is written out (the checkpoint the commit step restores).
 //
 // The rows of S (value index r) evolve independently: row r only needs k_i, q_i, v_i[r],
-// alpha_i, beta_i.  A CTA owns a slab of 16 rows of one (sequence, head) at a time (the grid
-// is persistent: a few CTAs per sequence loop over its (head, slab) items), keeps their fp32
-// state on chip and walks the whole tree once, depth-first, instead of one launch per depth
-// reading every parent snapshot back from HBM.  HBM traffic is the floor: S_0 read once per
-// root, each checkpoint written once.  Each row is held by 8 lanes (dk/8 columns each, in
-// interleaved 8-column chunks), so a row dot product costs 3 shuffles; k.q, the same for every
-// row, comes from a per-item table.  Column pairs use the paired fp32 FMA.  Every warp walks
-// the tree on its own -- no barrier inside the node loop -- with the next two nodes' k, q and
-// v prefetched into registers; the CTA's warps share one (sequence, head), so k and q come
-// from L1 after the first warp's read.
+// alpha_i, beta_i.  A CTA owns a slab of 16 rows of one (sequence, head) at a time -- a work
+// unit; the grid is persistent and each CTA loops over its units (see the unit plan below) --
+// keeps their fp32 state on chip and walks the whole tree once, depth-first, instead of one
+// launch per depth reading every parent snapshot back from HBM.  HBM traffic is the floor: S_0
+// read once per root, each checkpoint written once.  Each row is held by 8 lanes (dk/8 columns
+// each, in interleaved 8-column chunks), so a row dot product costs 3 shuffles; k.q, the same
+// for every row, comes from a per-unit table.  Column pairs use the paired fp32 FMA.  Every
+// warp walks the tree on its own -- no barrier inside the node loop -- with the next node's k,
+// q and v prefetched into registers; the CTA's warps share one (sequence, head), so k and q
+// come from L1 after the first warp's read.  For bf16 inputs on small trees a lane group holds
+// two rows (see RPL below).
 //
 // Depth-first order visits a node's leaf children first, then its light children, and its
 // heaviest child (largest subtree) last.  A leaf's state only goes to its snapshot, so a leaf
@@ -36,8 +37,9 @@ namespace {
 
 constexpr int kLPR = 8;                 // lanes per state row
 constexpr int kRows = 16;               // state rows per CTA
-constexpr int kThreads = kLPR * kRows;  // 128
+constexpr int kLanes = kLPR * kRows;    // 128 lane slots: 8 per state row
 constexpr int kSlots = 6;               // on-chip state slots 1..6 (S_0 is re-read for a root)
+constexpr int kGroup = 16;              // CTAs that walk adjacent slabs side by side
 // Column ownership: lane l of a row holds the chunks of 8 columns starting at l * 8 + j * kStride
 // (j = 0 .. CPL / 8 - 1), so one chunk-wide access by the 8 lanes of a row covers kStride
 // contiguous columns: full 32-byte sectors for every load and store of k, q, S_0 and states.
@@ -46,9 +48,6 @@ constexpr int kStride = 8 * kLPR;
 // What the node loop needs from the schedule, plus the current item's decay / write strength.
 struct Sched {
   int order[TV_MAX_NODES];   // node at each depth-first position
-  int src[TV_MAX_NODES];     // where the parent state comes from: -1 registers, 0 S_0, else a slot
-  int push[TV_MAX_NODES];    // slot the node's own state goes to (-1: not needed later)
-  int leaf[TV_MAX_NODES];    // 1: no children -- its state is stored, never kept in registers
   // per depth-first position t: {node, (src + 1) | (push + 1) << 8 | (snapshot slot + 1) << 16,
   // alpha bits, beta bits}
   int4 ent[TV_MAX_NODES];
@@ -68,6 +67,9 @@ struct BuildScratch {
   int before[TV_MAX_NODES];  // nodes of earlier siblings' subtrees
   int pre[TV_MAX_NODES];     // depth-first position
   int slot[TV_MAX_NODES];    // snapshot slot of each node (selective fork), -1: none
+  int src[TV_MAX_NODES];     // where the parent state comes from: -1 registers, 0 S_0, else a slot
+  int push[TV_MAX_NODES];    // slot the node's own state goes to (-1: not needed later)
+  int leaf[TV_MAX_NODES];    // 1: no children -- its state is stored, never kept in registers
   int maxdepth, root_acc, kept;
 };
 
@@ -133,7 +135,7 @@ __device__ int build_schedule(const int32_t* __restrict__ parents, int N, Sched&
     // Leaves never disturb the parent state in registers, so a node saves its state only when
     // a second non-leaf child will need it after the first one's subtree.
     const int slot = x.nchild[i] - x.nleaf[i] >= 2 ? 1 + light : -1;
-    s.push[i] = slot;
+    x.push[i] = slot;
     if (slot > 0) atomicMax(&s.maxslot, slot);
   }
   __syncthreads();
@@ -142,10 +144,10 @@ __device__ int build_schedule(const int32_t* __restrict__ parents, int N, Sched&
     // A leaf, and the first non-leaf child (right after the leaves), find the parent state in
     // registers; a later non-leaf child pops it.
     const bool pops = p >= 0 && x.nchild[i] != 0 && x.pre[i] != x.pre[p] + 1 + x.nleaf[p];
-    s.src[i] = (p < 0) ? 0 : (pops ? s.push[p] : -1);
-    s.leaf[i] = x.nchild[i] == 0;
+    x.src[i] = (p < 0) ? 0 : (pops ? x.push[p] : -1);
+    x.leaf[i] = x.nchild[i] == 0;
     // never expected: guards every index
-    if (s.order[i] < 0 || s.src[i] > kSlots || (pops && s.push[p] <= 0)) s.flag = 1;
+    if (s.order[i] < 0 || x.src[i] > kSlots || (pops && x.push[p] <= 0)) s.flag = 1;
   }
   __syncthreads();
   return (s.maxslot <= kSlots && !s.flag) ? 0 : TV_ERR_UNSUPPORTED;
@@ -214,50 +216,81 @@ struct Raw<float, CPL> {
 // FROM_W: the second pass of the two-pass fork -- w_i (and every output) already came from the
 // TreeWY pass in wsrc [B, N, H, dv]; this pass only materializes the snapshots,
 // S_i = alpha_i S_p + w_i k_i^T, along the same walk.
-template <typename TIO, typename TS, int DK, bool FROM_W>
-__global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __restrict__ states,
-                                                            int ctas_per_seq, int nslots, ForkSelect sel,
-                                                            const float* __restrict__ wsrc) {
+//
+// RPL: state rows per lane group (1 or 2).  With two, a group of 8 lanes holds rows rg and
+// rg + 8 of the slab (64 threads per CTA): the k and q loads and conversions, the schedule
+// decode and the prefetch serve both rows, and the four row dot products of a node reduce
+// together in four shuffles (plus two to broadcast w), so a row costs about half the
+// instructions of the one-row form.
+struct UnitPlan {
+  int group, share, stride;  // CTAs per group, units per CTA at most, units between group starts
+};
+
+template <typename TIO, typename TS, int DK, bool FROM_W, int RPL>
+__device__ __forceinline__ void gdn_fork_body(const GdnArgs& a, TS* __restrict__ states, int nslots, UnitPlan plan,
+                                              const ForkSelect& sel, const float* __restrict__ wsrc) {
+  const int group = plan.group, share = plan.share, stride = plan.stride;
+  static_assert(RPL == 1 || (RPL == 2 && !FROM_W), "two rows per lane group in the one-pass form only");
   constexpr int CPL = DK / kLPR;  // columns per lane
-  constexpr int Q4 = CPL / 4;     // float4 per lane per slot
+  constexpr int Q4 = CPL / 4;     // float4 per lane per slot and row
+  constexpr int kThreads = kLanes / RPL;
+  constexpr int RG = kRows / RPL;  // row distance between a lane group's rows
   extern __shared__ __align__(128) unsigned char smem[];
   Sched& sc = *reinterpret_cast<Sched*>(smem);
   float4* stack = reinterpret_cast<float4*>(smem + sizeof(Sched));
   BuildScratch& scratch = *reinterpret_cast<BuildScratch*>(stack);
 
-  const int b = blockIdx.x / ctas_per_seq, g = blockIdx.x % ctas_per_seq;
   const int N = a.N, H = a.H, dv = a.dv;
   const int tid = threadIdx.x;
-  // A sequence the TreeWY pass rejected keeps its status and no snapshot (its slots go to -1
-  // below when selecting).
-  const int prior = FROM_W ? a.err[b] : 0;
-  int status = prior ? prior : build_schedule(a.parents + (size_t)b * N, N, sc, scratch);
-  if (!status && sc.maxslot > nslots) status = TV_ERR_UNSUPPORTED;
-  // Snapshot slots (selective fork): nodes at or below the confidence threshold, numbered in
-  // node order by one warp's ballot scan; otherwise slot = node.
-  if (sel.confidence != nullptr) {
-    if (tid < 32) {
-      int carry = 0;
-      for (int base = 0; base < N; base += 32) {
-        const int i = base + tid;
-        const bool keep = i < N && sel.confidence[(size_t)b * N + i] <= sel.threshold;
-        const unsigned m = __ballot_sync(0xffffffffu, keep);
-        if (i < N) scratch.slot[i] = keep ? carry + __popc(m & ((1u << tid) - 1u)) : -1;
-        carry += __popc(m);
+  // Work units are (sequence, head, 16-row slab) in that order, U = B H dv / 16 of them.  The
+  // CTAs form groups of `group`; group gamma owns the units [gamma * stride, gamma * stride +
+  // min(group * share, stride)), and its CTA g takes every group-th of them from g.  So a CTA
+  // gets at most `share` units, and at any moment a group's CTAs work on adjacent slabs: their
+  // snapshot rows of a node land side by side in HBM.  With stride = the units of a sequence,
+  // a group is one sequence; with stride = group * share, groups tile the units whatever B is
+  // (the launcher picks the form with the smaller share), and a CTA's units may run through two
+  // sequences.  The CTA builds the schedule of each sequence it enters; the CTA holding a
+  // sequence's first unit writes its status and slot map.
+  int b = -1;
+  // Schedule, snapshot slots and per-position entries of sequence b; the sequence's status.
+  auto setup = [&](bool first_cta) -> int {
+    // A sequence the TreeWY pass rejected keeps its status and no snapshot (its slots go to -1
+    // below when selecting).
+    const int prior = FROM_W ? a.err[b] : 0;
+    int status = prior ? prior : build_schedule(a.parents + (size_t)b * N, N, sc, scratch);
+    if (!status && sc.maxslot > nslots) status = TV_ERR_UNSUPPORTED;
+    // Snapshot slots (selective fork): nodes at or below the confidence threshold, numbered in
+    // node order by one warp's ballot scan; otherwise slot = node.
+    if (sel.confidence != nullptr) {
+      if (tid < 32) {
+        int carry = 0;
+        for (int base = 0; base < N; base += 32) {
+          const int i = base + tid;
+          const bool keep = i < N && sel.confidence[(size_t)b * N + i] <= sel.threshold;
+          const unsigned m = __ballot_sync(0xffffffffu, keep);
+          if (i < N) scratch.slot[i] = keep ? carry + __popc(m & ((1u << tid) - 1u)) : -1;
+          carry += __popc(m);
+        }
+        if (tid == 0) scratch.kept = carry;
       }
-      if (tid == 0) scratch.kept = carry;
+      __syncthreads();
+      if (!status && scratch.kept > sel.capacity) status = TV_ERR_CAPACITY;
+      // a sequence that is skipped keeps no snapshot: its commit then replays from S_0
+      if (first_cta && sel.slot != nullptr)
+        for (int i = tid; i < N; i += kThreads) sel.slot[(size_t)b * N + i] = status ? -1 : scratch.slot[i];
+    } else {
+      for (int i = tid; i < N; i += kThreads) scratch.slot[i] = i;
+      __syncthreads();
     }
-    __syncthreads();
-    if (!status && scratch.kept > sel.capacity) status = TV_ERR_CAPACITY;
-    // a sequence that is skipped keeps no snapshot: its commit then replays from S_0
-    if (g == 0 && sel.slot != nullptr)
-      for (int i = tid; i < N; i += kThreads) sel.slot[(size_t)b * N + i] = status ? -1 : scratch.slot[i];
-  } else {
-    for (int i = tid; i < N; i += kThreads) scratch.slot[i] = i;
-    __syncthreads();
-  }
-  if (g == 0 && tid == 0 && (status || !FROM_W)) a.err[b] = status;
-  if (status) return;
+    if (first_cta && tid == 0 && (status || !FROM_W)) a.err[b] = status;
+    if (status) return status;
+    for (int t = tid; t < N; t += kThreads) {
+      const int i = sc.order[t];
+      sc.ent[t] = make_int4(i, (scratch.src[i] + 1) | ((scratch.push[i] + 1) << 8) | ((scratch.slot[i] + 1) << 16) |
+                                   (scratch.leaf[i] << 28), 0, 0);
+    }
+    return 0;
+  };
 
   const TIO* __restrict__ q = static_cast<const TIO*>(a.q);
   const TIO* __restrict__ k = static_cast<const TIO*>(a.k);
@@ -265,22 +298,24 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
   const TS* __restrict__ S0 = static_cast<const TS*>(a.S0);
   TIO* __restrict__ out = static_cast<TIO*>(a.out);
   const int lane = tid % kLPR, rl = tid / kLPR;
+  // the row whose v this lane loads and whose output it may write: RPL = 2 splits the group
+  // into lanes 0-3 (row rl) and 4-7 (row rl + 8)
+  const int rmine = rl + (RPL == 2 && (lane & 4) ? RG : 0);
   const int slabs = dv / kRows, items = H * slabs;
   const float q_scale = a.q_scale;
   const size_t node_stride = (size_t)H * dv;     // elements between consecutive nodes (out, v)
   const size_t state_stride = node_stride * DK;  // elements between consecutive nodes (states)
   const size_t kq_stride = (size_t)H * DK;       // elements between consecutive nodes (q, k)
-
-  for (int t = tid; t < N; t += kThreads) {
-    const int i = sc.order[t];
-    sc.ent[t] = make_int4(i, (sc.src[i] + 1) | ((sc.push[i] + 1) << 8) | ((scratch.slot[i] + 1) << 16) |
-                                 (sc.leaf[i] << 28), 0, 0);
-  }
+  const long long units = (long long)a.B * items;
+  const long long u_base = (long long)(blockIdx.x / group) * stride;
+  const long long u_begin = u_base + blockIdx.x % group;
+  const long long u_end = min(units, u_base + min((long long)group * share, (long long)stride));
   // Pulls one item's inputs into L2 ahead of use: alpha, beta, k and q of every node, the
   // slab's v rows and S_0 rows.  The node loop's register prefetch then waits on L2, not HBM.
-  auto prefetch_item = [&](int it) {
+  auto prefetch_unit = [&](long long u) {
+    const int bb = (int)(u / items), it = (int)(u % items);
     const int hh = it / slabs, r0 = (it % slabs) * kRows;
-    const size_t n0 = (size_t)b * N * H + hh;
+    const size_t n0 = (size_t)bb * N * H + hh;
     const int kq_lines = DK * (int)sizeof(TIO) / 128 > 0 ? DK * (int)sizeof(TIO) / 128 : 1;
     const int per_node = 2 * kq_lines + 1;       // k lines, q lines, the slab's v rows
     for (int x = tid; x < N * per_node; x += kThreads) {
@@ -294,48 +329,64 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
     }
     const int s0_lines = kRows * DK * (int)sizeof(TS) / 128;
     for (int x = tid; x < s0_lines; x += kThreads)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(S0 + (((size_t)b * H + hh) * dv + r0) * DK) + x * 128));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(S0 + (((size_t)bb * H + hh) * dv + r0) * DK) + x * 128));
     for (int x = tid; x < (N * H + 31) / 32; x += kThreads) {  // alpha and beta of the sequence
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.alpha + (size_t)b * N * H + x * 32));
-      if (!FROM_W) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beta + (size_t)b * N * H + x * 32));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.alpha + (size_t)bb * N * H + x * 32));
+      if (!FROM_W) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.beta + (size_t)bb * N * H + x * 32));
     }
   };
-  if (g < items) prefetch_item(g);
-  for (int item = g; item < items; item += ctas_per_seq) {
-    const int h = item / slabs, r = (item % slabs) * kRows + rl;
+  if (u_begin < u_end) prefetch_unit(u_begin);
+  int status = 0;
+  for (long long u = u_begin; u < u_end; u += group) {
+    const int item = (int)(u % items);
+    if ((int)(u / items) != b) {
+      __syncthreads();                           // the previous sequence's walk is done with the stack
+      b = (int)(u / items);
+      status = setup(item == 0);
+    }
+    if (u + group < u_end) prefetch_unit(u + group);
+    if (status) continue;                        // the same in every thread
+    const int h = item / slabs, r0 = (item % slabs) * kRows, r = r0 + rl;
     const size_t nh0 = (size_t)b * N * H + h;    // (b, node 0, h)
-    if (item + ctas_per_seq < items) prefetch_item(item + ctas_per_seq);
     __syncthreads();                             // the previous item is done with alpha / beta
     for (int t = tid; t < N; t += kThreads) {
       const size_t nh = nh0 + (size_t)sc.ent[t].x * H;
       sc.ent[t].z = __float_as_int(__ldg(a.alpha + nh));
       sc.ent[t].w = FROM_W ? 0 : __float_as_int(__ldg(a.beta + nh));  // w already holds beta
     }
-    // k_i . q_i is the same for every row of the head: 8 threads per node compute it once.
+    // k_i . q_i is the same for every row of the head: 8 threads per node compute it once,
+    // with the loads of KQB nodes in flight at a time (four when 64 threads serve the item).
     // The loop bound is warp-uniform, so every lane takes part in the shuffles.
-    for (int t0 = 0; !FROM_W && t0 < N; t0 += kThreads / kLPR) {
-      const int t = t0 + tid / kLPR;
-      float dot = 0.f;
-      if (t < N) {
-        const size_t nh = nh0 + (size_t)sc.order[t] * H;
-        Raw<TIO, CPL> x;
-        x.load(k + nh * DK + lane * 8, q + nh * DK + lane * 8, v + nh * dv);
+    constexpr int kNodesPerPass = kThreads / kLPR;
+    constexpr int KQB = RPL == 2 ? 4 : 1;
+    for (int t0 = 0; !FROM_W && t0 < N; t0 += KQB * kNodesPerPass) {
+      Raw<TIO, CPL> x[KQB];
 #pragma unroll
-        for (int e = 0; e < CPL; ++e) dot = fmaf(x.kf(e), x.qf(e), dot);
+      for (int u = 0; u < KQB; ++u) {
+        const int t = t0 + u * kNodesPerPass + tid / kLPR;
+        const size_t nh = nh0 + (size_t)sc.order[t < N ? t : N - 1] * H;
+        x[u].load(k + nh * DK + lane * 8, q + nh * DK + lane * 8, v + nh * dv);
       }
-      dot = group_sum<kLPR>(dot);
-      if (t < N && lane == 0) sc.kq[t] = dot;
+#pragma unroll
+      for (int u = 0; u < KQB; ++u) {
+        const int t = t0 + u * kNodesPerPass + tid / kLPR;
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < CPL; ++e) dot = fmaf(x[u].kf(e), x[u].qf(e), dot);
+        dot = group_sum<kLPR>(dot);
+        if (t < N && lane == 0) sc.kq[t] = dot;
+      }
     }
     __syncthreads();
 
     const TIO* kb = k + nh0 * DK + lane * 8;
     const TIO* qb = q + nh0 * DK + lane * 8;
-    const TIO* vb = v + nh0 * dv + r;
+    const TIO* vb = v + nh0 * dv + r0 + rmine;
     const TS* s0row = S0 + (((size_t)b * H + h) * dv + r) * DK + lane * 8;
-    TIO* out_r = out + nh0 * dv + r;
+    TIO* out_r = out + nh0 * dv + r0 + rmine;
     // snapshots of this sequence: [capacity][H][dv][dk]
     TS* st_r = states + ((((size_t)b * sel.capacity) * H + h) * dv + r) * DK + lane * 8;
-    const float* wb = FROM_W ? wsrc + nh0 * dv + r : nullptr;
+    const float* wb = FROM_W ? wsrc + nh0 * dv + r0 + rmine : nullptr;
     auto fetch = [&](int t, Raw<TIO, CPL>& x) {
       x.e = sc.ent[t < N ? t : N - 1];
       const int node = x.e.x;
@@ -346,94 +397,138 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
         x.load(kb + node * kq_stride, qb + node * kq_stride, vb + node * node_stride);
       }
     };
-    float2 cur[CPL / 2];  // the row's state, column pairs (2e, 2e + 1)
+    float2 cur[RPL][CPL / 2];  // the rows' states, column pairs (2e, 2e + 1)
     // One node: parent state -> output and S_i (kept in cur), checkpoint, optional push.  The
     // two row dot products use the parent state, so they share one reduction:
     //   (S_p k)_r, (S_p q)_r  ->  w = beta (v_r - alpha (S_p k)_r),
     //   o_r = (S_i q)_r = alpha (S_p q)_r + w (k.q),   S_i = alpha S_p + w k^T,
-    // with k.q from the per-item table.  Column pairs go through the paired fp32 FMA.
+    // with k.q from the per-unit table.  Column pairs go through the paired fp32 FMA.
     auto body = [&](const Raw<TIO, CPL>& x) {
       const int i = x.e.x;
       const int src = (x.e.y & 255) - 1, push = ((x.e.y >> 8) & 255) - 1, slot = ((x.e.y >> 16) & 1023) - 1;
       const bool leaf = (x.e.y >> 28) & 1;
       const float al = __int_as_float(x.e.z), be = __int_as_float(x.e.w);
       if (src == 0) {
-        float f[CPL];
 #pragma unroll
-        for (int j = 0; j < CPL / 8; ++j) load_vec<8>(s0row + j * kStride, f + 8 * j);  // a root starts from S_0
+        for (int rr = 0; rr < RPL; ++rr) {
+          float f[CPL];
 #pragma unroll
-        for (int e = 0; e < CPL / 2; ++e) cur[e] = make_float2(f[2 * e], f[2 * e + 1]);
+          for (int j = 0; j < CPL / 8; ++j) load_vec<8>(s0row + rr * RG * DK + j * kStride, f + 8 * j);  // a root starts from S_0
+#pragma unroll
+          for (int e = 0; e < CPL / 2; ++e) cur[rr][e] = make_float2(f[2 * e], f[2 * e + 1]);
+        }
       } else if (src > 0) {
 #pragma unroll
-        for (int j = 0; j < Q4; ++j) {
-          const float4 f = stack[((src - 1) * Q4 + j) * kThreads + tid];
-          cur[2 * j] = make_float2(f.x, f.y);
-          cur[2 * j + 1] = make_float2(f.z, f.w);
-        }
+        for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+          for (int j = 0; j < Q4; ++j) {
+            const float4 f = stack[(((src - 1) * RPL + rr) * Q4 + j) * kThreads + tid];
+            cur[rr][2 * j] = make_float2(f.x, f.y);
+            cur[rr][2 * j + 1] = make_float2(f.z, f.w);
+          }
       }
       float2 kf[CPL / 2];
 #pragma unroll
       for (int e = 0; e < CPL / 2; ++e) kf[e] = make_float2(x.kf(2 * e), x.kf(2 * e + 1));
-      float w;                                              // pseudo-value w_i[r]
+      float w[RPL];                                         // pseudo-values w_i[r] of the rows
       if constexpr (FROM_W) {
-        w = x.v;
+        w[0] = x.v;
       } else {
-        float2 qf[CPL / 2];
+        // Lane partials of (S_p k)_r and (S_p q)_r for each row.  With two rows they reduce in
+        // one butterfly over the group's 8 lanes in which every exchange moves half of the values
+        // still unreduced: lanes 0-3 / 4-7 keep row 0 / row 1, then lanes with bit 1 clear / set
+        // keep the k / q product, so lane l ends with the full S_p k (bit 1 clear) or S_p q (set)
+        // of row (l >> 2) & 1.
+        float pk[RPL], pq[RPL];
 #pragma unroll
-        for (int e = 0; e < CPL / 2; ++e) qf[e] = make_float2(x.qf(2 * e), x.qf(2 * e + 1));
-        float2 pk0 = make_float2(0.f, 0.f), pk1 = pk0, pq0 = pk0, pq1 = pk0;
+        for (int rr = 0; rr < RPL; ++rr) {
+          float2 k0 = make_float2(0.f, 0.f), q0 = k0, k1 = k0, q1 = k0;
 #pragma unroll
-        for (int e = 0; e < CPL / 2; e += 2) {
-          pk0 = __ffma2_rn(cur[e], kf[e], pk0);
-          pq0 = __ffma2_rn(cur[e], qf[e], pq0);
-          pk1 = __ffma2_rn(cur[e + 1], kf[e + 1], pk1);
-          pq1 = __ffma2_rn(cur[e + 1], qf[e + 1], pq1);
+          for (int e = 0; e < CPL / 2; e += 2) {
+            const float2 qa = make_float2(x.qf(2 * e), x.qf(2 * e + 1));
+            const float2 qb = make_float2(x.qf(2 * e + 2), x.qf(2 * e + 3));
+            k0 = __ffma2_rn(cur[rr][e], kf[e], k0);
+            q0 = __ffma2_rn(cur[rr][e], qa, q0);
+            k1 = __ffma2_rn(cur[rr][e + 1], kf[e + 1], k1);
+            q1 = __ffma2_rn(cur[rr][e + 1], qb, q1);
+          }
+          pk[rr] = (k0.x + k1.x) + (k0.y + k1.y);
+          pq[rr] = (q0.x + q1.x) + (q0.y + q1.y);
         }
-        float pk = (pk0.x + pk1.x) + (pk0.y + pk1.y), pq = (pq0.x + pq1.x) + (pq0.y + pq1.y);
+        if constexpr (RPL == 2) {
+          const bool b2 = lane & 4, b1 = lane & 2;
+          const float sk = __shfl_xor_sync(0xffffffffu, b2 ? pk[0] : pk[1], 4);
+          const float sq = __shfl_xor_sync(0xffffffffu, b2 ? pq[0] : pq[1], 4);
+          const float mk = (b2 ? pk[1] : pk[0]) + sk, mq = (b2 ? pq[1] : pq[0]) + sq;
+          float m = (b1 ? mq : mk) + __shfl_xor_sync(0xffffffffu, b1 ? mk : mq, 2);
+          m += __shfl_xor_sync(0xffffffffu, m, 1);
+          // w of this lane's row, valid where m is S_p k (lanes 0 and 4), to every lane
+          const float wl = be * (x.v - al * m);
+          const int g0 = (tid & 31) & ~(kLPR - 1);  // the group's first lane in the warp
+          w[0] = __shfl_sync(0xffffffffu, wl, g0);
+          w[1] = __shfl_sync(0xffffffffu, wl, g0 + 4);
+          // the output of this lane's row from lane 2 / 6, which hold S_p q
+          if ((lane & 3) == 2) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * m + (b2 ? w[1] : w[0]) * x.kq) * q_scale);
+        } else {
+          // one row: both sums to every lane in two independent chains of three shuffles
+          float sk = pk[0], sq = pq[0];
 #pragma unroll
-        for (int o = kLPR / 2; o > 0; o >>= 1) {
-          pk += __shfl_xor_sync(0xffffffffu, pk, o);
-          pq += __shfl_xor_sync(0xffffffffu, pq, o);
+          for (int o = kLPR / 2; o > 0; o >>= 1) {
+            sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            sq += __shfl_xor_sync(0xffffffffu, sq, o);
+          }
+          w[0] = be * (x.v - al * sk);
+          if (lane == 0) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * sq + w[0] * x.kq) * q_scale);
         }
-        w = be * (x.v - al * pk);
-        if (lane == 0) out_r[(size_t)i * node_stride] = from_f32<TIO>((al * pq + w * x.kq) * q_scale);
       }
-      const float2 al2 = make_float2(al, al), w2 = make_float2(w, w);
+      const float2 al2 = make_float2(al, al);
       if (leaf) {
         // A leaf's state only goes to its snapshot: cur keeps the parent state for the siblings.
         if (slot >= 0) {
-          float f[CPL];
 #pragma unroll
-          for (int e = 0; e < CPL / 2; ++e) {
-            const float2 s2 = __ffma2_rn(w2, kf[e], __fmul2_rn(al2, cur[e]));
-            f[2 * e] = s2.x;
-            f[2 * e + 1] = s2.y;
+          for (int rr = 0; rr < RPL; ++rr) {
+            const float2 w2 = make_float2(w[rr], w[rr]);
+            float f[CPL];
+#pragma unroll
+            for (int e = 0; e < CPL / 2; ++e) {
+              const float2 s2 = __ffma2_rn(w2, kf[e], __fmul2_rn(al2, cur[rr][e]));
+              f[2 * e] = s2.x;
+              f[2 * e + 1] = s2.y;
+            }
+#pragma unroll
+            for (int j = 0; j < CPL / 8; ++j)
+              store_vec_cs<8>(st_r + (size_t)slot * state_stride + rr * RG * DK + j * kStride, f + 8 * j);
           }
-#pragma unroll
-          for (int j = 0; j < CPL / 8; ++j) store_vec_cs<8>(st_r + (size_t)slot * state_stride + j * kStride, f + 8 * j);
         }
         return;
       }
 #pragma unroll
-      for (int e = 0; e < CPL / 2; ++e) cur[e] = __ffma2_rn(w2, kf[e], __fmul2_rn(al2, cur[e]));
-      {
+      for (int rr = 0; rr < RPL; ++rr) {
+        const float2 w2 = make_float2(w[rr], w[rr]);
+#pragma unroll
+        for (int e = 0; e < CPL / 2; ++e) cur[rr][e] = __ffma2_rn(w2, kf[e], __fmul2_rn(al2, cur[rr][e]));
         float f[CPL];
 #pragma unroll
-        for (int e = 0; e < CPL / 2; ++e) { f[2 * e] = cur[e].x; f[2 * e + 1] = cur[e].y; }
+        for (int e = 0; e < CPL / 2; ++e) { f[2 * e] = cur[rr][e].x; f[2 * e + 1] = cur[rr][e].y; }
         if (slot >= 0) {
 #pragma unroll
-          for (int j = 0; j < CPL / 8; ++j) store_vec_cs<8>(st_r + (size_t)slot * state_stride + j * kStride, f + 8 * j);
+          for (int j = 0; j < CPL / 8; ++j)
+            store_vec_cs<8>(st_r + (size_t)slot * state_stride + rr * RG * DK + j * kStride, f + 8 * j);
         }
       }
       if (push > 0) {
 #pragma unroll
-        for (int j = 0; j < Q4; ++j)
-          stack[((push - 1) * Q4 + j) * kThreads + tid] =
-              make_float4(cur[2 * j].x, cur[2 * j].y, cur[2 * j + 1].x, cur[2 * j + 1].y);
+        for (int rr = 0; rr < RPL; ++rr)
+#pragma unroll
+          for (int j = 0; j < Q4; ++j)
+            stack[(((push - 1) * RPL + rr) * Q4 + j) * kThreads + tid] =
+                make_float4(cur[rr][2 * j].x, cur[rr][2 * j].y, cur[rr][2 * j + 1].x, cur[rr][2 * j + 1].y);
       }
     };
-    // Three register buffers rotate by unrolling, so each prefetch stays in flight for two
-    // nodes (a register copy would wait for it).
+    // Two register buffers alternate by unrolling: node t + 1's inputs are requested before node
+    // t is computed (a register copy would wait for the load).  A deeper register prefetch and a
+    // cp.async ring in shared memory measured slower: the walk is bound by issue and by the
+    // dependent chain of each node, not by these loads.
     Raw<TIO, CPL> ra, rb;
     fetch(0, ra);
     for (int t = 0; t < N; t += 2) {
@@ -446,13 +541,37 @@ __global__ void __launch_bounds__(kThreads) gdn_fork_kernel(GdnArgs a, TS* __res
   }
 }
 
-template <typename TIO, typename TS, int DK, bool FROM_W = false>
-cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel, cudaStream_t s,
-                          const float* wsrc = nullptr, int max_ctas_per_sm = 0) {
-  auto kern = gdn_fork_kernel<TIO, TS, DK, FROM_W>;
+// Entry points over the same body.  The plain one leaves the register budget to the compiler;
+// the bounded ones ask for six (80 registers) or five 128-thread CTAs per SM, which pays for
+// the snapshot pass when its stack lets that many CTAs fit (at most three slots: six; four
+// slots: five) -- and only then: a minimum-blocks bound that does not raise occupancy measured
+// slower.
+template <typename TIO, typename TS, int DK, bool FROM_W, int RPL>
+__global__ void __launch_bounds__(kLanes / RPL) gdn_fork_kernel(GdnArgs a, TS* __restrict__ states, int nslots,
+                                                                UnitPlan plan, ForkSelect sel,
+                                                                const float* __restrict__ wsrc) {
+  gdn_fork_body<TIO, TS, DK, FROM_W, RPL>(a, states, nslots, plan, sel, wsrc);
+}
+template <typename TIO, typename TS, int DK, int MINB>
+__global__ void __launch_bounds__(kLanes, MINB) gdn_fork_snapshot_kernel(GdnArgs a, TS* __restrict__ states,
+                                                                         int nslots, UnitPlan plan, ForkSelect sel,
+                                                                         const float* __restrict__ wsrc) {
+  gdn_fork_body<TIO, TS, DK, true, 1>(a, states, nslots, plan, sel, wsrc);
+}
+
+template <typename TIO, typename TS, int DK, bool FROM_W, int RPL>
+cudaError_t launch_fork_rpl(const GdnArgs& a, void* states, const ForkSelect& sel, cudaStream_t s,
+                            const float* wsrc, int max_ctas_per_sm) {
+  constexpr int kThreads = kLanes / RPL;
   const int nslots = slots_for(a.N);
-  size_t stack = (size_t)nslots * (DK / kLPR / 4) * kThreads * sizeof(float4);
+  void (*kern)(GdnArgs, TS*, int, UnitPlan, ForkSelect, const float*) = gdn_fork_kernel<TIO, TS, DK, FROM_W, RPL>;
+  if constexpr (FROM_W) {
+    if (nslots <= 3) kern = gdn_fork_snapshot_kernel<TIO, TS, DK, 6>;
+    else if (nslots == 4) kern = gdn_fork_snapshot_kernel<TIO, TS, DK, 5>;
+  }
+  size_t stack = (size_t)nslots * (DK / kLPR / 4) * kLanes * sizeof(float4);
   if (stack < sizeof(BuildScratch)) stack = sizeof(BuildScratch);
+  stack = (stack + 15) / 16 * 16;
   const size_t smem = sizeof(Sched) + stack;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -460,16 +579,51 @@ cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel,
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
   if (e != cudaSuccess) return e;
   if (max_ctas_per_sm > 0 && occ > max_ctas_per_sm) occ = max_ctas_per_sm;
-  const int items = a.H * (a.dv / kRows);
-  const int slots = device_sm_count() * (occ > 0 ? occ : 1);
-  int per_seq = slots / a.B;
-  if (per_seq < 1) per_seq = 1;
-  if (per_seq > items) per_seq = items;
-  // The fewest CTAs per sequence with the same longest CTA: slots freed for other streams' work
-  // without lengthening this kernel.
-  per_seq = (items + (items + per_seq - 1) / per_seq - 1) / ((items + per_seq - 1) / per_seq);
-  kern<<<a.B * per_seq, kThreads, smem, s>>>(a, static_cast<TS*>(states), per_seq, nslots, sel, wsrc);
+  // At most one CTA per resident slot.  Either every sequence gets the same number of CTAs (a
+  // group per sequence, no CTA crosses sequences) or groups of kGroup CTAs tile the units
+  // regardless of sequence boundaries (an equal share whatever B is); the form with the smaller
+  // largest share (times the waves it needs) wins.  Then the fewest CTAs with that share,
+  // which frees slots for other streams' work without lengthening this kernel.
+  const long long items = (long long)a.H * (a.dv / kRows), units = a.B * items;
+  const long long slots = (long long)device_sm_count() * (occ > 0 ? occ : 1);
+  long long per_seq = slots / a.B;
+  per_seq = per_seq < 1 ? 1 : (per_seq > items ? items : per_seq);
+  const long long share_seq = (items + per_seq - 1) / per_seq;
+  long long groups = slots / kGroup;
+  if (groups < 1) groups = 1;
+  const long long share_grp = (units + groups * kGroup - 1) / (groups * kGroup);
+  // more sequences than slots: the per-sequence form runs in waves
+  const long long waves_seq = (a.B * per_seq + slots - 1) / slots;
+  UnitPlan plan;
+  long long grid;
+  // On a tie the groups win only when they tile each sequence exactly (measured: the strided
+  // per-sequence order is faster than groups that straddle sequences, slower than ones that
+  // do not).
+  const bool grp_tiles = items % (share_grp * kGroup) == 0;
+  if (share_seq * waves_seq < share_grp || (share_seq * waves_seq == share_grp && !grp_tiles)) {
+    per_seq = (items + share_seq - 1) / share_seq;
+    plan = UnitPlan{(int)per_seq, (int)share_seq, (int)items};
+    grid = a.B * per_seq;
+  } else {
+    groups = (units + share_grp * kGroup - 1) / (share_grp * kGroup);
+    plan = UnitPlan{kGroup, (int)share_grp, (int)(share_grp * kGroup)};
+    grid = groups * kGroup;
+  }
+  kern<<<(unsigned)grid, kThreads, smem, s>>>(a, static_cast<TS*>(states), nslots, plan, sel, wsrc);
   return cudaGetLastError();
+}
+
+// The one-pass form takes two rows per lane group for bf16 inputs when the tree needs at most
+// three stack slots (N <= 46): its 64-thread CTAs then fit six to an SM and issue about a third
+// fewer instructions per row.  Deeper stacks, fp32 inputs (twice the registers per row) and the
+// snapshot pass (no dot products to share) keep one row per group.
+template <typename TIO, typename TS, int DK, bool FROM_W = false>
+cudaError_t launch_fork_t(const GdnArgs& a, void* states, const ForkSelect& sel, cudaStream_t s,
+                          const float* wsrc = nullptr, int max_ctas_per_sm = 0) {
+  if constexpr (!FROM_W && sizeof(TIO) == 2) {
+    if (slots_for(a.N) <= 3) return launch_fork_rpl<TIO, TS, DK, FROM_W, 2>(a, states, sel, s, wsrc, max_ctas_per_sm);
+  }
+  return launch_fork_rpl<TIO, TS, DK, FROM_W, 1>(a, states, sel, s, wsrc, max_ctas_per_sm);
 }
 
 }  // namespace
