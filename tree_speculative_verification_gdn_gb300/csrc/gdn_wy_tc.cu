@@ -583,7 +583,9 @@ struct TcHeadS {
   int lz_nodes[kLazyMaxLen];
   float lz_g[kLazyMaxLen];
   float lz_lga;
-  int lz_L, lz_status, lz_pad[3];
+  int lz_L, lz_status;
+  int lz_store;          // a TMA store is reading the committed tile
+  int lz_pad;
 };
 static_assert(sizeof(TcHeadS) % 16 == 0, "the entry table after the head is 16-byte aligned");
 
@@ -592,7 +594,7 @@ struct WySmallLayout {
 };
 // Byte offsets from the 1024-byte aligned base: S_0 tile, stacked [K; Q] tiles, V tile (when it
 // fits), head, path-entry coefficients (cap float2 {c, e}), the entries' ancestor positions
-// (cap int, deep trees only), lazy-commit rows.  The second k-block's
+// (cap int, deep trees only), lazy-commit rows (w and keys, fp32).  The second k-block's
 // D2 A operand reads 128 rows from its start, so the allocation extends at least 16 KB past it.
 __host__ __device__ inline WySmallLayout wy_small_layout(int Npad, int cap, bool lazy, bool v_in_smem) {
   WySmallLayout L{};
@@ -605,7 +607,7 @@ __host__ __device__ inline WySmallLayout wy_small_layout(int Npad, int cap, bool
   uint32_t end = (L.anc + (uint32_t)cap * 4u + 15u) & ~15u;
   L.lz_w = end;
   L.lz_k = L.lz_w + (lazy ? (uint32_t)kLazyMaxLen * kD * 4u : 0u);
-  end = L.lz_k + (lazy ? (uint32_t)kLazyMaxLen * kD * 2u : 0u);
+  end = L.lz_k + (lazy ? (uint32_t)kLazyMaxLen * kD * 4u : 0u);
   const uint32_t overrun = L.kq + region + 128u * 128u;
   L.total = end > overrun ? end : overrun;
   return L;
@@ -713,6 +715,7 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
     hd.flag = 0;
     hd.maxdepth = 0;
     hd.mma_issued = 0;
+    hd.lz_store = 0;
     mbar_fence_init();
   }
   if (warp == 0) tmem_alloc(&hd.tmem_base, tmem_cols);
@@ -724,10 +727,10 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
   int* lz_nodes = hd.lz_nodes;
   float* lz_g = hd.lz_g;
   float* lz_w = reinterpret_cast<float*>(smem + Ly.lz_w);  // [L][128]
-  bf16* lz_k = reinterpret_cast<bf16*>(smem + Ly.lz_k);    // [L][128]
+  float* lz_k = reinterpret_cast<float*>(smem + Ly.lz_k);  // [L][128], converted once for every row
 
   if (warp >= 2) {
-    if (tid == 64) {
+    auto issue_tiles = [&]() {
       mbar_arrive_expect_tx(&hd.tma_bar, kTileA + (uint32_t)(v_in_smem ? 6 : 4) * (uint32_t)Npad * 128u);
       for (int kb = 0; kb < 2; ++kb) {
         tma_load_2d(sA + kb * (kTileA / 2), &mS0, kb * 64, (b * H + h) * kD, &hd.tma_bar);
@@ -735,16 +738,17 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
         tma_load_4d(sKQ + kb * region + Npad * 128, &mQ, kb * 64, h, 0, b, &hd.tma_bar);
         if (v_in_smem) tma_load_4d(sV + kb * Npad * 128, &mV, kb * 64, h, 0, b, &hd.tma_bar);
       }
-      // Without a commit to fold in, the MMAs start as soon as the tiles have landed.
-      if (!LAZY) {
-        if (mbar_wait(&hd.tma_bar, 0)) wy_small_issue_mma(tmem, sA, sKQ, region, Npad, hd);
-        else hd.fail = 1;
-      }
+    };
+    if (tid == 64 && !LAZY) {
+      issue_tiles();
+      if (mbar_wait(&hd.tma_bar, 0)) wy_small_issue_mma(tmem, sA, sKQ, region, Npad, hd);
+      else hd.fail = 1;
     }
     if (LAZY) {
       // The previous round's accepted path (TreeWY abstract: rebuild only the accepted state):
       // warps 2-3 stage the path's w and key rows from the unchecked entries, clamped into
-      // range, while warp 2 checks the links, one entry per lane.
+      // range, while warp 2 checks the links, one entry per lane.  Those loads go out before
+      // the tiles are requested (thread 64), so they do not queue behind them.
       const int Lraw = lz_len;
       const int Lc = Lraw < 0 ? 0 : min(Lraw, min(kLazyMaxLen, min(lz.Lmax, lz.Np)));
       // Every path entry first, then every row element (columns u and u + 64 of each entry), so
@@ -756,31 +760,44 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
         const int e = t < Lc ? lz_ent[t] : 0;
         node[t] = e < 0 ? 0 : (e >= lz.Np ? lz.Np - 1 : e);
       }
+      float w0[kLazyMaxLen], w1[kLazyMaxLen];
+      bf16 k0[kLazyMaxLen], k1[kLazyMaxLen];
 #pragma unroll
       for (int t = 0; t < kLazyMaxLen; ++t) {
         if (t < Lc) {
           const size_t nh = ((size_t)b * lz.Np + node[t]) * H + h;
           const float* w = lz.pseudo_v + nh * kD;
           const bf16* k = static_cast<const bf16*>(lz.k) + nh * kD;
-          lz_w[t * kD + u] = w[u];
-          lz_w[t * kD + u + 64] = w[u + 64];
-          lz_k[t * kD + u] = k[u];
-          lz_k[t * kD + u + 64] = k[u + 64];
+          w0[t] = w[u];
+          w1[t] = w[u + 64];
+          k0[t] = k[u];
+          k1[t] = k[u + 64];
+        }
+      }
+      const bool len_ok = Lraw >= 1 && Lraw <= lz.Lmax && Lraw <= lz.Np && Lraw <= kLazyMaxLen;
+      int lnode = -1, pn = -1;
+      float lgt = 0.f;
+      if (warp == 2 && len_ok && lane < Lraw) {
+#pragma unroll
+        for (int t = 0; t < kLazyMaxLen; ++t)
+          if (t == lane) lnode = lz_ent[t];
+        if (lnode >= 0 && lnode < lz.Np) {
+          pn = lz.parents[(size_t)b * lz.Np + lnode];
+          lgt = lz.log_gamma[((size_t)b * lz.Np + lnode) * H + h];
+        }
+      }
+      if (tid == 64) issue_tiles();
+#pragma unroll
+      for (int t = 0; t < kLazyMaxLen; ++t) {
+        if (t < Lc) {
+          lz_w[t * kD + u] = w0[t];
+          lz_w[t * kD + u + 64] = w1[t];
+          lz_k[t * kD + u] = to_f32(k0[t]);
+          lz_k[t * kD + u + 64] = to_f32(k1[t]);
         }
       }
       if (warp == 2) {  // the path's links, one entry per lane
-        const bool len_ok = Lraw >= 1 && Lraw <= lz.Lmax && Lraw <= lz.Np && Lraw <= kLazyMaxLen;
-        int node = -1, pn = -1;
-        float lgt = 0.f;
-        if (len_ok && lane < Lraw) {
-#pragma unroll
-          for (int t = 0; t < kLazyMaxLen; ++t)
-            if (t == lane) node = lz_ent[t];
-          if (node >= 0 && node < lz.Np) {
-            pn = lz.parents[(size_t)b * lz.Np + node];
-            lgt = lz.log_gamma[((size_t)b * lz.Np + node) * H + h];
-          }
-        }
+        const int node = lnode;
         int prev = __shfl_up_sync(0xffffffffu, node, 1);
         if (lane == 0) prev = -1;
         const bool mine = lane >= Lraw || (node >= 0 && node < lz.Np && pn == prev);
@@ -797,48 +814,6 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
         }
       }
       bar_sync_named(2, 64);
-      if (!hd.lz_status) {
-        // While warps 0-1 analyse the tree: S_0 <- gamma_a S_0 + sum_t (gamma_a / gamma_t) w_t
-        // k_t^T on the swizzled tile, in the commit kernel's operation order, thread u taking
-        // rows u and u + 64, one k-block (64 columns) at a time.  The MMAs then read the
-        // committed state; it goes back to HBM after the join, if the sequence runs.
-        const bool landed = mbar_wait(&hd.tma_bar, 0);
-        if (landed) {
-          const int L = hd.lz_L;
-          const float gam = expf(hd.lz_lga);
-          for (int row = tid - 64; row < kD; row += 64) {
-            for (int kb = 0; kb < 2; ++kb) {
-              unsigned char* rowp = sA + kb * (kTileA / 2) + row * 128;
-              float x[8][8];
-#pragma unroll
-              for (int ch = 0; ch < 8; ++ch) {
-                unpack8(*reinterpret_cast<const uint4*>(rowp + ((ch ^ (row & 7)) << 4)), x[ch]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[ch][e] *= gam;
-              }
-              for (int t = 0; t < L; ++t) {
-                const float c = lz_g[t] * lz_w[t * kD + row];
-                const uint4* kr = reinterpret_cast<const uint4*>(lz_k + t * kD + kb * 64);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                  float kf[8];
-                  unpack8(kr[ch], kf);
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) x[ch][e] = fmaf(c, kf[e], x[ch][e]);
-                }
-              }
-#pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4)) = pack8(x[ch]);
-            }
-          }
-          fence_proxy_async();  // the MMA reads the tile through the async proxy
-        } else if (tid == 64) {
-          hd.fail = 1;
-        }
-        bar_sync_named(2, 64);
-        if (tid == 64 && landed) wy_small_issue_mma(tmem, sA, sKQ, region, Npad, hd);
-      }
     }
   } else {
     // Tree analysis, warps 0-1 (named barrier 1): a parent must be -1 or an earlier node.
@@ -943,17 +918,65 @@ __global__ void __launch_bounds__(kSThreads, 1) gdn_wy_tc_small_kernel(
   int status = hd.flag ? TV_ERR_BAD_TREE : 0;
   if (LAZY && !status) status = hd.lz_status;
 
-  if (LAZY && !status && !hd.fail) {
-    // The committed state back to HBM (rows of the updated tile, 16 bytes per copy).
-    bf16* g = static_cast<bf16*>(const_cast<void*>(a.S0)) + ((size_t)b * H + h) * kD * kD;
-    for (int x = tid; x < 2 * kD * 8; x += kSThreads) {
-      const int row = x >> 4, kb = (x >> 3) & 1, ch = x & 7;
-      reinterpret_cast<uint4*>(g + (size_t)row * kD + kb * 64)[ch] =
-          *reinterpret_cast<const uint4*>(sA + kb * (kTileA / 2) + row * 128 + ((ch ^ (row & 7)) << 4));
+  if constexpr (LAZY) {
+    // The commit, once the analysis and the staging are both done: every thread takes one row,
+    // S_0[r] <- gamma_a S_0[r] + sum_t (gamma_a / gamma_t) w_t[r] k_t, in the commit kernel's
+    // operation order (paired FMAs are two plain ones), and writes it into the tile; thread 64
+    // then starts the MMAs on it and two TMA stores that write it back to HBM.  A sequence that
+    // does not run (bad tree or path) keeps its state.
+    if (!status && !hd.fail) {
+      const int row = tid, L = hd.lz_L;
+      const float gam = expf(hd.lz_lga);
+      if (mbar_wait(&hd.tma_bar, 0)) {
+        const float2 gam2 = make_float2(gam, gam);
+        for (int kb = 0; kb < 2; ++kb) {
+          unsigned char* rowp = sA + kb * (kTileA / 2) + row * 128;
+          float2 x[32];
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4*>(rowp + ((ch ^ (row & 7)) << 4)), f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[4 * ch + e] = __fmul2_rn(make_float2(f[2 * e], f[2 * e + 1]), gam2);
+          }
+          for (int t = 0; t < L; ++t) {
+            const float c = lz_g[t] * lz_w[t * kD + row];
+            const float2 c2 = make_float2(c, c);
+            const float4* kr = reinterpret_cast<const float4*>(lz_k + t * kD + kb * 64);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float4 k4 = kr[q];
+              x[2 * q] = __ffma2_rn(c2, make_float2(k4.x, k4.y), x[2 * q]);
+              x[2 * q + 1] = __ffma2_rn(c2, make_float2(k4.z, k4.w), x[2 * q + 1]);
+            }
+          }
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { f[2 * e] = x[4 * ch + e].x; f[2 * e + 1] = x[4 * ch + e].y; }
+            *reinterpret_cast<uint4*>(rowp + ((ch ^ (row & 7)) << 4)) = pack8(f);
+          }
+        }
+        fence_proxy_async();  // the MMAs read the tile through the async proxy
+      } else {
+        hd.fail = 1;
+      }
+    }
+    __syncthreads();  // the tile is committed (and hd.fail settled)
+    if (tid == 64 && !status && !hd.fail) {
+      wy_small_issue_mma(tmem, sA, sKQ, region, Npad, hd);
+      for (int kb = 0; kb < 2; ++kb)
+        asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                     ::"l"(&mS0), "r"(kb * 64), "r"((b * H + h) * kD), "r"(smem_addr(sA + kb * (kTileA / 2)))
+                     : "memory");
+      bulk_commit();
+      hd.lz_store = 1;
     }
   }
   const bool run = !status && !hd.fail;
   if (run && !mbar_wait(&hd.mma_bar, 0)) hd.fail = 1;
+  if (LAZY && tid == 64 && hd.lz_store) bulk_wait_read<0>();  // the tile is free once the store has read it
   tc_fence_after();
   __syncthreads();
 
