@@ -301,3 +301,27 @@ def test_small_tree_solve_variants(shape):
         trees = [[-1], [-1]]
     case = W.gdn_case(trees, H=3, dk=128, dv=128, io="bf16", state="bf16", seed=len(shape))
     _check_all(case)
+
+
+def test_wy_commit_with_a_wide_path_table_equals_the_staged_form():
+    """The WY commit stages the S_0 tile and the path's rows in shared memory when both fit, and
+    streams the tile through registers when a wide path table (min(Lmax, N) rows staged) leaves
+    no room for it.  Both forms compute the same arithmetic: equal bit for bit, and equal to
+    the oracle's commit within the bf16 rule."""
+    rng = np.random.default_rng(21)
+    trees = [W.random_tree(256, rng, max_children=4, max_depth=8) for _ in range(2)]
+    # bf16 keys, fp32 state: a 64 KB tile, and 256 staged rows of 768 bytes with the wide table
+    case = W.gdn_case(trees, H=2, dk=128, dv=128, io="bf16", state="f32", seed=21)
+    w = _gpu.run_wy(case)
+    assert (w["err"] == 0).all()
+    narrow = _gpu.run_commit(case, "wy", w)
+    B, Lmax = case.path.shape
+    wide = torch.full((B, 256), -1, dtype=torch.int32)
+    wide[:, :Lmax] = case.path
+    wide_S0 = _gpu.run_commit(case, "wy", w, path=wide)
+    assert (w["commit_err"] == 0).all()
+    assert torch.equal(narrow, wide_S0)
+    inp = case.oracle_inputs()
+    for b in range(B):
+        ref = G.node_state(inp, b, int(case.path[b, int(case.path_len[b]) - 1]))[0]
+        _gpu.assert_close(narrow[b], ref, "bf16", "wy commit, staged and register forms", stored="f32")

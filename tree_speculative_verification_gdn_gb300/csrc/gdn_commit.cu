@@ -155,16 +155,117 @@ constexpr int kLPR = 8;
 constexpr int kRows = 32;          // rows of S_0 per pass of a CTA in WY mode
 constexpr int kStride = 8 * kLPR;  // lane l holds columns l * 8 + j * kStride .. + 7
 
-// One CTA per (sequence, head): S_0 <- gamma_a S_0 + sum_r Gamma w k^T.  Thread (row rl, lane)
-// owns rows rl, rl + 32, ... of the head.  All of them are loaded before the path check; the
-// path's log(gamma), w rows and keys are then fetched in one phase into shared memory.
+// One CTA per (sequence, head): S_0 <- gamma_a S_0 + sum_r Gamma w k^T.  Thread 0 starts a bulk
+// copy of the head's S_0 tile into shared memory at once; the path's log(gamma), w rows and keys
+// are fetched while the path is checked.  Thread (row rl, lane) then updates rows rl, rl + 32,
+// ... of the tile in place, and one bulk store writes the tile back.
 template <typename TIO, typename TS, int DK>
-__global__ void __launch_bounds__(kThreads, 4) commit_wy_kernel(CommitArgs a0) {
+__global__ void __launch_bounds__(kThreads) commit_wy_kernel(CommitArgs a0) {
   constexpr int CPL = DK / kLPR;
   __shared__ PathCheck pc;
   __shared__ float coef[TV_MAX_NODES];
   __shared__ float lga_s;
-  extern __shared__ __align__(16) unsigned char dyn[];  // w [cap][dv] fp32, then k [cap][DK]
+  __shared__ __align__(8) uint64_t bar;
+  // the S_0 tile [dv][DK], then w [cap][dv] fp32, then k [cap][DK]
+  extern __shared__ __align__(128) unsigned char dyn[];
+  const int layer = blockIdx.x / (a0.B * a0.H), bh = blockIdx.x % (a0.B * a0.H);
+  const CommitArgs a = layer_view(a0, layer);
+  const int passes = a.dv / kRows;
+  const int b = bh / a.H, h = bh % a.H;
+  const int N = a.N, H = a.H, dv = a.dv;
+  const int cap = a.Lmax < N ? a.Lmax : N;
+  const uint32_t tile = (uint32_t)dv * DK * sizeof(TS);  // bytes, a multiple of 16
+  TS* tile_s = reinterpret_cast<TS*>(dyn);
+  float* wsm = reinterpret_cast<float*>(dyn + tile);
+  TIO* ksm = reinterpret_cast<TIO*>(dyn + tile + (size_t)cap * dv * sizeof(float));
+  TS* s0 = static_cast<TS*>(a.S0) + ((size_t)b * H + h) * dv * DK;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    mbar_arrive_expect_tx(&bar, tile);
+    bulk_g2s(tile_s, s0, tile, &bar);
+  }
+
+  // The path's log(gamma), w rows and keys are fetched from the unchecked path (its length and
+  // nodes clamped into range, so every read is in bounds) while the path is being checked; they
+  // are used only if the check passes, and then they are the path's.
+  const int Lu = path_prefetch(a, b, pc);  // its barrier also publishes the initialised mbarrier
+  auto node_at = [&](int r) {  // the unchecked entry, clamped into [0, N)
+    const int n = pc.path[r];
+    return n < 0 ? 0 : (n >= N ? N - 1 : n);
+  };
+  for (int r = threadIdx.x; r < Lu; r += kThreads) coef[r] = a.log_gamma[((size_t)b * N + node_at(r)) * H + h];
+  for (int x = threadIdx.x; x < Lu * dv; x += kThreads) {
+    const int r = x / dv, rr = x % dv;
+    wsm[x] = a.pseudo_v[(((size_t)b * N + node_at(r)) * H + h) * dv + rr];
+  }
+  constexpr int KV = DK * (int)sizeof(TIO) / 16;  // 16-byte vectors per key
+  for (int x = threadIdx.x; x < Lu * KV; x += kThreads) {
+    const int r = x / KV, c = x % KV;
+    reinterpret_cast<uint4*>(ksm + (size_t)r * DK)[c] =
+        __ldg(reinterpret_cast<const uint4*>(static_cast<const TIO*>(a.k) + (((size_t)b * N + node_at(r)) * H + h) * DK) + c);
+  }
+  const int st = check_prefetched_path(a, b, pc);  // barriers inside
+  if (layer == 0 && h == 0 && threadIdx.x == 0) a.err[b] = st;
+  // Every thread sees the tile through the barrier itself; a CTA that leaves early still waits
+  // for the copy (bounded) so that it does not outlive the CTA's shared memory.
+  const bool landed = mbar_wait(&bar, 0);
+  if (st || !landed) {
+    if (threadIdx.x == 0 && !st && !landed) a.err[b] = TV_ERR_TIMEOUT;
+    return;
+  }
+  const int L = pc.L;
+  if (threadIdx.x == 0) lga_s = coef[L - 1];
+  __syncthreads();
+  const float lga = lga_s;
+  const float gam = expf(lga);
+  const int lane8 = threadIdx.x % kLPR, rl = threadIdx.x / kLPR;
+  for (int p = 0; p < passes; ++p) {
+    TS* row = tile_s + (size_t)(p * kRows + rl) * DK + lane8 * 8;
+    float cur[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) load_vec_rw<8>(row + j * kStride, cur + 8 * j);
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) cur[e] *= gam;
+    for (int r = 0; r < L; ++r) {
+      const float c = expf(lga - coef[r]) * wsm[r * dv + p * kRows + rl];
+      const TIO* kr = ksm + (size_t)r * DK + lane8 * 8;
+#pragma unroll
+      for (int j = 0; j < CPL / 8; ++j) {
+        float kf[8];
+        if constexpr (sizeof(TIO) == 2) {
+          unpack8(*reinterpret_cast<const uint4*>(kr + j * kStride), kf);
+        } else {
+          const float4 x0 = *reinterpret_cast<const float4*>(kr + j * kStride);
+          const float4 x1 = *reinterpret_cast<const float4*>(kr + j * kStride + 4);
+          kf[0] = x0.x; kf[1] = x0.y; kf[2] = x0.z; kf[3] = x0.w;
+          kf[4] = x1.x; kf[5] = x1.y; kf[6] = x1.z; kf[7] = x1.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cur[8 * j + e] = fmaf(c, kf[e], cur[8 * j + e]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < CPL / 8; ++j) store_vec<8>(row + j * kStride, cur + 8 * j);
+  }
+  fence_async_shared();  // the bulk store reads the tile through the async proxy
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bulk_s2g(s0, tile_s, tile);
+    bulk_commit();
+    bulk_wait_read<0>();
+  }
+}
+
+// The same commit for paths too long to stage beside the tile: thread (row rl, lane) loads rows
+// rl, rl + 32, ... of the head into registers before the path check and stores them back.
+template <typename TIO, typename TS, int DK>
+__global__ void __launch_bounds__(kThreads, 4) commit_wy_regs_kernel(CommitArgs a0) {
+  constexpr int CPL = DK / kLPR;
+  __shared__ PathCheck pc;
+  __shared__ float coef[TV_MAX_NODES];
+  __shared__ float lga_s;
+  extern __shared__ __align__(128) unsigned char dyn[];  // w [cap][dv] fp32, then k [cap][DK]
   constexpr int P = 4;                 // passes of 32 rows: dv <= 128
   const int layer = blockIdx.x / (a0.B * a0.H), bh = blockIdx.x % (a0.B * a0.H);
   const CommitArgs a = layer_view(a0, layer);
@@ -334,10 +435,9 @@ cudaError_t launch_replay_t(const CommitArgs& a, const ReplayArgs& r, cudaStream
   const int cap = a.Lmax < a.N ? a.Lmax : a.N;
   const size_t smem = (size_t)cap * DK * sizeof(float);
   auto kern = commit_replay_kernel<TIO, TS, DK>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  // (static + dynamic shared memory may pass 48 KB with a dynamic part below it)
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   kern<<<a.B * a.H, kThreads, smem, s>>>(a, r);
   return cudaGetLastError();
 }
@@ -355,12 +455,19 @@ cudaError_t launch_fork_commit_t(const CommitArgs& a, cudaStream_t s) {
 template <typename TIO, typename TS, int DK>
 cudaError_t launch_wy_t(const CommitArgs& a, cudaStream_t s) {
   const int cap = a.Lmax < a.N ? a.Lmax : a.N;  // a valid path has distinct nodes
-  const size_t smem = (size_t)cap * (a.dv * sizeof(float) + DK * sizeof(TIO));
-  auto kern = commit_wy_kernel<TIO, TS, DK>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  const size_t rows = (size_t)cap * (a.dv * sizeof(float) + DK * sizeof(TIO));
+  const size_t tile = (size_t)a.dv * DK * sizeof(TS);
+  // The tile beside the path rows when both fit with the kernel's static shared memory, else
+  // the tile through registers.
+  cudaFuncAttributes fa;
+  cudaError_t e0 = cudaFuncGetAttributes(&fa, commit_wy_kernel<TIO, TS, DK>);
+  if (e0 != cudaSuccess) return e0;
+  const bool staged = fa.sharedSizeBytes + tile + rows <= (size_t)227 * 1024;
+  const size_t smem = staged ? tile + rows : rows;
+  auto kern = staged ? commit_wy_kernel<TIO, TS, DK> : commit_wy_regs_kernel<TIO, TS, DK>;
+  // (static + dynamic shared memory may pass 48 KB with a dynamic part below it)
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   kern<<<a.layers * a.B * a.H, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
