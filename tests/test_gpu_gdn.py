@@ -325,3 +325,36 @@ def test_wy_commit_with_a_wide_path_table_equals_the_staged_form():
     for b in range(B):
         ref = G.node_state(inp, b, int(case.path[b, int(case.path_len[b]) - 1]))[0]
         _gpu.assert_close(narrow[b], ref, "bf16", "wy commit, staged and register forms", stored="f32")
+
+
+def test_malformed_trees_in_a_wide_batch_fail_only_their_sequences():
+    """At the batch-64 layer the fork walks plan their units as groups of CTAs tiling every
+    sequence, so CTAs start and end inside sequences.  Two malformed trees -- one of them the
+    last sequence -- fail alone, in the one-pass call and in both passes of the two-pass call;
+    every other sequence equals a run without the faults bit for bit."""
+    case = W.stack_b64_layer()
+    clean = _gpu.run_fork(case, keep_device=True)
+    bad = W.stack_b64_layer()
+    for b in (17, 63):
+        bad.parents[b, 20] = 30         # a later node: not allowed
+    got = _gpu.run_fork(bad, keep_device=True)
+    want_err = [tv.TV_ERR_BAD_TREE if b in (17, 63) else 0 for b in range(64)]
+    assert got["err"].cpu().tolist() == want_err
+    keep = [b for b in range(64) if b not in (17, 63)]
+    assert torch.equal(got["out"][keep], clean["out"][keep])
+    assert torch.equal(got["states"][keep], clean["states"][keep])
+    x = _gpu.gdn_inputs(bad)
+    B, N, H, dk, dv = bad.shape
+    ws = torch.empty(tv.tv_gdn_fork_workspace_size(B, N, H, dv), dtype=torch.uint8, device="cuda")
+    out = torch.full((B, N, H, dv), float("nan"), dtype=torch.bfloat16, device="cuda")
+    states = torch.full((B, N, H, dv, dk), float("nan"), dtype=torch.bfloat16, device="cuda")
+    err = torch.full((B,), 12345, dtype=torch.int32, device="cuda")
+    tv.tv_gdn_tree_verify_fork_ws(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["S0"], x["parents"], out, states,
+                                  ws, err)
+    torch.cuda.synchronize()
+    assert err.cpu().tolist() == want_err
+    for b in (16, 18, 62):              # the neighbours of the malformed trees
+        _gpu.assert_close(states[b].cpu(), W.f64(clean["states"][b].cpu()), "bf16",
+                          "two-pass snapshots next to malformed trees", ref_rounded=True)
+        assert not torch.isnan(out[b].float()).any()
+    assert torch.isnan(states[17].float()).all() and torch.isnan(states[63].float()).all()
