@@ -220,8 +220,8 @@ struct Raw<float, CPL> {
 // RPL: state rows per lane group (1 or 2).  With two, a group of 8 lanes holds rows rg and
 // rg + 8 of the slab (64 threads per CTA): the k and q loads and conversions, the schedule
 // decode and the prefetch serve both rows, and the four row dot products of a node reduce
-// together in four shuffles (plus two to broadcast w), so a row costs about half the
-// instructions of the one-row form.
+// together in four shuffles (plus two to broadcast w), so a row costs about a third fewer
+// instructions than in the one-row form.
 struct UnitPlan {
   int group, share, stride;  // CTAs per group, units per CTA at most, units between group starts
 };
