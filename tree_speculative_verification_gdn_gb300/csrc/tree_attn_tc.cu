@@ -385,6 +385,512 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 5) tmem_dealloc(bar.tmem_base, L::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------------------------
+// CTA-pair form.  Two CTAs on two SMs take query-row tiles 2p (rank 0) and 2p + 1 (rank 1) of one
+// (sequence, KV head, key chunk) and run M = 256 MMAs over both, on key tiles of 128.  A key
+// tile's 128 keys split 64 per CTA and a value tile's head dim splits in halves, so each SM
+// loads half of every K/V tile and the pair reads the chunk once; the single-CTA form above
+// reads it once per row tile.  S = Q K^T runs with N = 128: an MMA of N = 64 costs about as
+// much as one of N = 128 here, since both read the same A slice.
+//   rank 0, warp 5   MMA issuer for the pair: S = Q K^T (M=256, N=128) and O += P V (M=256, N=hd);
+//                    each commit arrives on the barrier in both CTAs;
+//   rank 1, warp 5   relay: tells rank 0 when this CTA's K and V tiles have landed, zeroing
+//                    value rows past the sequence end first;
+//   warps 4 and 6    TMA producers of the CTA's own key and value halves, apart, so a value
+//                    load never waits behind a key stage;
+//   warps 0-3        each thread writes its query row into the 128-byte-swizzled Q tile, then
+//                    runs the softmax of that row: the tile's max over both 64-key halves
+//                    first, then P half by half; rank 1 arrives on rank 0's barriers.
+// Every wait is bounded; a CTA that gives up raises the abort flag in both CTAs, and both still
+// reach the closing cluster barrier and free the pair's tensor memory together.
+constexpr int PKT = 128;  // keys per tile
+constexpr int kPairThreads = 224;
+
+template <int HD>
+struct PairLayout {
+  static constexpr int KS = HD == 256 ? 2 : 4;         // half key tiles in the ring
+  static constexpr int VS = HD == 256 ? 3 : 6;         // half value tiles in the ring
+  static constexpr uint32_t QCHUNK = kRows * 128;      // one 64-column chunk of Q
+  static constexpr uint32_t KH_CHUNK = PKT / 2 * 128;  // 64 keys of one 64-column chunk
+  static constexpr uint32_t KHB = HD / 64 * KH_CHUNK;  // this CTA's half of a key tile
+  static constexpr uint32_t VCHUNK = PKT * 128;        // 128 keys of one 64-column chunk
+  static constexpr uint32_t VHB = HD / 128 * VCHUNK;   // this CTA's half of a value tile
+  static constexpr uint32_t Q = 0;
+  static constexpr uint32_t K0 = Q + HD / 64 * QCHUNK;
+  static constexpr uint32_t V0 = K0 + KS * KHB;
+  static constexpr uint32_t BARS = V0 + VS * VHB;
+  static constexpr uint32_t TOTAL = BARS + 512;
+  // O [0, HD), two S buffers [HD, HD + 2 PKT) (P over the first PKT / 2 columns of each)
+  static constexpr uint32_t TMEM_COLS = (HD + 2 * PKT <= 256) ? 256 : 512;
+};
+
+struct PairBars {
+  uint64_t q_ready;
+  uint64_t k_land[4], k_peer[4], k_empty[4];
+  uint64_t v_land[6], v_peer[6], v_empty[6];
+  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  uint32_t go;
+};
+static_assert(sizeof(PairBars) <= 512, "pair barriers fit their reserved region");
+
+// Bounded wait with cluster-scope acquire: the thread sleeps in the barrier unit until the phase
+// completes or about a microsecond passes.
+__device__ __forceinline__ bool mbar_try_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(1000u)
+      : "memory");
+  return done != 0;
+}
+
+template <int HD>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    attn_partial_pair_kernel(AttnArgs a, const __nv_bfloat16* __restrict__ qrot, float* __restrict__ ml,
+                             float* __restrict__ acc, int chunk, int nsplit, int npairs, int npt,
+                             const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV) {
+  using L = PairLayout<HD>;
+  constexpr int KS = L::KS, VS = L::VS;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* sm = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  PairBars& bar = *reinterpret_cast<PairBars*>(sm + L::BARS);
+  volatile int* abort = &bar.abort;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+
+  const int b = blockIdx.y;
+  int x = blockIdx.x >> 1;
+  const int pair = x % npairs;
+  x /= npairs;
+  const int split = x % nsplit;
+  const int kvh = x / nsplit;
+  const int mt = 2 * pair + (int)rank;
+  const int N = a.N, P = a.prefix_len[b], total = P + N;
+  const int lo = split * chunk;
+  if (lo >= total) return;  // the same for both CTAs of the pair
+  const int hi = min(total, lo + chunk);
+  const int T = (hi - lo + PKT - 1) / PKT;
+  const int G = a.Hq / a.Hkv, R = G * N;
+  auto warps_of = [&](int t) { return (G * max(0, min(npt, N - t * npt)) + 31) / 32; };
+  const int active_warps = warps_of(mt);
+
+  if (tid == 0) {
+    const uint32_t pair_warps = (uint32_t)(warps_of(2 * pair) + warps_of(2 * pair + 1));
+    mbar_init(&bar.q_ready, pair_warps);  // one arrival per softmax warp with query rows
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&bar.k_land[s], 1);
+      mbar_init(&bar.k_peer[s], 1);
+      mbar_init(&bar.k_empty[s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(&bar.v_land[s], 1);
+      mbar_init(&bar.v_peer[s], 1);
+      mbar_init(&bar.v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar.s_full[s], 1);
+      mbar_init(&bar.p_full[s], pair_warps);
+      mbar_init(&bar.pv_done[s], 1);
+    }
+    mbar_init(&bar.drain, 1);
+    bar.abort = 0;
+    bar.go = a.err[b] == 0 ? 1u : 0u;
+    mbar_fence_init();
+  }
+  // Both CTAs' barriers exist before either signals the other.  Rank 0's reading of the status
+  // word decides for the pair, so both take the same branch even if another CTA writes it.
+  cluster_sync();
+  if (!cluster_ld_u32(cluster_map(smem_addr(&bar.go), 0))) {
+    cluster_sync();  // rank 0 stays until rank 1 has read its flag
+    return;
+  }
+  if (warp == 5) tmem_alloc_pair(&bar.tmem_base, L::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tO = bar.tmem_base;        // output accumulator
+  const uint32_t tS = bar.tmem_base + HD;   // two S buffers
+  const uint32_t peer_abort = cluster_map(smem_addr((const void*)&bar.abort), peer);
+  auto fail = [&]() {
+    *abort = 1;
+    cluster_st_u32(peer_abort, 1u);
+  };
+  auto pwait = [&](uint64_t* w, uint32_t parity) -> bool {
+    for (uint32_t it = 0; it < (1u << 20); ++it) {
+      if (mbar_try_cluster(w, parity)) return true;
+      if (*abort) return false;
+    }
+    fail();
+    return false;
+  };
+  auto to_rank0 = [&](uint64_t* w) { return cluster_map(smem_addr(w), 0); };
+  int issued_k = 0, issued_v = 0;
+
+  if (warp == 4 || warp == 6) {
+    // ------------------------------------------------------------ TMA producers (whole warps)
+    // Warp 4 loads this CTA's keys, pages 4 rank .. 4 rank + 3 of a tile (lanes 0-3); warp 6
+    // loads its values, the head-dim half `rank` of all eight pages (lanes 0-7).
+    const int last_lb = (total - 1) / 16;
+    const int* table = a.block_table + (size_t)b * a.max_blocks;
+    auto wait_all = [&](uint64_t* w, uint32_t parity) { return __all_sync(0xffffffffu, pwait(w, parity)); };
+    if (warp == 4) {
+      auto kpage = [&](int j) {
+        return (lane < 4 && j < T) ? table[min((lo + j * PKT) / 16 + 4 * (int)rank + lane, last_lb)] : 0;
+      };
+      int blk = kpage(0);
+      for (int j = 0; j < T; ++j) {
+        const int st = j % KS;
+        if (j >= KS && !wait_all(&bar.k_empty[st], ((j - KS) / KS) & 1)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bar.k_land[st], L::KHB);
+        __syncwarp();
+        if (lane < 4)
+          for (int c = 0; c < HD / 64; ++c)
+            tma_load_4d(sm + L::K0 + st * L::KHB + c * L::KH_CHUNK + lane * 2048, &mK, c * 64, 0, kvh, blk,
+                        &bar.k_land[st]);
+        issued_k = j + 1;
+        blk = kpage(j + 1);
+      }
+    } else {
+      auto vpage = [&](int j) { return (lane < 8 && j < T) ? table[min((lo + j * PKT) / 16 + lane, last_lb)] : 0; };
+      int blk = vpage(0);
+      for (int j = 0; j < T; ++j) {
+        const int st = j % VS;
+        if (j >= VS && !wait_all(&bar.v_empty[st], ((j - VS) / VS) & 1)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bar.v_land[st], L::VHB);
+        __syncwarp();
+        if (lane < 8)
+          for (int cc = 0; cc < HD / 128; ++cc)
+            tma_load_4d(sm + L::V0 + st * L::VHB + cc * L::VCHUNK + lane * 2048, &mV,
+                        ((int)rank * (HD / 128) + cc) * 64, 0, kvh, blk, &bar.v_land[st]);
+        issued_v = j + 1;
+        blk = vpage(j + 1);
+      }
+    }
+  } else if (warp == 5 && rank == 0) {
+    // ------------------------------------------------------------ MMA issuer for the pair
+    // Event-driven: S of the next tile once both halves of its keys have landed and its S buffer
+    // is free (the PV that reads the buffer's P has been issued, and MMAs run in issue order);
+    // PV of the oldest tile once its P (both CTAs) and both halves of its values are ready.
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16_f32(256, PKT), idO = idesc_bf16_f32(256, HD, true);
+      const uint32_t q0 = smem_addr(sm + L::Q);
+      bool ok = pwait(&bar.q_ready, 0);
+      int ns = 0, np = 0;
+      uint32_t idle = 0;
+      while (ok && np < T) {
+        bool progressed = false;
+        const int ks = ns % KS, kph = (ns / KS) & 1;
+        if (ns < T && ns < np + 2 && mbar_test(&bar.k_land[ks], kph) && mbar_test_cluster(&bar.k_peer[ks], kph)) {
+          tc_fence_after();
+          const int st = ns & 1;
+          const uint32_t k0 = smem_addr(sm + L::K0 + ks * L::KHB);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            mma_bf16_pair(tS + st * PKT, sw128_desc(q0 + (kk / 4) * L::QCHUNK + (kk % 4) * 32),
+                          sw128_desc(k0 + (kk / 4) * L::KH_CHUNK + (kk % 4) * 32), idS, kk ? 1u : 0u);
+          mma_commit_pair(&bar.s_full[st], 3);
+          mma_commit_pair(&bar.k_empty[ks], 3);
+          ++ns;
+          progressed = true;
+        }
+        const int vs = np % VS, vph = (np / VS) & 1;
+        if (np < ns && mbar_test_cluster(&bar.p_full[np & 1], (np >> 1) & 1) && mbar_test(&bar.v_land[vs], vph) &&
+            mbar_test_cluster(&bar.v_peer[vs], vph)) {
+          tc_fence_after();
+          const int ps = np & 1;
+          const uint32_t v0 = smem_addr(sm + L::V0 + vs * L::VHB);
+#pragma unroll
+          for (int kk = 0; kk < PKT / 16; ++kk)
+            mma_bf16_tmem_a_pair(tO, tS + ps * PKT + kk * 8, sw128_mn_desc(v0 + kk * 2048, L::VCHUNK), idO,
+                                 (np > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_pair(&bar.pv_done[ps], 3);
+          mma_commit_pair(&bar.v_empty[vs], 3);
+          ++np;
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else if (++idle > (1u << 20)) {
+          fail();
+          ok = false;
+        } else {
+          // sleep in the barrier unit on what the oldest tile still lacks, else on the keys of
+          // the next one
+          if (np < ns && !mbar_test_cluster(&bar.p_full[np & 1], (np >> 1) & 1))
+            mbar_try_cluster(&bar.p_full[np & 1], (np >> 1) & 1);
+          else if (np < ns && !mbar_test(&bar.v_land[vs], vph))
+            mbar_try_cluster(&bar.v_land[vs], vph);
+          else if (np < ns)
+            mbar_try_cluster(&bar.v_peer[vs], vph);
+          else
+            mbar_try_cluster(&bar.k_land[ks], kph);
+          if (*abort) ok = false;
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ relay (rank 1, whole warp)
+    bool ok = true;
+    int nk = 0, nv = 0;
+    uint32_t idle = 0;
+    while (ok && (nk < T || nv < T)) {
+      bool progressed = false;
+      if (nk < T && __shfl_sync(0xffffffffu, lane == 0 && mbar_test(&bar.k_land[nk % KS], (nk / KS) & 1), 0)) {
+        if (lane == 0) mbar_arrive_cluster_relaxed(to_rank0(&bar.k_peer[nk % KS]));
+        ++nk;
+        progressed = true;
+      }
+      if (nv < T && __shfl_sync(0xffffffffu, lane == 0 && mbar_test(&bar.v_land[nv % VS], (nv / VS) & 1), 0)) {
+        const int base = lo + nv * PKT;
+        if (base + PKT > hi) {  // value rows past the chunk end: their P is 0 but contents are unknown
+          const int first = hi - base;
+          unsigned char* v0 = sm + L::V0 + (nv % VS) * L::VHB;
+          for (int idx = lane; idx < (PKT - first) * (HD / 16); idx += 32) {
+            const int kr = first + idx / (HD / 16), rem = idx % (HD / 16);
+            *reinterpret_cast<uint4*>(v0 + (rem / 8) * L::VCHUNK + kr * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive_cluster_relaxed(to_rank0(&bar.v_peer[nv % VS]));
+        ++nv;
+        progressed = true;
+      }
+      if (progressed) {
+        idle = 0;
+      } else if (++idle > (1u << 20)) {
+        if (lane == 0) fail();
+        ok = false;
+      } else {
+        if (lane == 0) {
+          if (nk < T)
+            mbar_try_cluster(&bar.k_land[nk % KS], (nk / KS) & 1);
+          else
+            mbar_try_cluster(&bar.v_land[nv % VS], (nv / VS) & 1);
+        }
+        ok = __shfl_sync(0xffffffffu, *abort == 0, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax, one row per thread
+    const int r = tid;
+    const int node = mt * npt + r / G, g = r % G;
+    const bool active = (r < G * npt) && node < N;
+    const bool warp_idle = warp >= active_warps;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    bool ok = true;
+    if (!warp_idle) {
+      // this row's rotated query (zeros for padding rows) into the Q tile that the MMA reads
+      const uint4* qrow =
+          reinterpret_cast<const uint4*>(qrot + (((size_t)b * N + (active ? node : 0)) * a.Hq + kvh * G + g) * HD);
+#pragma unroll 1
+      for (int c = 0; c < HD / 64; ++c) {
+        unsigned char* row = sm + L::Q + c * L::QCHUNK + (r / 8) * 1024 + (r % 8) * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(row + ((u ^ (r % 8)) << 4)) = active ? qrow[c * 8 + u] : make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&bar.q_ready);
+        else
+          mbar_arrive_cluster(to_rank0(&bar.q_ready));
+      }
+    }
+    uint32_t mb[TV_MAX_NODES / 32];
+#pragma unroll
+    for (int w = 0; w < TV_MAX_NODES / 32; ++w) mb[w] = 0;
+    if (active) {
+      const int32_t* par = a.parents + (size_t)b * N;
+      for (int j = node; j >= 0; j = par[j]) {
+#pragma unroll
+        for (int w = 0; w < TV_MAX_NODES / 32; ++w)
+          if ((j >> 5) == w) mb[w] |= 1u << (j & 31);
+      }
+    }
+    const float scale = a.sm_scale * kLog2e;
+    // Visible keys of the 64-key half starting at slot `base` for this row: the prefix part and,
+    // on node slots, the row node's ancestors and itself.
+    auto visible = [&](int base) -> uint64_t {
+      if (!active) return 0;
+      const int nprefix = min(max(min(hi, P) - base, 0), 64);
+      uint64_t vis = nprefix >= 64 ? ~0ull : ((1ull << nprefix) - 1ull);
+      const int node_end = min(hi - base, 64);
+      for (int c = max(nprefix, 0); c < node_end; ++c) {
+        const int n = base + c - P;
+        uint32_t word = 0;
+#pragma unroll
+        for (int w = 0; w < TV_MAX_NODES / 32; ++w) word = ((n >> 5) == w) ? mb[w] : word;
+        vis |= (uint64_t)((word >> (n & 31)) & 1u) << c;
+      }
+      return vis;
+    };
+    float m_used = -INFINITY, l = 0.f;
+    for (int j = 0; j < T && !warp_idle; ++j) {
+      const int st = j & 1;
+      if (!__all_sync(0xffffffffu, pwait(&bar.s_full[st], (j >> 1) & 1))) { ok = false; break; }
+      tc_fence_after();
+      const int base = lo + j * PKT;
+      const uint32_t sbuf = tS + lane_base + st * PKT;
+      // the whole tile's S in registers, one load
+      float s[PKT];
+      {
+        uint32_t rawv[PKT];
+#pragma unroll
+        for (int q4 = 0; q4 < PKT / 16; ++q4) tmem_ld16_nowait(sbuf + q4 * 16, rawv + q4 * 16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < PKT; ++c) s[c] = __uint_as_float(rawv[c]) * scale;  // log2 units
+      }
+      // tiles wholly inside the prefix need no mask; others set invisible keys to -inf
+      if (!__all_sync(0xffffffffu, active && base + PKT <= min(hi, P))) {
+        const uint64_t vis0 = visible(base), vis1 = visible(base + 64);
+#pragma unroll
+        for (int c = 0; c < PKT; ++c)
+          if (!((((c < 64) ? vis0 : vis1) >> (c & 63)) & 1ull)) s[c] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < PKT; ++c) mx = fmaxf(mx, s[c]);
+      const bool raise = mx > m_used + kRescale;
+      const bool rescale_o = raise && m_used != -INFINITY;
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        if (!__all_sync(0xffffffffu, pwait(&bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float f = rescale_o ? ex2_approx(m_used - mx) : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < HD; c0 += 16) {
+          float o16[16];
+          tmem_ld16(tO + lane_base + c0, o16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o16[e] *= f;
+          tmem_st16(tO + lane_base + c0, o16);
+        }
+      }
+      if (raise) {
+        l = rescale_o ? l * ex2_approx(m_used - mx) : 0.f;
+        m_used = mx;
+      }
+      // P in bf16 pairs over the first PKT / 2 columns of the S buffer (already read); a row
+      // with nothing visible yet keeps m_used = -inf and gives 0, masked keys give 2^-inf = 0
+      const float mneg = m_used == -INFINITY ? 0.f : -m_used;
+      const bool none = m_used == -INFINITY;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+        float psum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = none ? 0.f : ex2_approx(s[64 * h + 2 * e] + mneg);
+          const float p1 = none ? 0.f : ex2_approx(s[64 * h + 2 * e + 1] + mneg);
+          pk[e] = pack_bf16x2(p0, p1);
+          psum += bf16lo(pk[e]) + bf16hi(pk[e]);
+        }
+        tmem_st32(sbuf + h * 32, pk);
+        l += psum;
+      }
+      if (rank == 0 && base + PKT > hi) {  // rank 0's value rows past the chunk end (rank 1's relay zeroes its own)
+        if (!__all_sync(0xffffffffu, pwait(&bar.v_land[j % VS], (j / VS) & 1))) {
+          ok = false;
+          break;
+        }
+        const int first = hi - base;
+        unsigned char* v0 = sm + L::V0 + (j % VS) * L::VHB;
+        for (int idx = r; idx < (PKT - first) * (HD / 16); idx += 32 * active_warps) {
+          const int kr = first + idx / (HD / 16), rem = idx % (HD / 16);
+          *reinterpret_cast<uint4*>(v0 + (rem / 8) * L::VCHUNK + kr * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&bar.p_full[st]);
+        else
+          mbar_arrive_cluster_relaxed(to_rank0(&bar.p_full[st]));
+      }
+    }
+    if (ok && !warp_idle && __all_sync(0xffffffffu, pwait(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1))) {
+      tc_fence_after();
+      const size_t row = (((size_t)b * a.Hkv + kvh) * nsplit + split) * R + (size_t)node * G + g;
+#pragma unroll 1
+      for (int c0 = 0; c0 < HD; c0 += 16) {
+        float o16[16];
+        tmem_ld16(tO + lane_base + c0, o16);
+        if (active) {
+          float4* dst = reinterpret_cast<float4*>(acc + row * HD + c0);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_float4(o16[4 * e], o16[4 * e + 1], o16[4 * e + 2], o16[4 * e + 3]);
+        }
+      }
+      if (active) {
+        ml[row * 2] = m_used;
+        ml[row * 2 + 1] = l;
+      }
+    }
+  }
+  __syncthreads();
+  // Close: rank 0's last commit reaches both CTAs once every pair MMA has completed; each CTA
+  // then lets its own loads land, and neither leaves or frees tensor memory before the other.
+  if (warp == 5 && lane == 0) {
+    if (rank == 0) mma_commit_pair(&bar.drain, 3);
+    if (!mbar_wait(&bar.drain, 0)) *abort = 1;
+  }
+  __syncthreads();
+  if (*abort) {
+    if (warp == 4 && lane == 0)
+      for (int j = issued_k - KS < 0 ? 0 : issued_k - KS; j < issued_k; ++j)
+        mbar_wait(&bar.k_land[j % KS], (j / KS) & 1);
+    if (warp == 6 && lane == 0)
+      for (int j = issued_v - VS < 0 ? 0 : issued_v - VS; j < issued_v; ++j)
+        mbar_wait(&bar.v_land[j % VS], (j / VS) & 1);
+    if (tid == 0) a.err[b] = TV_ERR_TIMEOUT;
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc_pair(bar.tmem_base, L::TMEM_COLS);
+}
+
+template <int HD>
+cudaError_t launch_pair_t(const AttnArgs& a, const void* qrot, float* ml, float* acc, int chunk, int nsplit,
+                          cudaStream_t s) {
+  using L = PairLayout<HD>;
+  const int G = a.Hq / a.Hkv;
+  const int npt = kRows / G;
+  const int mtiles = (a.N + npt - 1) / npt;
+  const int npairs = (mtiles + 1) / 2;
+  CUtensorMap mK, mV;
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)HD, 16, (cuuint64_t)a.Hkv, (cuuint64_t)a.num_blocks};
+    const cuuint64_t strides[3] = {(cuuint64_t)HD * 2, (cuuint64_t)16 * HD * 2, (cuuint64_t)a.Hkv * 16 * HD * 2};
+    const cuuint32_t box[4] = {64, 16, 1, 1};
+    if (!make_map_bf16_sw128(&mK, a.k_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16_sw128(&mV, a.v_cache, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  const size_t smem = L::TOTAL + 1024;
+  auto kern = attn_partial_pair_kernel<HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(nsplit * npairs * 2 * a.Hkv, a.B);
+  kern<<<grid, kPairThreads, smem, s>>>(a, static_cast<const __nv_bfloat16*>(qrot), ml, acc, chunk, nsplit, npairs,
+                                        npt, mK, mV);
+  return cudaGetLastError();
+}
+
 template <int HD>
 cudaError_t launch_t(const AttnArgs& a, const void* qrot, float* ml, float* acc, int chunk, int nsplit,
                      cudaStream_t s) {
@@ -427,9 +933,9 @@ bool attn_tc_supported(const AttnArgs& a) {
 
 cudaError_t launch_attn_partial_tc(const AttnArgs& a, const void* qrot, float* ml, float* acc, int chunk,
                                    int nsplit, cudaStream_t s) {
-  if (chunk % KT) return cudaErrorInvalidValue;
-  return a.hd == 128 ? launch_t<128>(a, qrot, ml, acc, chunk, nsplit, s)
-                     : launch_t<256>(a, qrot, ml, acc, chunk, nsplit, s);
+  if (chunk % PKT) return cudaErrorInvalidValue;
+  return a.hd == 128 ? launch_pair_t<128>(a, qrot, ml, acc, chunk, nsplit, s)
+                     : launch_pair_t<256>(a, qrot, ml, acc, chunk, nsplit, s);
 }
 
 }  // namespace tv
