@@ -35,17 +35,28 @@ AttnPlan plan_attn(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int bs
   AttnPlan p;
   const long long slots = (long long)max_blocks * bs;
   const long long work = (long long)B * Hkv * slots;
-  // About 1536 partial CTAs -- (sequence, KV head, chunk) items times the tiles of 128 query
-  // rows each item has, ten per SM of a 152-SM GPU: longer chunks mean fewer CTA set-ups and
-  // partial rows to combine, shorter ones a smaller tail.  With two row tiles (the 40-node trees
-  // of a 4-head group) that is ~768 items, the best of a sweep over 512 .. 2048; wider trees
-  // take longer chunks rather than more CTAs.  The count depends on the sizes alone, and so does
-  // the workspace size.
+  // Whole sequences as items when they alone give at least four waves of partial CTAs on a
+  // 152-SM GPU (then only sequences past 16384 keys split); otherwise about 152 CTAs -- items
+  // times the tiles of 128 query rows each item has, rounded up to CTA pairs, one per SM -- but
+  // no chunk longer than 6912 keys, so that sequences of unequal length still spread evenly.
+  // A partial CTA's set-up and pipeline fill cost about as much as several key tiles, so long
+  // chunks pay until the longest ones make the tail; a sweep over 1536 .. 152 CTAs and caps of
+  // 6912 .. 32768 keys picked these.  The chunk count comes first and the capacity is then
+  // split evenly, so no chunk is a short remainder.  The plan depends on the sizes alone, and
+  // so does the workspace size.
   const long long mtiles = ((long long)(Hq / Hkv) * N + 127) / 128;
-  long long chunk = (work * mtiles + 1535) / 1536;
-  chunk = (chunk + 127) / 128 * 128;
+  const long long whole_ctas = (long long)B * Hkv * 2 * ((mtiles + 1) / 2);
+  long long chunk;
+  if (whole_ctas >= 4 * 152) {
+    chunk = 16384;
+  } else {
+    chunk = (work * mtiles + 151) / 152;
+    if (chunk > 6912) chunk = 6912;
+  }
   if (chunk < 128) chunk = 128;
-  if (chunk > 8192) chunk = 8192;
+  const long long nsplit = (slots + chunk - 1) / chunk;
+  chunk = (slots + nsplit - 1) / nsplit;
+  chunk = (chunk + 127) / 128 * 128;
   p.chunk = (int)chunk;
   p.nsplit = (int)((slots + chunk - 1) / chunk);
   p.R = (Hq / Hkv) * N;
