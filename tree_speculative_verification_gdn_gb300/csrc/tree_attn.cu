@@ -68,10 +68,26 @@ AttnPlan plan_attn(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int bs
   return p;
 }
 
-__global__ void attn_check_kernel(AttnArgs a) {
+// Inverse frequencies theta^(-2c/hd), c < hd/2, computed once per call in fp64 on the host and
+// passed as fp32 (hi, lo) pairs: hi + lo carries about 48 bits.
+struct RopeTable {
+  float2 inv[128];
+};
+
+// One CTA per (sequence, node).  Every CTA first checks its sequence -- the tree, the cache
+// capacity for prefix + N slots, and the block ids those slots use -- so that nothing is written
+// for a sequence that fails; the CTA of node 0 records the status.  The angle pos * inv is formed as a double-float product
+// (the FMA gives the rounding error of pos * hi exactly) and reduced modulo 2 pi with the
+// three-part Cody-Waite split 2 pi = C1 + C2 + C3, C1 = 25/4 having 5 significant bits so that
+// k * C1 is exact for every k < 2^19 (positions below 2^21); the reduced angle is then within a
+// few ulp before the fp32 sincos.
+__global__ void attn_rope_kernel(AttnArgs a, bf16* __restrict__ qrot, const __grid_constant__ RopeTable tab) {
+  constexpr float C1 = 6.25f, C2 = 3.318530693650246e-2f, C3 = 2.430837753308879e-10f;
+  constexpr float kInv2Pi = 0.15915494309189535f;
+  __shared__ float2 cs[128];  // (cos, sin) of each pair index c
   __shared__ int par[TV_MAX_NODES];
   __shared__ int flag, bad_block;
-  const int b = blockIdx.x;
+  const int b = blockIdx.x / a.N, i = blockIdx.x % a.N;
   int st = load_and_check_tree(a.parents + (size_t)b * a.N, a.N, par, &flag);
   if (!st) {
     const int P = a.prefix_len[b];
@@ -88,29 +104,9 @@ __global__ void attn_check_kernel(AttnArgs a) {
     __syncthreads();
     if (bad_block) st = TV_ERR_BAD_BLOCK;
   }
-  if (threadIdx.x == 0) a.err[b] = st;
-}
-
-// Inverse frequencies theta^(-2c/hd), c < hd/2, computed once per call in fp64 on the host and
-// passed as fp32 (hi, lo) pairs: hi + lo carries about 48 bits.
-struct RopeTable {
-  float2 inv[128];
-};
-
-// One CTA per (sequence, node).  The angle pos * inv is formed as a double-float product (the
-// FMA gives the rounding error of pos * hi exactly) and reduced modulo 2 pi with the three-part
-// Cody-Waite split 2 pi = C1 + C2 + C3, C1 = 25/4 having 5 significant bits so that k * C1 is
-// exact for every k < 2^19 (positions below 2^21); the reduced angle is then within a few ulp
-// before the fp32 sincos.
-__global__ void attn_rope_kernel(AttnArgs a, bf16* __restrict__ qrot, const __grid_constant__ RopeTable tab) {
-  constexpr float C1 = 6.25f, C2 = 3.318530693650246e-2f, C3 = 2.430837753308879e-10f;
-  constexpr float kInv2Pi = 0.15915494309189535f;
-  __shared__ float2 cs[128];  // (cos, sin) of each pair index c
-  const int b = blockIdx.x / a.N, i = blockIdx.x % a.N;
-  if (a.err[b]) return;
-  const int32_t* par = a.parents + (size_t)b * a.N;
-  int depth = 0;
-  for (int j = par[i]; j >= 0; j = par[j]) ++depth;
+  if (i == 0 && threadIdx.x == 0) a.err[b] = st;
+  if (st) return;
+  const int depth = node_depth(par, i);
   const int P = a.prefix_len[b];
   const float pos = (float)(P + depth);  // exact: positions stay below 2^24
   const int hd = a.hd, half = hd / 2, bs = a.block_size;
@@ -282,62 +278,88 @@ __global__ void __launch_bounds__(kPartialThreads) attn_partial_simt_kernel(Attn
   }
 }
 
-// One CTA per (sequence, node).  Thread h < Hq first forms query head h's running max M and
-// normaliser l over the key chunks; then the CTA merges the chunks' unnormalised outputs four
-// head dims (16 bytes) per thread at a time: o = sum_s 2^(m_s - M) acc_s / l.
+// A thread merges four head dims (16 bytes) of one (sequence, node, query head) at a time:
+// o = sum_s 2^(m_s - M) acc_s / l,
+// l = sum_s 2^(m_s - M) l_s, M = max_s m_s.  The chunks' (m_s, l_s) and outputs are all loaded
+// before any is used -- up to kBatch chunks in one round trip of loads -- and the arithmetic
+// then runs chunk by chunk in order.  With `per_node`, CTA x takes the units of (sequence, node)
+// x (used when those CTAs fill the GPU); otherwise one wave of CTAs takes all units grid-stride.
 constexpr int kCombineThreads = 256;
+constexpr int kBatch = 8;
 
 __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(AttnArgs a, const float* __restrict__ ml,
                                                                        const float* __restrict__ acc, int chunk,
-                                                                       int nsplit) {
-  extern __shared__ float head_ml[];  // [Hq] max, then [Hq] normaliser
-  const int i = blockIdx.x % a.N;
-  const int b = blockIdx.x / a.N;
-  if (a.err[b]) return;
-  const int Hq = a.Hq, hd = a.hd;
+                                                                       int nsplit, int per_node) {
+  const int Hq = a.Hq, hd = a.hd, v4 = hd / 4;
   const int G = Hq / a.Hkv, R = G * a.N;
-  const int total = a.prefix_len[b] + a.N;
-  const int nsp = (total + chunk - 1) / chunk;
-  auto row_of = [&](int h, int s) {  // partial row of (sequence b, node i, query head h) in chunk s
-    return (((size_t)b * a.Hkv + h / G) * nsplit + s) * R + (size_t)i * G + h % G;
-  };
-  for (int h = threadIdx.x; h < Hq; h += blockDim.x) {
-    float M = -INFINITY;
-    for (int s = 0; s < nsp; ++s) M = fmaxf(M, ml[row_of(h, s) * 2]);
-    float lsum = 0.f;
-    for (int s = 0; s < nsp; ++s) {
-      const size_t row = row_of(h, s);
-      const float ms = ml[row * 2];
-      if (ms == -INFINITY) continue;
-      lsum = fmaf(ml[row * 2 + 1], exp2f(ms - M), lsum);
+  const long long node_units = (long long)Hq * v4;
+  const long long units = per_node ? node_units * (blockIdx.x + 1) : (long long)a.B * a.N * node_units;
+  const long long first = per_node ? node_units * blockIdx.x + threadIdx.x : (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long step = per_node ? blockDim.x : (long long)gridDim.x * blockDim.x;
+  for (long long u = first; u < units; u += step) {
+    const int c = (int)(u % v4) * 4;
+    const long long bih = u / v4;  // (sequence, node, query head)
+    const int h = (int)(bih % Hq), i = (int)(bih / Hq % a.N), b = (int)(bih / Hq / a.N);
+    if (a.err[b]) continue;
+    const int total = a.prefix_len[b] + a.N;
+    const int nsp = (total + chunk - 1) / chunk;
+    bf16* out = static_cast<bf16*>(a.out) + ((size_t)b * a.N + i) * Hq * hd;
+    // partial row of (sequence b, node i, query head h) in chunk 0; chunk s is s * R rows on
+    const size_t row0 = (((size_t)b * a.Hkv + h / G) * nsplit) * R + (size_t)i * G + h % G;
+    if (nsp <= kBatch) {
+      float2 m_l[kBatch];
+      float4 p[kBatch];
+#pragma unroll
+      for (int s = 0; s < kBatch; ++s)
+        if (s < nsp) {
+          const size_t row = row0 + (size_t)s * R;
+          m_l[s] = *reinterpret_cast<const float2*>(ml + row * 2);
+          p[s] = *reinterpret_cast<const float4*>(acc + row * hd + c);
+        }
+      float M = -INFINITY;
+#pragma unroll
+      for (int s = 0; s < kBatch; ++s)
+        if (s < nsp) M = fmaxf(M, m_l[s].x);
+      float lsum = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < kBatch; ++s)
+        if (s < nsp && m_l[s].x != -INFINITY) {
+          const float wgt = exp2f(m_l[s].x - M);
+          lsum = fmaf(m_l[s].y, wgt, lsum);
+          o.x = fmaf(p[s].x, wgt, o.x);
+          o.y = fmaf(p[s].y, wgt, o.y);
+          o.z = fmaf(p[s].z, wgt, o.z);
+          o.w = fmaf(p[s].w, wgt, o.w);
+        }
+      bf16* dst = out + (size_t)h * hd + c;
+      dst[0] = from_f32<bf16>(o.x / lsum);
+      dst[1] = from_f32<bf16>(o.y / lsum);
+      dst[2] = from_f32<bf16>(o.z / lsum);
+      dst[3] = from_f32<bf16>(o.w / lsum);
+    } else {
+      float M = -INFINITY;
+      for (int s = 0; s < nsp; ++s) M = fmaxf(M, ml[(row0 + (size_t)s * R) * 2]);
+      float lsum = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < nsp; ++s) {
+        const size_t row = row0 + (size_t)s * R;
+        const float ms = ml[row * 2];
+        if (ms == -INFINITY) continue;
+        const float wgt = exp2f(ms - M);
+        lsum = fmaf(ml[row * 2 + 1], wgt, lsum);
+        const float4 pp = *reinterpret_cast<const float4*>(acc + row * hd + c);
+        o.x = fmaf(pp.x, wgt, o.x);
+        o.y = fmaf(pp.y, wgt, o.y);
+        o.z = fmaf(pp.z, wgt, o.z);
+        o.w = fmaf(pp.w, wgt, o.w);
+      }
+      bf16* dst = out + (size_t)h * hd + c;
+      dst[0] = from_f32<bf16>(o.x / lsum);
+      dst[1] = from_f32<bf16>(o.y / lsum);
+      dst[2] = from_f32<bf16>(o.z / lsum);
+      dst[3] = from_f32<bf16>(o.w / lsum);
     }
-    head_ml[h] = M;
-    head_ml[Hq + h] = lsum;
-  }
-  __syncthreads();
-  const int v4 = hd / 4;
-  bf16* out = static_cast<bf16*>(a.out) + ((size_t)b * a.N + i) * Hq * hd;
-  for (int x = threadIdx.x; x < Hq * v4; x += blockDim.x) {
-    const int h = x / v4, c = (x % v4) * 4;
-    const float M = head_ml[h];
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < nsp; ++s) {
-      const size_t row = row_of(h, s);
-      const float ms = ml[row * 2];
-      if (ms == -INFINITY) continue;
-      const float wgt = exp2f(ms - M);
-      const float4 p = *reinterpret_cast<const float4*>(acc + row * hd + c);
-      o.x = fmaf(p.x, wgt, o.x);
-      o.y = fmaf(p.y, wgt, o.y);
-      o.z = fmaf(p.z, wgt, o.z);
-      o.w = fmaf(p.w, wgt, o.w);
-    }
-    const float lsum = head_ml[Hq + h];
-    bf16* dst = out + (size_t)h * hd + c;
-    dst[0] = from_f32<bf16>(o.x / lsum);
-    dst[1] = from_f32<bf16>(o.y / lsum);
-    dst[2] = from_f32<bf16>(o.z / lsum);
-    dst[3] = from_f32<bf16>(o.w / lsum);
   }
 }
 
@@ -350,6 +372,22 @@ cudaError_t launch_partial(const AttnArgs& a, const AttnPlan& p, char* ws, cudaS
   return cudaGetLastError();
 }
 
+// One wave of combine CTAs on the current device: SMs times the resident CTAs of 256 threads
+// (cached per device ordinal).
+int combine_grid() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1216;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_combine_kernel, kCombineThreads, 0) != cudaSuccess ||
+      sms * per_sm <= 0)
+    return 1216;
+  if (dev >= 0 && dev < 64) cached[dev] = sms * per_sm;
+  return sms * per_sm;
+}
+
 }  // namespace
 
 size_t attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int block_size) {
@@ -360,14 +398,13 @@ cudaError_t launch_tree_attn(const AttnArgs& a, void* workspace, size_t workspac
   const AttnPlan p = plan_attn(a.B, a.N, a.Hq, a.Hkv, a.hd, a.max_blocks, a.block_size);
   if (workspace_bytes < p.total) return cudaErrorInvalidValue;
   char* ws = static_cast<char*>(workspace);
-  attn_check_kernel<<<a.B, 128, 0, s>>>(a);
   RopeTable tab;
   for (int c = 0; c < a.hd / 2; ++c) {
     const double inv = pow((double)a.rope_theta, -2.0 * c / a.hd);
     tab.inv[c].x = (float)inv;
     tab.inv[c].y = (float)(inv - (double)tab.inv[c].x);
   }
-  attn_rope_kernel<<<a.B * a.N, 128, 0, s>>>(a, reinterpret_cast<bf16*>(ws + p.off_qrot), tab);
+  attn_rope_kernel<<<a.B * a.N, 256, 0, s>>>(a, reinterpret_cast<bf16*>(ws + p.off_qrot), tab);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (attn_tc_supported(a))
@@ -377,9 +414,11 @@ cudaError_t launch_tree_attn(const AttnArgs& a, void* workspace, size_t workspac
   else if (a.hd == 128) e = launch_partial<128>(a, p, ws, s);
   else e = launch_partial<256>(a, p, ws, s);
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<a.B * a.N, kCombineThreads, 2 * a.Hq * sizeof(float), s>>>(
+  const int wave = combine_grid();
+  const int per_node = a.B * a.N >= wave ? 1 : 0;
+  attn_combine_kernel<<<per_node ? a.B * a.N : wave, kCombineThreads, 0, s>>>(
       a, reinterpret_cast<const float*>(ws + p.off_ml), reinterpret_cast<const float*>(ws + p.off_acc), p.chunk,
-      p.nsplit);
+      p.nsplit, per_node);
   return cudaGetLastError();
 }
 
