@@ -53,6 +53,24 @@ def test_ragged_prefixes_and_sizes(hd):
     _check_attn(case)
 
 
+def test_single_row_tile_at_head_dim_256():
+    """At most 128 query rows per KV head (20 nodes x 4 heads): the single-CTA tensor-core
+    partial, at head dim 256, with prefixes that end inside a key tile."""
+    rng = np.random.default_rng(7)
+    trees = [W.random_tree(20, rng) for _ in range(3)]
+    case = W.attn_case(trees, [0, 130, 700], Hq=8, Hkv=2, hd=256, seed=7)
+    _check_attn(case)
+
+
+def test_odd_row_tiles_leave_the_last_pair_a_padding_peer():
+    """Three tiles of query rows per KV head (70 nodes x 4 heads = 280 rows): the second CTA
+    pair's peer holds no row, and still loads its key and value halves."""
+    rng = np.random.default_rng(8)
+    trees = [W.random_tree(70, rng) for _ in range(2)]
+    case = W.attn_case(trees, [5, 333], Hq=8, Hkv=2, hd=128, seed=8)
+    _check_attn(case)
+
+
 @pytest.mark.parametrize("n", [1, 2, 3])
 def test_tiny_trees(n):
     case = W.attn_case([W.chain(n), [-1] * n], [5, 16], Hq=2, Hkv=1, hd=64, seed=n)

@@ -35,19 +35,22 @@ AttnPlan plan_attn(int B, int N, int Hq, int Hkv, int hd, int max_blocks, int bs
   AttnPlan p;
   const long long slots = (long long)max_blocks * bs;
   const long long work = (long long)B * Hkv * slots;
-  // Whole sequences as items when they alone give at least four waves of partial CTAs on a
-  // 152-SM GPU (then only sequences past 16384 keys split); otherwise about 152 CTAs -- items
-  // times the tiles of 128 query rows each item has, rounded up to CTA pairs, one per SM -- but
-  // no chunk longer than 6912 keys, so that sequences of unequal length still spread evenly.
-  // A partial CTA's set-up and pipeline fill cost about as much as several key tiles, so long
-  // chunks pay until the longest ones make the tail; a sweep over 1536 .. 152 CTAs and caps of
-  // 6912 .. 32768 keys picked these.  The chunk count comes first and the capacity is then
-  // split evenly, so no chunk is a short remainder.  The plan depends on the sizes alone, and
-  // so does the workspace size.
+  // Items with one tile of 128 query rows run on single CTAs: about 1536 of them, ten per SM,
+  // chunks of 128 .. 8192 keys (a sweep over 512 .. 2048 items picked it).  Items with more row
+  // tiles run on CTA pairs, whose set-up and pipeline fill cost about as much as several key
+  // tiles, so they take far fewer, longer chunks: whole sequences when those alone give at least
+  // four waves of CTAs on a 152-SM GPU (then only sequences past 16384 keys split), otherwise
+  // about 152 CTAs with no chunk longer than 6912 keys, so that sequences of unequal length
+  // still spread evenly (a sweep over 1536 .. 152 CTAs and caps of 6912 .. 32768 keys picked
+  // these).  The chunk count comes first and the capacity is then split evenly, so no chunk is
+  // a short remainder.  The plan depends on the sizes alone, and so does the workspace size.
   const long long mtiles = ((long long)(Hq / Hkv) * N + 127) / 128;
   const long long whole_ctas = (long long)B * Hkv * 2 * ((mtiles + 1) / 2);
   long long chunk;
-  if (whole_ctas >= 4 * 152) {
+  if (mtiles == 1) {
+    chunk = (work + 1535) / 1536;
+    if (chunk > 8192) chunk = 8192;
+  } else if (whole_ctas >= 4 * 152) {
     chunk = 16384;
   } else {
     chunk = (work * mtiles + 151) / 152;

@@ -1,21 +1,14 @@
-// Split-KV tree attention partials on the 5th-generation tensor cores (bf16, head dim 128/256).
+// Split-KV tree attention partials on the 5th-generation tensor cores (bf16, head dim 128/256),
+// run by pairs of CTAs on pairs of SMs with M = 256 MMAs (cta_group::2).
 //
 // Same contract as the CUDA-core partial kernel in tree_attn.cu (handbook chapter
-// 树形草稿与 EAGLE, §实现, forward_with_mask): one CTA takes one (sequence, KV head, key chunk,
-// tile of 128 query rows) -- query rows are (node, group member) pairs that share the KV head --
-// and leaves the chunk's running max, sum and unnormalised output per row for the combine
-// kernel.  Roles inside the CTA:
-//   warp 4      TMA producer: the rotated queries once, then K and V tiles of 64 keys (four
-//               16-token pages per tile, reached through the block table) into a 2-stage ring;
-//   warp 5      MMA issuer: S = Q K^T (M=128, N=64, K=head dim) into one of two TMEM S buffers,
-//               then O += P V (M=128, N=head dim, K=64, V read as an MN-major operand) into
-//               the TMEM accumulator;
-//   warps 0-3   softmax, one query row per thread (TMEM lane = row): tree mask on the node
-//               slots, running max in log2 units, P = 2^(s - m) in bf16 into shared memory.
-// The running max is raised lazily: only when a row's tile max exceeds it by more than 2^8,
-// in which case the warp rescales its rows of O in TMEM after the previous PV has completed.
-// Keys past the chunk end are masked; V rows past the sequence end are zeroed in shared memory
-// before PV, so unused cache contents never reach the accumulator.
+// 树形草稿与 EAGLE, §实现, forward_with_mask): for one (sequence, KV head, key chunk) and the
+// query rows of that KV head -- (node, group member) pairs -- the kernel leaves the chunk's
+// running max, sum and unnormalised output per row for the combine kernel.  The tree mask is
+// applied on the node slots, the running max is kept in log2 units and raised lazily (only when
+// a tile's max exceeds it by more than 2^8, the output in tensor memory then rescaled), and
+// value rows past the sequence end are zeroed in shared memory before PV so that unused cache
+// contents never reach the accumulator.
 #include "tv_async.cuh"
 #include "tv_common.cuh"
 #include "tv_internal.h"
@@ -25,11 +18,22 @@
 namespace tv {
 namespace {
 
-constexpr int KT = 64;            // keys per tile
-constexpr int kRows = 128;        // query rows per CTA
-constexpr int kThreads = 192;     // warps 0-3 softmax, warp 4 TMA, warp 5 MMA
+constexpr int kRows = 128;        // query rows per CTA (TMEM lanes)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale = 8.0f;  // log2 headroom of the lazily raised running max
+
+// ---------------------------------------------------------------------------------------------
+// Single-CTA form, for items with one tile of query rows (where a pair would leave one SM's
+// softmax idle): one CTA takes one (sequence, KV head, key chunk, tile of 128 query rows) and
+// runs M = 128 MMAs on key tiles of 64.
+//   warp 4      TMA producer: the rotated queries once, then K and V tiles of 64 keys (four
+//               16-token pages per tile, reached through the block table) into a 2-stage and
+//               a 3-stage ring;
+//   warp 5      MMA issuer: S = Q K^T (M=128, N=64, K=head dim) into one of two TMEM S buffers,
+//               then O += P V (M=128, N=head dim, K=64, V read as an MN-major operand);
+//   warps 0-3   softmax, one query row per thread (TMEM lane = row).
+constexpr int KT = 64;            // keys per tile
+constexpr int kThreads = 192;     // warps 0-3 softmax, warp 4 TMA, warp 5 MMA
 constexpr int kKStages = 2;       // key tiles in the ring
 constexpr int kVStages = 3;       // value tiles in the ring
 
@@ -386,11 +390,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// CTA-pair form.  Two CTAs on two SMs take query-row tiles 2p (rank 0) and 2p + 1 (rank 1) of one
-// (sequence, KV head, key chunk) and run M = 256 MMAs over both, on key tiles of 128.  A key
-// tile's 128 keys split 64 per CTA and a value tile's head dim splits in halves, so each SM
-// loads half of every K/V tile and the pair reads the chunk once; the single-CTA form above
-// reads it once per row tile.  S = Q K^T runs with N = 128: an MMA of N = 64 costs about as
+// Two CTAs on two SMs take query-row tiles 2p (rank 0) and 2p + 1 (rank 1) of one (sequence,
+// KV head, key chunk) and run M = 256 MMAs over both, on key tiles of 128.  A key tile's 128
+// keys split 64 per CTA and a value tile's head dim splits in halves, so each SM loads half of
+// every K/V tile and the pair reads the chunk once (one CTA per row tile would read it once per
+// row tile).  S = Q K^T runs with N = 128: an MMA of N = 64 costs about as
 // much as one of N = 128 here, since both read the same A slice.
 //   rank 0, warp 5   MMA issuer for the pair: S = Q K^T (M=256, N=128) and O += P V (M=256, N=hd);
 //                    each commit arrives on the barrier in both CTAs;
@@ -926,6 +930,8 @@ cudaError_t launch_t(const AttnArgs& a, const void* qrot, float* ml, float* acc,
 
 }  // namespace
 
+int attn_tc_row_tiles(const AttnArgs& a) { return (a.Hq / a.Hkv * a.N + kRows - 1) / kRows; }
+
 bool attn_tc_supported(const AttnArgs& a) {
   const int G = a.Hq / a.Hkv;
   return (a.hd == 128 || a.hd == 256) && G >= 1 && G <= 128 && (128 % G) == 0 && a.block_size == 16;
@@ -934,6 +940,9 @@ bool attn_tc_supported(const AttnArgs& a) {
 cudaError_t launch_attn_partial_tc(const AttnArgs& a, const void* qrot, float* ml, float* acc, int chunk,
                                    int nsplit, cudaStream_t s) {
   if (chunk % PKT) return cudaErrorInvalidValue;
+  if (attn_tc_row_tiles(a) == 1)
+    return a.hd == 128 ? launch_t<128>(a, qrot, ml, acc, chunk, nsplit, s)
+                       : launch_t<256>(a, qrot, ml, acc, chunk, nsplit, s);
   return a.hd == 128 ? launch_pair_t<128>(a, qrot, ml, acc, chunk, nsplit, s)
                      : launch_pair_t<256>(a, qrot, ml, acc, chunk, nsplit, s);
 }

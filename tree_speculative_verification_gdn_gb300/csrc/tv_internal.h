@@ -128,6 +128,8 @@ int tree_attn_check_args(const void* q, const void* k_new, const void* v_new, co
 // Split-KV partials on the tensor cores (head dim 128 or 256, Hq/Hkv dividing 128); the
 // CUDA-core partial kernel covers every other supported shape.
 bool attn_tc_supported(const AttnArgs& a);
+// Tiles of 128 query rows per (sequence, KV head): one runs on single CTAs, more on CTA pairs.
+int attn_tc_row_tiles(const AttnArgs& a);
 cudaError_t launch_attn_partial_tc(const AttnArgs& a, const void* qrot, float* ml, float* acc, int chunk,
                                    int nsplit, cudaStream_t s);
 cudaError_t launch_tree_attn(const AttnArgs& a, void* workspace, size_t workspace_bytes,
