@@ -280,8 +280,8 @@ class Round:
         self.rows = ["tree_prepare", "fork_verify", "fork_materialize", "accept_walk", "fork_commit", "wy_verify",
                      "wy_commit", "tree_attn", "kv_compact"]
         # tree prepare; per layer the fork's two passes and the TreeWY verify; one commit launch per
-        # mode for the whole stack; two accept walks; four attention kernels; the compaction
-        self.launches_per_step = 1 + layers * 3 + 2 + 2 + 4 + 1
+        # mode for the whole stack; two accept walks; three attention kernels; the compaction
+        self.launches_per_step = 1 + layers * 3 + 2 + 2 + 3 + 1
 
     def step(self, ev=None, io=None):
         """One verify round.  ``ev``: optional dict row -> list of (start, end, calls) entries.
