@@ -398,13 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // much as one of N = 128 here, since both read the same A slice.
 //   rank 0, warp 5   MMA issuer for the pair: S = Q K^T (M=256, N=128) and O += P V (M=256, N=hd);
 //                    each commit arrives on the barrier in both CTAs;
-//   rank 1, warp 5   relay: tells rank 0 when this CTA's K and V tiles have landed, zeroing
+//   rank 1, warp 5   relay: tells rank 0 when this CTA's Q, K and V tiles have landed, zeroing
 //                    value rows past the sequence end first;
-//   warps 4 and 6    TMA producers of the CTA's own key and value halves, apart, so a value
-//                    load never waits behind a key stage;
-//   warps 0-3        each thread writes its query row into the 128-byte-swizzled Q tile, then
-//                    runs the softmax of that row: the tile's max over both 64-key halves
-//                    first, then P half by half; rank 1 arrives on rank 0's barriers.
+//   warps 4 and 6    TMA producers of the CTA's own Q tile and key half (warp 4) and value half
+//                    (warp 6), apart, so a value load never waits behind a key stage;
+//   warps 0-3        softmax, one query row per thread, the tile's 128 scores in registers;
+//                    rank 1 arrives on rank 0's barriers.  At the end each thread moves its
+//                    output row from tensor memory into the (then idle) stage region and copies
+//                    it out with one bulk copy.
 // Every wait is bounded; a CTA that gives up raises the abort flag in both CTAs, and both still
 // reach the closing cluster barrier and free the pair's tensor memory together.
 constexpr int PKT = 128;  // keys per tile
@@ -429,7 +430,7 @@ struct PairLayout {
 };
 
 struct PairBars {
-  uint64_t q_ready;
+  uint64_t q_land, q_peer;
   uint64_t k_land[4], k_peer[4], k_empty[4];
   uint64_t v_land[6], v_peer[6], v_empty[6];
   uint64_t s_full[2], p_full[2], pv_done[2];
@@ -456,8 +457,8 @@ __device__ __forceinline__ bool mbar_try_cluster(uint64_t* bar, uint32_t parity)
 
 template <int HD>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
-    attn_partial_pair_kernel(AttnArgs a, const __nv_bfloat16* __restrict__ qrot, float* __restrict__ ml,
-                             float* __restrict__ acc, int chunk, int nsplit, int npairs, int npt,
+    attn_partial_pair_kernel(AttnArgs a, float* __restrict__ ml, float* __restrict__ acc, int chunk, int nsplit,
+                             int npairs, int npt, const __grid_constant__ CUtensorMap mQ,
                              const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV) {
   using L = PairLayout<HD>;
   constexpr int KS = L::KS, VS = L::VS;
@@ -487,7 +488,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 
   if (tid == 0) {
     const uint32_t pair_warps = (uint32_t)(warps_of(2 * pair) + warps_of(2 * pair + 1));
-    mbar_init(&bar.q_ready, pair_warps);  // one arrival per softmax warp with query rows
+    mbar_init(&bar.q_land, 1);
+    mbar_init(&bar.q_peer, 1);
     for (int s = 0; s < KS; ++s) {
       mbar_init(&bar.k_land[s], 1);
       mbar_init(&bar.k_peer[s], 1);
@@ -545,6 +547,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const int* table = a.block_table + (size_t)b * a.max_blocks;
     auto wait_all = [&](uint64_t* w, uint32_t parity) { return __all_sync(0xffffffffu, pwait(w, parity)); };
     if (warp == 4) {
+      if (lane == 0) {  // this CTA's 128 query rows (padding rows past N read as zeros)
+        mbar_arrive_expect_tx(&bar.q_land, (uint32_t)(HD * G * npt * 2));
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_5d(sm + L::Q + c * L::QCHUNK, &mQ, c * 64, 0, kvh, mt * npt, b, &bar.q_land);
+      }
       auto kpage = [&](int j) {
         return (lane < 4 && j < T) ? table[min((lo + j * PKT) / 16 + 4 * (int)rank + lane, last_lb)] : 0;
       };
@@ -585,7 +592,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(256, PKT), idO = idesc_bf16_f32(256, HD, true);
       const uint32_t q0 = smem_addr(sm + L::Q);
-      bool ok = pwait(&bar.q_ready, 0);
+      bool ok = pwait(&bar.q_land, 0) && pwait(&bar.q_peer, 0);
       int ns = 0, np = 0;
       uint32_t idle = 0;
       while (ok && np < T) {
@@ -641,7 +648,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ relay (rank 1, whole warp)
-    bool ok = true;
+    bool ok = __all_sync(0xffffffffu, pwait(&bar.q_land, 0));
+    if (ok && lane == 0) mbar_arrive_cluster_relaxed(to_rank0(&bar.q_peer));
     int nk = 0, nv = 0;
     uint32_t idle = 0;
     while (ok && (nk < T || nv < T)) {
@@ -690,26 +698,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const bool warp_idle = warp >= active_warps;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     bool ok = true;
-    if (!warp_idle) {
-      // this row's rotated query (zeros for padding rows) into the Q tile that the MMA reads
-      const uint4* qrow =
-          reinterpret_cast<const uint4*>(qrot + (((size_t)b * N + (active ? node : 0)) * a.Hq + kvh * G + g) * HD);
-#pragma unroll 1
-      for (int c = 0; c < HD / 64; ++c) {
-        unsigned char* row = sm + L::Q + c * L::QCHUNK + (r / 8) * 1024 + (r % 8) * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(row + ((u ^ (r % 8)) << 4)) = active ? qrow[c * 8 + u] : make_uint4(0, 0, 0, 0);
-      }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        if (rank == 0)
-          mbar_arrive(&bar.q_ready);
-        else
-          mbar_arrive_cluster(to_rank0(&bar.q_ready));
-      }
-    }
     uint32_t mb[TV_MAX_NODES / 32];
 #pragma unroll
     for (int w = 0; w < TV_MAX_NODES / 32; ++w) mb[w] = 0;
@@ -829,20 +817,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
     if (ok && !warp_idle && __all_sync(0xffffffffu, pwait(&bar.pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1))) {
       tc_fence_after();
+      // Every key and value stage has been consumed: the row goes through the stage region,
+      // padded by 16 bytes per row so that a warp's 16-byte stores meet all banks, and out with
+      // one bulk copy.
       const size_t row = (((size_t)b * a.Hkv + kvh) * nsplit + split) * R + (size_t)node * G + g;
+      float* stage = reinterpret_cast<float*>(sm + L::K0) + (size_t)r * (HD + 4);
 #pragma unroll 1
-      for (int c0 = 0; c0 < HD; c0 += 16) {
-        float o16[16];
-        tmem_ld16(tO + lane_base + c0, o16);
-        if (active) {
-          float4* dst = reinterpret_cast<float4*>(acc + row * HD + c0);
+      for (int c0 = 0; c0 < HD; c0 += 64) {
+        uint32_t o[64];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_float4(o16[4 * e], o16[4 * e + 1], o16[4 * e + 2], o16[4 * e + 3]);
-        }
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld16_nowait(tO + lane_base + c0 + q4 * 16, o + q4 * 16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          *reinterpret_cast<uint4*>(stage + c0 + 4 * e) = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
       }
+      fence_proxy_async();
       if (active) {
+        bulk_s2g(acc + row * HD, stage, HD * 4);
+        bulk_commit();
         ml[row * 2] = m_used;
         ml[row * 2 + 1] = l;
+        bulk_wait_read<0>();
       }
     }
   }
@@ -855,9 +851,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   }
   __syncthreads();
   if (*abort) {
-    if (warp == 4 && lane == 0)
+    if (warp == 4 && lane == 0) {
+      mbar_wait(&bar.q_land, 0);
       for (int j = issued_k - KS < 0 ? 0 : issued_k - KS; j < issued_k; ++j)
         mbar_wait(&bar.k_land[j % KS], (j / KS) & 1);
+    }
     if (warp == 6 && lane == 0)
       for (int j = issued_v - VS < 0 ? 0 : issued_v - VS; j < issued_v; ++j)
         mbar_wait(&bar.v_land[j % VS], (j / VS) & 1);
@@ -877,7 +875,15 @@ cudaError_t launch_pair_t(const AttnArgs& a, const void* qrot, float* ml, float*
   const int npt = kRows / G;
   const int mtiles = (a.N + npt - 1) / npt;
   const int npairs = (mtiles + 1) / 2;
-  CUtensorMap mK, mV;
+  CUtensorMap mQ, mK, mV;
+  {
+    // rotated queries [B][N][Hkv][G][hd]
+    const cuuint64_t dims[5] = {(cuuint64_t)HD, (cuuint64_t)G, (cuuint64_t)a.Hkv, (cuuint64_t)a.N, (cuuint64_t)a.B};
+    const cuuint64_t strides[4] = {(cuuint64_t)HD * 2, (cuuint64_t)G * HD * 2, (cuuint64_t)a.Hq * HD * 2,
+                                   (cuuint64_t)a.N * a.Hq * HD * 2};
+    const cuuint32_t box[5] = {64, (cuuint32_t)G, 1, (cuuint32_t)npt, 1};
+    if (!make_map_bf16_sw128(&mQ, qrot, 5, dims, strides, box)) return cudaErrorInvalidValue;
+  }
   {
     const cuuint64_t dims[4] = {(cuuint64_t)HD, 16, (cuuint64_t)a.Hkv, (cuuint64_t)a.num_blocks};
     const cuuint64_t strides[3] = {(cuuint64_t)HD * 2, (cuuint64_t)16 * HD * 2, (cuuint64_t)a.Hkv * 16 * HD * 2};
@@ -890,8 +896,7 @@ cudaError_t launch_pair_t(const AttnArgs& a, const void* qrot, float* ml, float*
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(nsplit * npairs * 2 * a.Hkv, a.B);
-  kern<<<grid, kPairThreads, smem, s>>>(a, static_cast<const __nv_bfloat16*>(qrot), ml, acc, chunk, nsplit, npairs,
-                                        npt, mK, mV);
+  kern<<<grid, kPairThreads, smem, s>>>(a, ml, acc, chunk, nsplit, npairs, npt, mQ, mK, mV);
   return cudaGetLastError();
 }
 
