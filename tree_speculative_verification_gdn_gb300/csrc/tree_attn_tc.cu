@@ -427,6 +427,8 @@ struct PairLayout {
   static constexpr uint32_t TOTAL = BARS + 512;
   // O [0, HD), two S buffers [HD, HD + 2 PKT) (P over the first PKT / 2 columns of each)
   static constexpr uint32_t TMEM_COLS = (HD + 2 * PKT <= 256) ? 256 : 512;
+  static_assert(KS <= 4 && VS <= 6, "the barrier arrays hold the rings");
+  static_assert(kRows * (HD + 4) * 4 <= BARS - K0, "the padded output rows fit the stage region");
 };
 
 struct PairBars {
