@@ -24,6 +24,11 @@ Sources
   entries all come from one other block, each at its own row, takes that block by an exchange
   of the two table entries; every other kept entry is moved as above.  The logical contents
   of slots [0, new length) are those of the moving compaction.
+* Query operand precision: the pages' attention runs on the model's bf16 tensors, and a
+  tensor-core score product takes the rotated query as a bf16 operand.  Everything here is
+  fp64 by default; ``query_bf16=True`` rounds the rotated query, and nothing else, to bf16
+  (nearest, ties to even) before the score product, so that a comparison can separate the
+  effect of that one rounding from every other error.
 """
 from __future__ import annotations
 
@@ -59,8 +64,16 @@ def physical_slot(table_row: np.ndarray, s: int, block_size: int = 16) -> int:
     return int(table_row[s // block_size]) * block_size + s % block_size
 
 
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """x rounded to the nearest bf16 value (8 significant bits, ties to even), as fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    mant, expo = np.frexp(x)                    # x = mant * 2^expo, 0.5 <= |mant| < 1
+    return np.ldexp(np.round(mant * 256.0) / 256.0, expo)   # np.round: half to even
+
+
 def attend_one(q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, prefix_k: np.ndarray,
-               prefix_v: np.ndarray, parents, theta: float, sm_scale: float | None = None):
+               prefix_v: np.ndarray, parents, theta: float, sm_scale: float | None = None,
+               query_bf16: bool = False):
     """One sequence: ``q [N,Hq,hd]``, ``k_new, v_new [N,Hkv,hd]``, ``prefix_k, prefix_v
     [P,Hkv,hd]`` (prefix keys already rotated).  Returns ``o [N,Hq,hd]`` and the rotated node
     keys ``[N,Hkv,hd]`` that the cache receives."""
@@ -70,6 +83,8 @@ def attend_one(q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, prefix_k: np
     scale = hd ** -0.5 if sm_scale is None else sm_scale
     pos = P + np.asarray(depths(parents))
     qr = rope(q, pos, theta)
+    if query_bf16:
+        qr = bf16_round(qr)
     kr = rope(k_new, pos, theta)
     K = np.concatenate([prefix_k, kr], axis=0)
     V = np.concatenate([prefix_v, v_new], axis=0)
@@ -87,7 +102,7 @@ def attend_one(q: np.ndarray, k_new: np.ndarray, v_new: np.ndarray, prefix_k: np
     return o, kr
 
 
-def tree_attention(case_f64: dict, batch=None):
+def tree_attention(case_f64: dict, batch=None, query_bf16: bool = False):
     """Paged form.  ``case_f64`` holds fp64 numpy arrays ``q, k_new, v_new, k_cache, v_cache``
     and int arrays ``block_table, prefix_len, parents`` plus ``rope_theta``.  Returns
     ``o [B,N,Hq,hd]`` (NaN rows for sequences not computed) and the rotated node keys."""
@@ -104,7 +119,7 @@ def tree_attention(case_f64: dict, batch=None):
         pv = logical_rows(case_f64["v_cache"], row, P, bs)
         o[b], kr_all[b] = attend_one(q[b], case_f64["k_new"][b], case_f64["v_new"][b], pk, pv,
                                      case_f64["parents"][b], case_f64["rope_theta"],
-                                     case_f64.get("sm_scale"))
+                                     case_f64.get("sm_scale"), query_bf16)
     return o, kr_all
 
 

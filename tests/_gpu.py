@@ -14,6 +14,10 @@ Tolerance of the floating-point outputs:
     own(ref) is that one rounding and nothing more; every other error must fit in 2e-2 * RMS.
     Where the reference is itself a bf16 result of the library (two kernels compared with each
     other), each side carries its own rounding: own(ref) = 2 * 2^-8 * |ref|.
+  * Attention outputs are compared twice (assert_attention_close): with the oracle whose rotated
+    query is rounded to bf16 -- the operand precision of the tensor-core score product -- under
+    the rule above, and with the plain fp64 oracle under the rule above plus, per element, the
+    change that this one rounding makes to the oracle's own result.
 Integer outputs are compared exactly.
 """
 from __future__ import annotations
@@ -52,14 +56,15 @@ def max_err(got, ref) -> float:
     return float(np.abs(g - np.asarray(ref, dtype=np.float64)).max())
 
 
-def _record(what: str, io: str, own: bool, g: np.ndarray, r: np.ndarray, diff: np.ndarray, own_k: float) -> dict:
+def _record(what: str, io: str, own: bool, g: np.ndarray, r: np.ndarray, diff: np.ndarray, own_k: float,
+            extra=0.0) -> dict:
     scale = rms(r)
     m = dict(what=what, io=io, stored_bf16=own, own_k=own_k, n=int(r.size), rms_ref=scale, max_abs=float(diff.max()))
     if io != "f32" and scale > 0:
         strict = BF16_REL * scale
         m.update(max_over_rms=float(diff.max()) / scale, rms_err_over_rms=rms(g - r) / scale,
                  n_over_strict=int((diff > strict).sum()),
-                 worst_vs_bound=float((diff / (strict + (own_k * np.abs(r) if own else 0.0))).max()))
+                 worst_vs_bound=float((diff / (strict + (own_k * np.abs(r) if own else 0.0) + extra)).max()))
     MARGINS.append(m)
     path = os.environ.get("TV_PARITY_MARGINS")
     if path:
@@ -68,11 +73,13 @@ def _record(what: str, io: str, own: bool, g: np.ndarray, r: np.ndarray, diff: n
     return m
 
 
-def assert_close(got, ref, io: str, what: str, stored: str | None = None, ref_rounded: bool = False) -> None:
+def assert_close(got, ref, io: str, what: str, stored: str | None = None, ref_rounded: bool = False,
+                 extra=None) -> None:
     """``io``: the workload's I/O type ("f32" or "bf16"), which picks the rule above.
     ``stored``: how the kernel stored the compared values ("bf16" or "f32"); taken from the
     tensor's dtype when ``got`` is a torch tensor, and required for numpy input under bf16 I/O.
-    ``ref_rounded``: the reference is another kernel's bf16 result (two roundings allowed)."""
+    ``ref_rounded``: the reference is another kernel's bf16 result (two roundings allowed).
+    ``extra``: a per-element allowance added to the bf16 bound (see assert_attention_close)."""
     if isinstance(got, torch.Tensor):
         st = "bf16" if got.dtype == torch.bfloat16 else "f32"
         assert stored in (None, st), f"{what}: stored={stored} but the tensor is {got.dtype}"
@@ -89,7 +96,8 @@ def assert_close(got, ref, io: str, what: str, stored: str | None = None, ref_ro
     diff = np.abs(g - r)
     own = stored == "bf16"
     own_k = (2.0 if ref_rounded else 1.0) * BF16_OWN
-    _record(what, io, own, g, r, diff, own_k)
+    ex = 0.0 if extra is None else np.asarray(extra, dtype=np.float64)
+    _record(what, io, own, g, r, diff, own_k, ex)
     if io == "f32":
         err = float(diff.max())
         assert err <= 1e-4, f"{what}: max abs err {err:.3e} > 1e-4"
@@ -97,11 +105,25 @@ def assert_close(got, ref, io: str, what: str, stored: str | None = None, ref_ro
     scale = rms(r)
     rel = rms(g - r) / scale if scale > 0 else rms(g - r)
     assert rel <= BF16_REL, f"{what}: RMS err / RMS(ref) = {rel:.3e} > {BF16_REL}"
-    bound = BF16_REL * scale + (own_k * np.abs(r) if own else 0.0)
+    bound = BF16_REL * scale + (own_k * np.abs(r) if own else 0.0) + ex
     worst = np.unravel_index(np.argmax(diff - bound), diff.shape)
     assert (diff <= bound).all(), (f"{what}: element {worst}: |err| {diff[worst]:.3e} > "
                                    f"{float(np.broadcast_to(bound, diff.shape)[worst]):.3e} "
                                    f"(ref {r[worst]:.3e}, RMS {scale:.3e}, stored {stored})")
+
+
+def assert_attention_close(got, case_f64: dict, seqs, what: str = "attention o"):
+    """The attention outputs ``got[seqs]`` against the oracle (see the module docstring): within
+    the bf16 rule of the oracle on the bf16-rounded rotated query, and within that rule plus the
+    oracle's own change under that rounding of the plain fp64 oracle.  Returns the plain
+    oracle's (outputs, rotated node keys)."""
+    from oracle import attention as A
+    o_ref, kr_ref = A.tree_attention(case_f64, batch=seqs)
+    o_rq, _ = A.tree_attention(case_f64, batch=seqs, query_bf16=True)
+    g = got[seqs]
+    assert_close(g, o_rq[seqs], "bf16", what + " (bf16 query)")
+    assert_close(g, o_ref[seqs], "bf16", what, extra=np.abs(o_rq[seqs] - o_ref[seqs]))
+    return o_ref, kr_ref
 
 
 def margin_summary() -> list[str]:

@@ -218,3 +218,38 @@ def test_block_boundary_prefix_lengths(hd):
         f = _f64_case(case)
         o, _ = A.tree_attention(f)
         assert np.isfinite(o).all()
+
+
+def test_bf16_round_is_round_to_nearest_even_at_8_significant_bits():
+    # ties go to the even neighbour, anything past a tie goes up
+    vals = np.array([1 + 2.0**-8, 1 + 3 * 2.0**-8, -(1 + 2.0**-8), 1 + 2.0**-8 + 2.0**-20, 3 * 2.0**-9, 255.0, 255.5])
+    want = np.array([1.0, 1 + 2.0**-6, -1.0, 1 + 2.0**-7, 3 * 2.0**-9, 255.0, 256.0])
+    assert np.array_equal(A.bf16_round(vals), want)
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal(20000) * 10.0 ** rng.uniform(-6, 6, 20000)
+    r = A.bf16_round(x)
+    assert (np.abs(r - x) <= 2.0**-8 * np.abs(x)).all()          # at most half an ulp
+    assert np.array_equal(A.bf16_round(r), r)                      # representable: a fixed point
+    e = np.floor(np.log2(np.abs(r)))
+    assert np.array_equal(np.ldexp(r, (7 - e).astype(int)) % 1, np.zeros_like(r))  # 8 significant bits
+
+
+def test_bf16_query_is_the_plain_result_where_the_query_is_not_rotated():
+    # one node and no prefix: the query sits at position 0, where the rotation is the identity,
+    # and a bf16 input is already representable, so rounding the rotated query changes nothing
+    f = _f64_case(W.attn_case([[-1]], [0], Hq=4, Hkv=2, hd=64, seed=3))
+    o, _ = A.tree_attention(f)
+    o_rq, _ = A.tree_attention(f, query_bf16=True)
+    assert np.array_equal(o, o_rq)
+
+
+def test_bf16_query_moves_the_output_by_a_few_hundredths_of_its_rms():
+    # rotated queries off position 0 are not bf16 values: the option acts, and by no more than
+    # about the half-ulp rounding of the query can move a softmax average
+    rng = np.random.default_rng(4)
+    f = _f64_case(W.attn_case([W.random_tree(30, rng)], [200], Hq=4, Hkv=2, hd=128, seed=4))
+    o, _ = A.tree_attention(f)
+    o_rq, _ = A.tree_attention(f, query_bf16=True)
+    d = np.abs(o_rq - o)
+    rms = np.sqrt(np.mean(o ** 2))
+    assert d.max() > 0 and d.max() < 0.05 * rms
