@@ -24,8 +24,8 @@ Sources
   entries all come from one other block, each at its own row, takes that block by an exchange
   of the two table entries; every other kept entry is moved as above.  The logical contents
   of slots [0, new length) are those of the moving compaction.
-* Query operand precision: the pages' attention runs on the model's bf16 tensors, and a
-  tensor-core score product takes the rotated query as a bf16 operand.  Everything here is
+* Query operand precision: the handbook chapter's ``forward_with_mask`` runs on the model's
+  bf16 tensors, and a tensor-core score product takes the rotated query as a bf16 operand.  Everything here is
   fp64 by default; ``query_bf16=True`` rounds the rotated query, and nothing else, to bf16
   (nearest, ties to even) before the score product, so that a comparison can separate the
   effect of that one rounding from every other error.
