@@ -369,7 +369,9 @@ TV_API int tv_gdn_commit_selective(const int32_t* accepted_path, const int32_t* 
  *                share a workspace must not overlap in time.
  *   err          [B] int32                out 0, TV_ERR_BAD_TREE, TV_ERR_CAPACITY
  *                                         (prefix_len + N > max_blocks * block_size or
- *                                         prefix_len < 0) or TV_ERR_BAD_BLOCK
+ *                                         prefix_len < 0), TV_ERR_BAD_BLOCK, or TV_ERR_TIMEOUT
+ *                                         (a bounded device wait gave up; that sequence's
+ *                                         outputs are then unspecified)
  * Supported: hd in {64, 128, 256}; block_size = 16; Hq a multiple of Hkv; B <= 65535.
  * ---------------------------------------------------------------------------------------- */
 TV_API size_t tv_tree_attn_workspace_size(int B, int N, int Hq, int Hkv, int hd, int max_blocks,
